@@ -1,0 +1,457 @@
+"""Benchmark of the truly sparse linear layer on GB300.
+
+Workload (default): W 10000 x 10000 at 90% unstructured sparsity
+(nnz = 10,000,000, support uniform without replacement), fp32, batch 4: the
+layer of the SNACK page's Table 3 / Fig. 3 ("Beyond Masked Sparsity: SNACK
+Enables Truly Sparse Neural Networks on GPU").  One step = one pass of the hot
+path over one batch: forward SpMM (with bias), transposed SpMM (dX) and the
+weight gradient on the support (dW, with db).  The restructure
+(prune_regrow) runs at its own cadence and is timed separately
+(``restructure`` key).
+
+Metric: microseconds per call and achieved HBM GB/s for forward / dX / dW.
+``value`` = algorithmic bytes of the step's three kernels / their summed
+device time, over all ranks (GB/s).  L2 is flushed (a 512 MB write) before
+every kernel, outside the timed interval; each kernel is bracketed by CUDA
+events on the stream it is launched on.
+
+Algorithmic bytes per launch (what each kernel must move at least):
+  forward  nnz*8 (values, cols) + (out+1)*4 (row_ptr) + b*in*4 (X) + b*out*4 (Y) + out*4 (bias)
+  dX       nnz*12 (rows_c, perm, values) + (in+1)*4 (col_ptr) + b*out*4 (dY) + b*in*4 (dX)
+  dW       nnz*8 (cols read, dW written) + (out+1)*4 + b*(in+out)*4 (X, dY) + out*4 (db)
+The contract formula bytes (nnz*12 + b*(in+out)*4, plus nnz*4 for dW) are
+reported beside them as ``formula``.
+
+--impl reference runs the CPU oracle (the plain fp64 reference) on the host
+cores instead, each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s (% of roofline) for fwd/dX/dW at b=1–64"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--out", type=int, default=10000)
+    p.add_argument("--inp", type=int, default=10000)
+    p.add_argument("--sparsity", type=float, default=90)
+    p.add_argument("--batch", type=int, default=4)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="also print one extra JSON object per (sparsity, batch) to stderr")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def op_bytes(out_f, in_f, nnz, b):
+    alg = {
+        "fwd": nnz * 8 + (out_f + 1) * 4 + b * in_f * 4 + b * out_f * 4 + out_f * 4,
+        "dx": nnz * 12 + (in_f + 1) * 4 + b * out_f * 4 + b * in_f * 4,
+        "dw": nnz * 8 + (out_f + 1) * 4 + b * (in_f + out_f) * 4 + out_f * 4,
+    }
+    formula = {
+        "fwd": nnz * 12 + b * (in_f + out_f) * 4,
+        "dx": nnz * 12 + b * (in_f + out_f) * 4,
+        "dw": nnz * 16 + b * (in_f + out_f) * 4,
+    }
+    return alg, formula
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_linear_layer_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_tag, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(kernel_tag)
+    if not e or e.get("workload") != workload or e.get("source_digest") != kernel_source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- reference arm
+def oracle_step_sample(lay, X, dY, rows_lo, rows_hi):
+    """One bounded oracle step: forward, dX and dW restricted to the entries of
+    rows [rows_lo, rows_hi) of the canonical triple."""
+    import oracle
+    o = oracle
+    sel = slice(int(lay["row_ptr"][rows_lo]), int(lay["row_ptr"][rows_hi]))
+    v, r, c = lay["values"][sel], lay["rows"][sel], lay["cols"][sel]
+    o.forward(lay["out"], lay["in"], v, r, c, X, None)
+    o.backward_input(lay["out"], lay["in"], v, r, c, dY)
+    o.backward_weight(lay["out"], lay["in"], r, c, X, dY)
+    return int(sel.stop - sel.start)
+
+
+def run_reference(args, workload, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from sparse_linear_layer_gb300 import synth
+    oracle.build()
+    lay0 = synth.make_layer(args.out, args.inp, args.sparsity, 0.01, 21, 22)
+    can = oracle.canonicalize(args.out, args.inp, lay0.values, lay0.rows, lay0.cols)
+    can["out"], can["in"] = args.out, args.inp
+    b = args.batch
+    X = synth.normal((b, args.inp), 1.0, 23)
+    dY = synth.normal((b, args.out), 1.0, 24)
+    rows_per_step = max(1, args.out // 100)
+    for i in range(args.warmup):
+        lo = (i * rows_per_step) % args.out
+        oracle_step_sample(can, X, dY, lo, min(args.out, lo + rows_per_step))
+    t0 = time.perf_counter()
+    nnz_done = 0
+    for i in range(args.steps):
+        lo = (i * rows_per_step) % args.out
+        nnz_done += oracle_step_sample(can, X, dY, lo, min(args.out, lo + rows_per_step))
+    dt = time.perf_counter() - t0
+    # bytes of the sampled work: entries scale the triple terms; the dense
+    # operands are counted for the rows touched
+    alg, _ = op_bytes(args.out, args.inp, lay0.nnz, b)
+    total_bytes = sum(alg.values()) * (nnz_done / lay0.nnz if lay0.nnz else 0.0)
+    value = total_bytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: forward + dX + dW of the oracle over the entries of "
+                                   f"{rows_per_step} consecutive rows of W (about 1% of the layer), "
+                                   f"batch {b}; rows advance each step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- our arm
+def launches_per_op(n_src, b, max_smem):
+    launches = 0
+    for t0 in range(0, b, 64):
+        bt = min(64, b - t0)
+        bp = 1
+        while bp < bt:
+            bp <<= 1
+        launches += 1 if n_src * bp * 4 <= max_smem else 2
+    return launches
+
+
+def time_cpu_baseline(lay, X, dY, budget_s=12.0, max_steps=25):
+    import oracle
+    oracle.build()
+    can = oracle.canonicalize(lay.out_f, lay.in_f, lay.values, lay.rows, lay.cols)
+    v, r, c = can["values"], can["rows"], can["cols"]
+    steps = 0
+    t0 = time.perf_counter()
+    while steps < max_steps and (time.perf_counter() - t0) < budget_s:
+        oracle.forward(lay.out_f, lay.in_f, v, r, c, X, None)
+        oracle.backward_input(lay.out_f, lay.in_f, v, r, c, dY)
+        oracle.backward_weight(lay.out_f, lay.in_f, r, c, X, dY)
+        steps += 1
+    return steps, time.perf_counter() - t0
+
+
+def run_ours(args, workload, rank, world, local):
+    import numpy as np
+    import torch
+
+    from sparse_linear_layer_gb300 import binding, build, synth
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    out_f, in_f, b = args.out, args.inp, args.batch
+    lay = synth.make_layer(out_f, in_f, args.sparsity, 0.01, 21, 22)
+    nnz = lay.nnz
+    X_h = synth.normal((b, in_f), 1.0, 23)
+    dY_h = synth.normal((b, out_f), 1.0, 24)
+    bias_h = synth.normal(out_f, 0.1, 25)
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    g = binding.SparseLinear(out_f, in_f, td(lay.values), td(lay.rows), td(lay.cols))
+    X, dY, bias = td(X_h), td(dY_h), td(bias_h)
+    Y = torch.empty((b, out_f), device=dev)
+    dX = torch.empty((b, in_f), device=dev)
+    dW = torch.empty(nnz, device=dev)
+    db = torch.empty(out_f, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def fwd():
+        binding.snk_forward(g.handle, X, bias, Y, sh)
+
+    def bwi():
+        binding.snk_backward_input(g.handle, dY, dX, sh)
+
+    def bww():
+        binding.snk_backward_weight(g.handle, X, dY, dW, db, sh)
+
+    ops = [("fwd", fwd), ("dx", bwi), ("dw", bww)]
+    for _ in range(args.warmup):
+        for _, f in ops:
+            flush.zero_()
+            f()
+    torch.cuda.synchronize()
+
+    ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)] for name, _ in ops}
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        smi_id = str(local)
+    with ClockSampler(smi_id) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            for name, f in ops:
+                flush.zero_()
+                e0, e1 = ev[name][i]
+                e0.record(stream)
+                f()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    per_op_ms = {name: [e0.elapsed_time(e1) for e0, e1 in ev[name]] for name, _ in ops}
+    total_ms = sum(sum(v) for v in per_op_ms.values())
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    alg, formula = op_bytes(out_f, in_f, nnz, b)
+    step_bytes = sum(alg.values())
+    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    us = {name: statistics.median(v) * 1e3 for name, v in per_op_ms.items()}
+    p10 = {name: sorted(v)[len(v) // 10] * 1e3 for name, v in per_op_ms.items()}
+    p90 = {name: sorted(v)[(9 * len(v)) // 10] * 1e3 for name, v in per_op_ms.items()}
+    mean_us = {name: sum(v) / len(v) * 1e3 for name, v in per_op_ms.items()}
+    peak, peak_kind = measured_peaks()
+    dom = max(mean_us, key=mean_us.get)
+    achieved = alg[dom] / (mean_us[dom] * 1e-6) / 1e9
+    kernel_tags = {"fwd": "k_spmm_fwd", "dx": "k_spmm_dx", "dw": "k_sddmm"}
+    traffic = committed_traffic(kernel_tags[dom], workload["workload"])
+    roofline = {
+        "bound": "hbm", "kernel": kernel_tags[dom], "achieved": achieved, "peak": peak,
+        "peak_kind": f"hbm_gbs, {peak_kind}", "unit": "GB/s", "frac": achieved / peak,
+        "traffic": traffic, "algorithmic_bytes_per_launch": alg[dom],
+        "per_op": {n: {"us_median": us[n], "us_p10": p10[n], "us_p90": p90[n],
+                       "gbs": alg[n] / (mean_us[n] * 1e-6) / 1e9,
+                       "frac": alg[n] / (mean_us[n] * 1e-6) / 1e9 / peak,
+                       "formula_gbs": formula[n] / (mean_us[n] * 1e-6) / 1e9}
+                   for n in us},
+    }
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        Xp = torch.from_numpy(X_h).pin_memory()
+        dYp = torch.from_numpy(dY_h).pin_memory()
+        Yp = torch.empty((b, out_f)).pin_memory()
+        dXp = torch.empty((b, in_f)).pin_memory()
+        n_e2e = max(10, args.steps // 2)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_e2e)]
+        for i in range(n_e2e + 3):
+            flush.zero_()
+            if i >= 3:
+                evs[i - 3][0].record(stream)
+            X.copy_(Xp, non_blocking=True)
+            dY.copy_(dYp, non_blocking=True)
+            fwd()
+            bwi()
+            bww()
+            Yp.copy_(Y, non_blocking=True)
+            dXp.copy_(dX, non_blocking=True)
+            if i >= 3:
+                evs[i - 3][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(z) for a, z in evs)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * step_bytes * n_e2e / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": (X_h.nbytes + dY_h.nbytes),
+               "d2h_bytes_per_step": b * (out_f + in_f) * 4,
+               "ms_per_step": e2e_ms / n_e2e,
+               "note": "pinned host X, dY copied in; Y, dX copied out; dW stays on the device "
+                       "for the optimizer; L2 flushed before each step only"}
+
+    # ---- restructure (SET cadence work), timed separately
+    restructure = None
+    if rank == 0:
+        torch.cuda.synchronize()
+        reps = 3
+        ts = []
+        for i in range(reps):
+            t0 = time.perf_counter()
+            g.prune_regrow(0.3, 0x5E7 + i)
+            torch.cuda.synchronize()
+            ts.append((time.perf_counter() - t0) * 1e6)
+        restructure = {"op": "prune_regrow", "zeta": 0.3, "us_median_host_timed": statistics.median(ts),
+                       "note": "synchronous call (it reads device counts back); wall-clock µs"}
+
+    max_smem = torch.cuda.get_device_properties(dev).shared_memory_per_block_optin
+    launches = args.steps * (launches_per_op(in_f, b, max_smem) + launches_per_op(out_f, b, max_smem)
+                             + launches_per_op(in_f, b, max_smem))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        steps_c, dt_c = time_cpu_baseline(lay, X_h, dY_h)
+        cpu = {"value": step_bytes * steps_c / dt_c / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{steps_c} full steps (forward + dX + dW, fp64 accumulation) of the same "
+                         f"{out_f}x{in_f} layer, batch {b}, single-threaded"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload,
+            "us_per_call": us, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk.summary(), "restructure": restructure,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    g.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    nnz = None
+    try:
+        from sparse_linear_layer_gb300 import synth
+        nnz = synth.nnz_for(args.out, args.inp, args.sparsity)
+    except Exception:
+        pass
+    workload = {
+        "workload": f"layer{args.out}x{args.inp}_s{args.sparsity:g}_b{args.batch}",
+        "description": f"W {args.out}x{args.inp}, {args.sparsity:g}% uniform random sparsity, fp32, "
+                       f"batch {args.batch}; step = forward (bias) + backward_input + "
+                       f"backward_weight (db)",
+        "out": args.out, "in": args.inp, "sparsity_pct": args.sparsity, "nnz": nnz,
+        "batch": args.batch, "l2": "flushed by a 512 MB write before every kernel, untimed",
+        "parallelism": f"replicas x{world}",
+    }
+    if args.impl == "reference":
+        run_reference(args, workload, rank, world)
+    else:
+        run_ours(args, workload, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

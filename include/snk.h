@@ -1,0 +1,187 @@
+/*
+ * snk.h - C ABI of libsnk, a truly sparse linear layer for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The weight W (out x in) exists only as its non-zeros, a COO triple
+ * (values, rows, cols) in device memory.  The library computes
+ *   forward            Y  = X W^T + b                      (SpMM)
+ *   backward_input     dX = dY W                           (transposed SpMM)
+ *   backward_weight    dW_k = sum_beta dY[beta,r_k] X[beta,c_k], db = 1^T dY
+ *                      (the weight gradient on supp(W) only: an SDDMM)
+ *   prune_regrow       magnitude prune of a fraction zeta, then a seeded
+ *                      uniform regrow of as many new zero-valued entries
+ *                      (nnz unchanged)
+ * with hand-written CUDA kernels.  The caller owns every buffer it passes;
+ * the library owns only the workspace behind the handle.
+ *
+ * Sources (page titles; sections, figures and tables as printed there):
+ *   [SNACK] "Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural
+ *           Networks on GPU"
+ *   [PCSR]  "Padded-CSR: A sparse storage format for dynamic sparse training
+ *           on CPU"
+ *
+ * Common conventions
+ *   - Matrices are row-major fp32: X is [batch, in], Y and dY are
+ *     [batch, out], dX is [batch, in] (the nn.Linear layout of [PCSR]
+ *     sec. 2.2; [PCSR] sec. 6.1 writes the same product features-major).
+ *   - Every pointer argument is a DEVICE pointer on the current CUDA device,
+ *     to contiguous memory.  values/rows/cols and dW must be 16-byte
+ *     aligned; X, Y, dY, dX, bias and db 4-byte aligned.  Violations return
+ *     SNK_ERR_ARG before any work is queued.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous on that stream unless said otherwise.
+ *   - Outputs are overwritten, never accumulated into.  batch == 0 is a
+ *     no-op that returns SNK_OK.
+ *   - A handle is used by one stream at a time; calls on one handle that
+ *     overlap on the GPU race on its workspace.
+ *   - Nothing crosses the ABI as an exception; every entry point returns a
+ *     status code (snk_status_string gives its text).
+ *   - Limits: 1 <= out, in <= 2^31 - 1; 0 <= nnz <= min(out*in, 2^31 - 1);
+ *     out*in < 2^63.
+ *   - Numerics: fp32 products accumulated in fp32 with at least 32 partial
+ *     sums per output reduced by a tree, so that each output y satisfies
+ *     |y - exact| <= 1e-5 * A + 1e-6 with A the sum of |terms| (+|bias|).
+ */
+#ifndef SNK_H
+#define SNK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SNK_OK 0          /* success                                          */
+#define SNK_ERR_ARG 1     /* bad shape, null or misaligned pointer, bad zeta   */
+#define SNK_ERR_DUP 2     /* the triple holds the same (row, col) twice        */
+#define SNK_ERR_RANGE 3   /* a row or column index lies outside the matrix     */
+#define SNK_ERR_CUDA 4    /* a CUDA call or kernel launch failed               */
+#define SNK_ERR_OOM 5     /* workspace allocation failed                       */
+#define SNK_ERR_NOSPACE 6 /* fewer free positions than entries to regrow       */
+#define SNK_ERR_LIMIT 7   /* the regrow draw limit (64 k + 1024) was reached   */
+
+typedef struct snk_layer* snk_handle;
+
+/*
+ * snk_create - bind a layer to a caller-owned COO triple and build its
+ * topology.
+ *   [SNACK] Fig. 1: the weight is stored on the GPU as the COO triple over its
+ *   non-zeros only.  [PCSR] sec. 3.2 / 4.1: entries sorted by row, then by
+ *   column within a row, with a row pointer.  [SNACK] Table 7 and [PCSR]
+ *   sec. 7.2: the column-sorted (CSC) view and the permutation map that
+ *   gathers values into column order, built once per topology.
+ *
+ * handle   out: the new handle (unchanged on error).
+ * out_features, in_features: W is out_features x in_features.
+ * nnz      number of stored entries.
+ * values, rows, cols: device arrays of nnz fp32 / int32 / int32 in any order.
+ *          They are sorted IN PLACE into canonical order (by row, then
+ *          column) and BORROWED for the life of the handle: the caller keeps
+ *          them allocated, may update `values` between calls (e.g. an SGD
+ *          step), and must not modify `rows` or `cols`.
+ * stream   queue for the build.  The call synchronises the stream before it
+ *          returns, so that device-detected errors can be reported.
+ * Errors:  SNK_ERR_ARG, SNK_ERR_RANGE (an index outside the matrix),
+ *          SNK_ERR_DUP (a repeated position), SNK_ERR_OOM, SNK_ERR_CUDA.  On
+ *          SNK_ERR_RANGE / SNK_ERR_DUP the caller's arrays are left as given.
+ */
+int snk_create(snk_handle* handle, int64_t out_features, int64_t in_features, int64_t nnz,
+               float* values, int32_t* rows, int32_t* cols, void* stream);
+
+/*
+ * snk_forward - Y = X W^T + bias over supp(W) only.
+ *   [SNACK] Fig. 1 (the forward pass computed directly on the triple);
+ *   [PCSR] sec. 6.1 (for each live entry, scale the matching input and add
+ *   it to the output row).
+ * X     [batch, in] input.   bias  [out] or NULL (then no bias term).
+ * Y     [batch, out] output; a row of W with no entries yields bias (or 0).
+ * Errors: SNK_ERR_ARG, SNK_ERR_CUDA.
+ */
+int snk_forward(snk_handle handle, const float* X, int64_t batch, const float* bias, float* Y,
+                void* stream);
+
+/*
+ * snk_backward_input - dX = dY W (the transposed SpMM).
+ *   [PCSR] sec. 7.1 (dL/dX = W^T dL/dY in its features-major form, another
+ *   SpMM) and sec. 7.2 (the transpose is read through the column-sorted view
+ *   and the permutation built at create / restructure time; only the values
+ *   are gathered per call).
+ * dY    [batch, out] upstream gradient.
+ * dX    [batch, in] output; a column of W with no entries yields 0.
+ * Errors: SNK_ERR_ARG, SNK_ERR_CUDA.
+ */
+int snk_backward_input(snk_handle handle, const float* dY, int64_t batch, float* dX,
+                       void* stream);
+
+/*
+ * snk_backward_weight - the weight gradient at live entries only (SDDMM),
+ * and optionally the bias gradient.
+ *   [PCSR] sec. 7.1 (dL/dW only at live slots: a dot product of the dL/dY row
+ *   with the X row for each live entry); [SNACK] Fig. 1 (the backward pass as
+ *   a sparse outer product over supp(W)).  db = sum over the batch of dY, the
+ *   plain gradient of the bias (not on the pages).
+ * X, dY as above.
+ * dW    [nnz] output in canonical order: dW[k] belongs to (rows[k], cols[k]).
+ * db    [out] output or NULL.
+ * Errors: SNK_ERR_ARG, SNK_ERR_CUDA.
+ */
+int snk_backward_weight(snk_handle handle, const float* X, const float* dY, int64_t batch,
+                        float* dW, float* db, void* stream);
+
+/*
+ * snk_prune_regrow - one dynamic-sparse-training restructure, nnz fixed.
+ *   [PCSR] sec. 4.3 (drop a fraction of the live entries, grow the same
+ *   number elsewhere), sec. 1.1 (prune by smallest magnitude), sec. 8.2 (SET
+ *   with a drop fraction); [SNACK] Fig. 1 (connections added or dropped in
+ *   place).  The pages give no order of ties and no generator; this library
+ *   fixes them as follows.
+ *   Prune: k = floor((double)zeta * nnz) entries with the smallest keys
+ *     (bit pattern of |value|, row*in + col) are removed.
+ *   Regrow: positions p_t = floor(z_t * out*in / 2^64), z_t the t-th output
+ *     (t = 0, 1, ...) of SplitMix64 started at state `seed`, are accepted in
+ *     draw order when not held by a kept entry nor accepted before, until k
+ *     are accepted.  New entries get value +0.0f.  A position pruned in this
+ *     call may be drawn again.
+ *   The whole triple is then re-emitted in canonical order into the caller's
+ *   values/rows/cols, and the topology is rebuilt.
+ * zeta  in [0, 1).   seed  any 64-bit value.
+ * The call synchronises the stream (it reads device counts back).
+ * Errors: SNK_ERR_ARG (zeta outside [0,1)), SNK_ERR_NOSPACE (fewer than k
+ *   free positions, found before any work), SNK_ERR_LIMIT (fewer than k
+ *   positions accepted after 64 k + 1024 draws), SNK_ERR_OOM, SNK_ERR_CUDA.
+ *   On every error the caller's arrays and the topology are left unchanged.
+ */
+int snk_prune_regrow(snk_handle handle, float zeta, uint64_t seed, void* stream);
+
+/*
+ * snk_destroy - free the library-owned workspace (never the caller's arrays).
+ * NULL is accepted.  Waits for work queued on the handle's device.
+ */
+int snk_destroy(snk_handle handle);
+
+/* Text of a status code (static storage). */
+const char* snk_status_string(int status);
+
+/*
+ * snk_get_shape - sizes and the topology version of a handle.  The version
+ * starts at 1 and grows by one at each restructure that changes the support
+ * ([PCSR] sec. 5.1, the topology_version counter).  Any output may be NULL.
+ */
+int snk_get_shape(snk_handle handle, int64_t* out_features, int64_t* in_features, int64_t* nnz,
+                  int64_t* topology_version);
+
+/*
+ * snk_copy_topology - copy the derived index arrays to caller device buffers
+ * (any may be NULL): row_ptr [out+1], col_ptr [in+1], rows_c [nnz] (row of the
+ * j-th entry in column order) and perm [nnz] (its canonical slot, so values
+ * in column order are values[perm]).  [SNACK] Table 7; [PCSR] sec. 7.2.
+ * Asynchronous on `stream`.
+ */
+int snk_copy_topology(snk_handle handle, int32_t* row_ptr, int32_t* col_ptr, int32_t* rows_c,
+                      int32_t* perm, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SNK_H */

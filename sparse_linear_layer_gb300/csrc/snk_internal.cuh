@@ -1,0 +1,93 @@
+// Internal declarations of libsnk (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "snk.h"
+
+namespace snk {
+
+constexpr int kWarp = 32;
+constexpr int kThreads = 1024;       // SpMM / SDDMM block size: one block per SM
+constexpr int kWarpsPerBlock = kThreads / kWarp;
+constexpr int kChunksPerSm = 64;     // merge-path chunks per SM (2 per warp)
+constexpr int kMaxBatchTile = 64;    // batch columns handled by one launch
+
+// Device status word bits.
+constexpr int kStatRange = 1;
+constexpr int kStatDup = 2;
+constexpr int kStatLimit = 4;
+
+struct RestructureWs;
+
+// Library-owned state behind an snk_handle.
+struct Layer {
+    int64_t out_f = 0, in_f = 0, nnz = 0;
+    float* v = nullptr;       // caller-owned, canonical order
+    int32_t* r = nullptr;     // caller-owned
+    int32_t* c = nullptr;     // caller-owned
+
+    int device = 0;
+    int num_sms = 0;
+    int max_smem = 0;         // opt-in dynamic shared memory per block (bytes)
+    int64_t topology_version = 0;
+
+    // topology (rebuilt at create and after each restructure)
+    int32_t* row_ptr = nullptr;   // [out+1]
+    int32_t* col_ptr = nullptr;   // [in+1]
+    int32_t* rows_c = nullptr;    // [nnz] row of the j-th entry in column order
+    int32_t* perm = nullptr;      // [nnz] canonical slot of the j-th entry in column order
+
+    // merge-path chunking of the canonical (row) and column orders
+    int32_t chunk = 0;            // nnz per chunk
+    int32_t n_chunks = 0;         // ceil(nnz / chunk)
+    int32_t* own_r = nullptr;     // [n_chunks+1] first row whose start lies in chunk q
+    int32_t* own_c = nullptr;     // [n_chunks+1] same for columns
+
+    // scratch of the SpMM kernels
+    float* part = nullptr;        // [n_chunks * 2 * kMaxBatchTile] split-segment partials
+    int32_t* cnt = nullptr;       // [max(out,in)] arrival counters, all zero between calls
+    float* xt = nullptr;          // [max(out,in) * kMaxBatchTile] transposed operand
+
+    int32_t* status = nullptr;    // device status word
+
+    // sort workspace (topology build)
+    void* sort_keys = nullptr;    // 2 * nnz uint64
+    uint32_t* sort_vals = nullptr;// 2 * nnz
+    uint32_t* col_keys = nullptr; // 2 * nnz (column sort)
+    uint32_t* col_vals = nullptr; // 2 * nnz
+    int32_t* tile_hist = nullptr; // radix histograms
+    int64_t tile_hist_len = 0;
+
+    RestructureWs* rws = nullptr; // allocated on first prune_regrow
+};
+
+// ---- small helpers -------------------------------------------------------
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int batch_tile(int64_t b) {
+    int bp = 1;
+    while (bp < b) bp <<= 1;
+    return bp;
+}
+
+// ---- topology (snk_topology.cu) -----------------------------------------
+// Sort + validate + write back the canonical triple + CSR + CSC + chunk tables.
+// Returns an SNK_* status; synchronises `s`.
+int build_topology(Layer* L, cudaStream_t s, bool validate);
+
+// Radix helpers reused by the restructure code.
+int exclusive_scan_i32(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp, int64_t tmp_len,
+                       int32_t* total, cudaStream_t s);
+int64_t scan_tmp_len(int64_t n);
+
+// ---- kernels launched by the API ----------------------------------------
+int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float* Y,
+                   cudaStream_t s);
+int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaStream_t s);
+int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b, float* dW,
+                           float* db, cudaStream_t s);
+int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s);
+void free_restructure(Layer* L);
+
+}  // namespace snk

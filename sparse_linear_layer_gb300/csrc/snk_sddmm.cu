@@ -1,0 +1,209 @@
+// Weight gradient on the support (SDDMM) and the bias gradient.
+//
+//   "Padded-CSR: A sparse storage format for dynamic sparse training on CPU",
+//     sec. 7.1: dL/dW is wanted only at the live slots of W; for each live
+//     slot at (i, c) it is the dot product of the dL/dY row i with the X
+//     row c, so the dense M x K gradient is never formed.
+//   "Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks on
+//     GPU", Fig. 1: the backward pass as a sparse outer product over supp(W).
+//
+//     dW_k  = sum_beta dY[beta, r_k] * X[beta, c_k]     (canonical order)
+//     db[o] = sum_beta dY[beta, o]
+//
+// GB300 design: the same merge-path chunks and lane layout as the SpMM
+// kernel, walking the canonical order.  The row index comes from the row
+// pointer (no rows[] stream), the dY values of a row sit in registers for
+// the whole row, X is staged transposed in shared memory, and the output is
+// written with 128-bit stores in the order it is read, so the only HBM
+// streams are cols (read) and dW (write).  No entry depends on another, so no
+// chunk ever waits for another.
+#include "snk_device.cuh"
+
+namespace snk {
+
+struct SddmmArgs {
+    const int32_t* col;     // canonical column indices
+    const int32_t* row_ptr; // [out+1]
+    const int32_t* own;     // [n_chunks+1]
+    int64_t nnz, out_f, in_f;
+    int b;                  // batch columns of this tile
+    int chunk, n_chunks;
+    const float* X;         // [b, in] (tile)
+    const float* xt;        // [in][BP] (global path)
+    const float* dY;        // [b, out] (tile)
+    float* dW;              // [nnz]
+    bool accumulate;        // add to dW (later batch tiles)
+    const float* dY_all;    // [b_all, out] for db, or null
+    int64_t b_all;
+    float* db;              // [out] or null
+};
+
+template <int BP, bool SMEM>
+__global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
+    using TL = Tile<BP>;
+    constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
+    extern __shared__ float4 smem4[];
+    float* xs = reinterpret_cast<float*>(smem4);
+
+    if (a.db) {
+        // bias gradient over the whole batch, sequential in batch order
+        for (int64_t o = blockIdx.x * (int64_t)kThreads + threadIdx.x; o < a.out_f;
+             o += (int64_t)gridDim.x * kThreads) {
+            float sacc = 0.f;
+            for (int64_t beta = 0; beta < a.b_all; ++beta) sacc += a.dY_all[beta * a.out_f + o];
+            a.db[o] = sacc;
+        }
+    }
+    if constexpr (SMEM) {
+        stage_transposed<BP>(xs, a.X, a.in_f, a.b, a.in_f, threadIdx.x, kThreads);
+        __syncthreads();
+    }
+    const float* xsrc = SMEM ? xs : a.xt;
+
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / LPE;
+    const int sub = lane % LPE;
+    const int n_warps = gridDim.x * kWarpsPerBlock;
+    const uint32_t nnz = (uint32_t)a.nnz;
+    for (int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); q < a.n_chunks; q += n_warps) {
+        const uint32_t k0 = (uint32_t)q * (uint32_t)a.chunk;
+        const uint32_t k1 = min(k0 + (uint32_t)a.chunk, nnz);
+        const int lo = a.own[q];
+        const int hi = a.own[q + 1];
+        const int r_begin = (lo > 0 && (uint32_t)a.row_ptr[lo] > k0) ? lo - 1 : lo;
+        for (int r = r_begin; r < hi; ++r) {
+            const uint32_t s = max((uint32_t)a.row_ptr[r], k0);
+            const uint32_t e = min((uint32_t)a.row_ptr[r + 1], k1);
+            if (s >= e) continue;
+            float dyr[VEC];
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const int beta = sub * VEC + j;
+                dyr[j] = beta < a.b ? __ldg(a.dY + (int64_t)beta * a.out_f + r) : 0.f;
+            }
+            for (uint32_t base0 = s & ~3u; base0 < e; base0 += 4 * GPW) {
+                const uint32_t base = base0 + 4 * grp;
+                int col[4];
+                stream4(a.col, base, nnz, col);
+                float res[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t k = base + j;
+                    const bool ok = k >= s && k < e;
+                    float x[VEC];
+                    const float* px = xsrc + (ok ? col[j] : 0) * BP + sub * VEC;
+                    if constexpr (SMEM) VecF<VEC>::load(px, x);
+                    else VecF<VEC>::ldg(px, x);
+                    float p = 0.f;
+#pragma unroll
+                    for (int t = 0; t < VEC; ++t) p = fmaf(dyr[t], x[t], p);
+#pragma unroll
+                    for (int o = 1; o < LPE; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                    res[j] = p;
+                }
+                if (sub == 0) {
+                    const bool all4 = base >= s && base + 3 < e;
+                    if (all4) {
+                        float4 v = make_float4(res[0], res[1], res[2], res[3]);
+                        float4* dst = reinterpret_cast<float4*>(a.dW + base);
+                        if (a.accumulate) {
+                            float4 o4 = *dst;
+                            v.x += o4.x;
+                            v.y += o4.y;
+                            v.z += o4.z;
+                            v.w += o4.w;
+                        }
+                        *dst = v;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t k = base + j;
+                            if (k >= s && k < e)
+                                a.dW[k] = a.accumulate ? a.dW[k] + res[j] : res[j];
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int BP>
+__global__ void k_transpose_x(const float* __restrict__ X, int64_t n, int b, float* __restrict__ xt) {
+    stage_transposed<BP>(xt, X, n, b, n, blockIdx.x * blockDim.x + threadIdx.x,
+                         gridDim.x * blockDim.x);
+}
+
+__global__ void k_bias_grad_only(const float* __restrict__ dY, int64_t b, int64_t n,
+                                 float* __restrict__ db) {
+    for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < n;
+         o += (int64_t)gridDim.x * blockDim.x) {
+        float sacc = 0.f;
+        for (int64_t beta = 0; beta < b; ++beta) sacc += dY[beta * n + o];
+        db[o] = sacc;
+    }
+}
+
+template <int BP>
+static int launch_bp(Layer* L, SddmmArgs a, cudaStream_t s) {
+    const size_t smem = (size_t)a.in_f * BP * sizeof(float);
+    const int grid = (int)std::min<int64_t>(L->num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
+    if (smem <= (size_t)L->max_smem) {
+        auto fn = k_sddmm<BP, true>;
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+            return SNK_ERR_CUDA;
+        fn<<<grid, kThreads, smem, s>>>(a);
+    } else {
+        k_transpose_x<BP><<<L->num_sms * 4, 256, 0, s>>>(a.X, a.in_f, a.b, L->xt);
+        a.xt = L->xt;
+        k_sddmm<BP, false><<<grid, kThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+}
+
+int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b, float* dW,
+                           float* db, cudaStream_t s) {
+    if (L->nnz == 0) {
+        if (db) {
+            k_bias_grad_only<<<L->num_sms * 4, 256, 0, s>>>(dY, b, L->out_f, db);
+            if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
+        }
+        return SNK_OK;
+    }
+    SddmmArgs a{};
+    a.col = L->c;
+    a.row_ptr = L->row_ptr;
+    a.own = L->own_r;
+    a.nnz = L->nnz;
+    a.out_f = L->out_f;
+    a.in_f = L->in_f;
+    a.chunk = L->chunk;
+    a.n_chunks = L->n_chunks;
+    a.dW = dW;
+    a.b_all = b;
+    a.dY_all = dY;
+    for (int64_t t0 = 0; t0 < b; t0 += kMaxBatchTile) {
+        const int64_t bt = std::min<int64_t>(kMaxBatchTile, b - t0);
+        a.b = (int)bt;
+        a.X = X + t0 * L->in_f;
+        a.dY = dY + t0 * L->out_f;
+        a.accumulate = t0 > 0;
+        a.db = (t0 == 0) ? db : nullptr;
+        int st;
+        switch (batch_tile(bt)) {
+            case 1: st = launch_bp<1>(L, a, s); break;
+            case 2: st = launch_bp<2>(L, a, s); break;
+            case 4: st = launch_bp<4>(L, a, s); break;
+            case 8: st = launch_bp<8>(L, a, s); break;
+            case 16: st = launch_bp<16>(L, a, s); break;
+            case 32: st = launch_bp<32>(L, a, s); break;
+            default: st = launch_bp<64>(L, a, s); break;
+        }
+        if (st != SNK_OK) return st;
+    }
+    return SNK_OK;
+}
+
+}  // namespace snk
