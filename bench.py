@@ -56,8 +56,14 @@ def parse():
     p.add_argument("--batch", type=int, default=4)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--sweep", action="store_true",
-                   help="also print one extra JSON object per (sparsity, batch) to stderr")
+    p.add_argument("--no-restructure", action="store_true")
+    p.add_argument("--only", choices=["fwd", "dx", "dw"], default=None,
+                   help="time a single operation (profiling runs)")
+    p.add_argument("--flush-mb", type=int, default=512,
+                   help="L2 flush buffer written before every kernel (0 = no flush)")
+    p.add_argument("--sweep", default=None, metavar="FILE",
+                   help="instead of the single line, write one JSON object per "
+                        "(sparsity, batch) of the 10000x10000 sweep to FILE")
     return p.parse_args()
 
 
@@ -66,6 +72,24 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def reduce_max_ms(ms, device=None):
+    """Max over ranks of a per-rank elapsed time (timing plumbing only; the
+    layer itself exchanges nothing between ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(world, bytes_per_step, steps, max_ms):
+    """Whole-job GB/s: every rank moved bytes_per_step per step; the job took
+    the slowest rank's time."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
 
 
 def op_bytes(out_f, in_f, nnz, b):
@@ -255,6 +279,89 @@ def time_cpu_baseline(lay, X, dY, budget_s=12.0, max_steps=25):
     return steps, time.perf_counter() - t0
 
 
+def time_ops(binding, g, X, dY, bias, Y, dX, dW, db, flush, stream, steps, warmup, only=None):
+    """Per-op device times (ms) over `steps` steps, each kernel bracketed by
+    CUDA events on its stream, L2 flushed before every kernel (untimed)."""
+    import torch
+    sh = stream.cuda_stream
+    ops = [("fwd", lambda: binding.snk_forward(g.handle, X, bias, Y, sh)),
+           ("dx", lambda: binding.snk_backward_input(g.handle, dY, dX, sh)),
+           ("dw", lambda: binding.snk_backward_weight(g.handle, X, dY, dW, db, sh))]
+    if only:
+        ops = [o for o in ops if o[0] == only]
+    for _ in range(warmup):
+        for _, f in ops:
+            if flush is not None:
+                flush.zero_()
+            f()
+    torch.cuda.synchronize()
+    ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps)] for name, _ in ops}
+    for i in range(steps):
+        for name, f in ops:
+            if flush is not None:
+                flush.zero_()
+            e0, e1 = ev[name][i]
+            e0.record(stream)
+            f()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    return {name: [e0.elapsed_time(e1) for e0, e1 in ev[name]] for name, _ in ops}
+
+
+def summarize(per_op_ms, alg, formula, peak):
+    out = {}
+    for n, v in per_op_ms.items():
+        mean_us = sum(v) / len(v) * 1e3
+        srt = sorted(v)
+        out[n] = {"us_median": statistics.median(v) * 1e3, "us_mean": mean_us,
+                  "us_p10": srt[len(v) // 10] * 1e3, "us_p90": srt[(9 * len(v)) // 10] * 1e3,
+                  "gbs": alg[n] / (mean_us * 1e-6) / 1e9,
+                  "frac": alg[n] / (mean_us * 1e-6) / 1e9 / peak,
+                  "formula_gbs": formula[n] / (mean_us * 1e-6) / 1e9}
+    return out
+
+
+def make_device_layer(torch, binding, synth, dev, out_f, in_f, sparsity, b):
+    import numpy as np
+    lay = synth.make_layer(out_f, in_f, sparsity, 0.01, 21, 22)
+    X_h = synth.normal((b, in_f), 1.0, 23)
+    dY_h = synth.normal((b, out_f), 1.0, 24)
+    bias_h = synth.normal(out_f, 0.1, 25)
+    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    g = binding.SparseLinear(out_f, in_f, td(lay.values), td(lay.rows), td(lay.cols))
+    return lay, g, X_h, dY_h, td(X_h), td(dY_h), td(bias_h)
+
+
+def run_sweep(args, dev):
+    import torch
+
+    from sparse_linear_layer_gb300 import binding, synth
+    peak, peak_kind = measured_peaks()
+    flush = torch.empty(max(1, args.flush_mb) * 1024 * 1024 // 4, device=dev) if args.flush_mb else None
+    stream = torch.cuda.current_stream(dev)
+    with open(args.sweep, "w") as fo:
+        for sp in (90, 95, 99):
+            lay, g, _, _, _, _, bias = make_device_layer(torch, binding, synth, dev, args.out,
+                                                         args.inp, sp, 1)
+            for b in (1, 2, 4, 8, 16, 32, 64):
+                X = torch.randn(b, args.inp, device=dev)
+                dY = torch.randn(b, args.out, device=dev)
+                Y = torch.empty(b, args.out, device=dev)
+                dX = torch.empty(b, args.inp, device=dev)
+                dW = torch.empty(lay.nnz, device=dev)
+                db = torch.empty(args.out, device=dev)
+                ms = time_ops(binding, g, X, dY, bias, Y, dX, dW, db, flush, stream,
+                              args.steps, args.warmup)
+                alg, formula = op_bytes(args.out, args.inp, lay.nnz, b)
+                row = {"out": args.out, "in": args.inp, "sparsity_pct": sp, "nnz": lay.nnz,
+                       "batch": b, "peak_gbs": peak, "peak_kind": peak_kind,
+                       "ops": summarize(ms, alg, formula, peak)}
+                fo.write(json.dumps(row) + "\n")
+                fo.flush()
+            g.close()
+
+
 def run_ours(args, workload, rank, world, local):
     import numpy as np
     import torch
@@ -263,45 +370,25 @@ def run_ours(args, workload, rank, world, local):
     build.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.sweep:
+        run_sweep(args, dev)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
     out_f, in_f, b = args.out, args.inp, args.batch
-    lay = synth.make_layer(out_f, in_f, args.sparsity, 0.01, 21, 22)
+    lay, g, X_h, dY_h, X, dY, bias = make_device_layer(torch, binding, synth, dev, out_f, in_f,
+                                                       args.sparsity, b)
     nnz = lay.nnz
-    X_h = synth.normal((b, in_f), 1.0, 23)
-    dY_h = synth.normal((b, out_f), 1.0, 24)
-    bias_h = synth.normal(out_f, 0.1, 25)
-    td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    g = binding.SparseLinear(out_f, in_f, td(lay.values), td(lay.rows), td(lay.cols))
-    X, dY, bias = td(X_h), td(dY_h), td(bias_h)
     Y = torch.empty((b, out_f), device=dev)
     dX = torch.empty((b, in_f), device=dev)
     dW = torch.empty(nnz, device=dev)
     db = torch.empty(out_f, device=dev)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = (torch.empty(args.flush_mb * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+             if args.flush_mb else None)
     stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
 
-    def fwd():
-        binding.snk_forward(g.handle, X, bias, Y, sh)
-
-    def bwi():
-        binding.snk_backward_input(g.handle, dY, dX, sh)
-
-    def bww():
-        binding.snk_backward_weight(g.handle, X, dY, dW, db, sh)
-
-    ops = [("fwd", fwd), ("dx", bwi), ("dw", bww)]
-    for _ in range(args.warmup):
-        for _, f in ops:
-            flush.zero_()
-            f()
-    torch.cuda.synchronize()
-
-    ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(args.steps)] for name, _ in ops}
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -311,49 +398,31 @@ def run_ours(args, workload, rank, world, local):
         smi_id = str(local)
     with ClockSampler(smi_id) as clk:
         wall0 = time.perf_counter()
-        for i in range(args.steps):
-            for name, f in ops:
-                flush.zero_()
-                e0, e1 = ev[name][i]
-                e0.record(stream)
-                f()
-                e1.record(stream)
-        torch.cuda.synchronize()
+        per_op_ms = time_ops(binding, g, X, dY, bias, Y, dX, dW, db, flush, stream, args.steps,
+                             args.warmup, args.only)
         wall = time.perf_counter() - wall0
     if world > 1:
         torch.distributed.barrier()
-    per_op_ms = {name: [e0.elapsed_time(e1) for e0, e1 in ev[name]] for name, _ in ops}
-    total_ms = sum(sum(v) for v in per_op_ms.values())
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_ms(sum(sum(v) for v in per_op_ms.values()), dev)
     alg, formula = op_bytes(out_f, in_f, nnz, b)
-    step_bytes = sum(alg.values())
-    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
-    us = {name: statistics.median(v) * 1e3 for name, v in per_op_ms.items()}
-    p10 = {name: sorted(v)[len(v) // 10] * 1e3 for name, v in per_op_ms.items()}
-    p90 = {name: sorted(v)[(9 * len(v)) // 10] * 1e3 for name, v in per_op_ms.items()}
-    mean_us = {name: sum(v) / len(v) * 1e3 for name, v in per_op_ms.items()}
+    step_bytes = sum(alg[n] for n in per_op_ms)
+    value = aggregate_gbs(world, step_bytes, args.steps, total_ms)
     peak, peak_kind = measured_peaks()
-    dom = max(mean_us, key=mean_us.get)
-    achieved = alg[dom] / (mean_us[dom] * 1e-6) / 1e9
+    per_op = summarize(per_op_ms, alg, formula, peak)
+    us = {n: v["us_median"] for n, v in per_op.items()}
+    dom = max(per_op, key=lambda n: per_op[n]["us_mean"])
     kernel_tags = {"fwd": "k_spmm_fwd", "dx": "k_spmm_dx", "dw": "k_sddmm"}
-    traffic = committed_traffic(kernel_tags[dom], workload["workload"])
     roofline = {
-        "bound": "hbm", "kernel": kernel_tags[dom], "achieved": achieved, "peak": peak,
-        "peak_kind": f"hbm_gbs, {peak_kind}", "unit": "GB/s", "frac": achieved / peak,
-        "traffic": traffic, "algorithmic_bytes_per_launch": alg[dom],
-        "per_op": {n: {"us_median": us[n], "us_p10": p10[n], "us_p90": p90[n],
-                       "gbs": alg[n] / (mean_us[n] * 1e-6) / 1e9,
-                       "frac": alg[n] / (mean_us[n] * 1e-6) / 1e9 / peak,
-                       "formula_gbs": formula[n] / (mean_us[n] * 1e-6) / 1e9}
-                   for n in us},
+        "bound": "hbm", "kernel": kernel_tags[dom], "op": dom, "achieved": per_op[dom]["gbs"],
+        "peak": peak, "peak_kind": f"hbm_gbs, {peak_kind}", "unit": "GB/s",
+        "frac": per_op[dom]["frac"], "traffic": committed_traffic(kernel_tags[dom], workload["workload"]),
+        "algorithmic_bytes_per_launch": alg[dom], "per_op": per_op,
     }
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.only is None:
+        sh = stream.cuda_stream
         Xp = torch.from_numpy(X_h).pin_memory()
         dYp = torch.from_numpy(dY_h).pin_memory()
         Yp = torch.empty((b, out_f)).pin_memory()
@@ -362,25 +431,22 @@ def run_ours(args, workload, rank, world, local):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n_e2e)]
         for i in range(n_e2e + 3):
-            flush.zero_()
+            if flush is not None:
+                flush.zero_()
             if i >= 3:
                 evs[i - 3][0].record(stream)
             X.copy_(Xp, non_blocking=True)
             dY.copy_(dYp, non_blocking=True)
-            fwd()
-            bwi()
-            bww()
+            binding.snk_forward(g.handle, X, bias, Y, sh)
+            binding.snk_backward_input(g.handle, dY, dX, sh)
+            binding.snk_backward_weight(g.handle, X, dY, dW, db, sh)
             Yp.copy_(Y, non_blocking=True)
             dXp.copy_(dX, non_blocking=True)
             if i >= 3:
                 evs[i - 3][1].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(z) for a, z in evs)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * step_bytes * n_e2e / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e2e_ms = reduce_max_ms(sum(a0.elapsed_time(z) for a0, z in evs), dev)
+        e2e = {"value": aggregate_gbs(world, step_bytes, n_e2e, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": (X_h.nbytes + dY_h.nbytes),
                "d2h_bytes_per_step": b * (out_f + in_f) * 4,
                "ms_per_step": e2e_ms / n_e2e,
@@ -389,26 +455,28 @@ def run_ours(args, workload, rank, world, local):
 
     # ---- restructure (SET cadence work), timed separately
     restructure = None
-    if rank == 0:
+    if rank == 0 and not args.no_restructure:
         torch.cuda.synchronize()
-        reps = 3
         ts = []
-        for i in range(reps):
+        for i in range(3):
             t0 = time.perf_counter()
             g.prune_regrow(0.3, 0x5E7 + i)
             torch.cuda.synchronize()
             ts.append((time.perf_counter() - t0) * 1e6)
-        restructure = {"op": "prune_regrow", "zeta": 0.3, "us_median_host_timed": statistics.median(ts),
+        restructure = {"op": "prune_regrow", "zeta": 0.3,
+                       "us_median_host_timed": statistics.median(ts),
                        "note": "synchronous call (it reads device counts back); wall-clock µs"}
 
     max_smem = torch.cuda.get_device_properties(dev).shared_memory_per_block_optin
-    launches = args.steps * (launches_per_op(in_f, b, max_smem) + launches_per_op(out_f, b, max_smem)
-                             + launches_per_op(in_f, b, max_smem))
+    per_op_launch = {"fwd": launches_per_op(in_f, b, max_smem),
+                     "dx": launches_per_op(out_f, b, max_smem),
+                     "dw": launches_per_op(in_f, b, max_smem)}
+    launches = args.steps * sum(per_op_launch[n] for n in per_op_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         steps_c, dt_c = time_cpu_baseline(lay, X_h, dY_h)
-        cpu = {"value": step_bytes * steps_c / dt_c / 1e9, "unit": "GB/s", "cores": 1,
+        cpu = {"value": sum(alg.values()) * steps_c / dt_c / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle",
                "sample": f"{steps_c} full steps (forward + dX + dW, fp64 accumulation) of the same "
                          f"{out_f}x{in_f} layer, batch {b}, single-threaded"}
@@ -444,7 +512,9 @@ def main():
                        f"batch {args.batch}; step = forward (bias) + backward_input + "
                        f"backward_weight (db)",
         "out": args.out, "in": args.inp, "sparsity_pct": args.sparsity, "nnz": nnz,
-        "batch": args.batch, "l2": "flushed by a 512 MB write before every kernel, untimed",
+        "batch": args.batch,
+        "l2": (f"flushed by a {args.flush_mb} MB write before every kernel, untimed"
+               if args.flush_mb else "not flushed"),
         "parallelism": f"replicas x{world}",
     }
     if args.impl == "reference":

@@ -87,29 +87,89 @@ __device__ __forceinline__ void stream4(const int32_t* __restrict__ p, uint32_t 
 }
 
 // Stage the operand transposed: dst[i*BP + beta] = src[beta*ld + i] for
-// beta < b, 0 for b <= beta < BP, for i < n.  Reads are coalesced over i.
+// beta < b, 0 for b <= beta < BP, for i < n.  Reads are coalesced over i;
+// U columns per thread are loaded before any is stored so that enough loads
+// are in flight to hide the latency of the (L2-resident) source.
 template <int BP>
 __device__ __forceinline__ void stage_transposed(float* dst, const float* __restrict__ src,
                                                  int64_t ld, int b, int64_t n, int tid,
                                                  int nthreads) {
-    for (int64_t i = tid; i < n; i += nthreads) {
+    // at most 8 float4 (BP >= 4) or 16 floats (BP < 4) are held per thread
+    constexpr int Q = BP >= 4 ? BP / 4 : 1;   // float4 per column
+    constexpr int QB = Q < 8 ? Q : 8;          // float4 per column per batch
+    constexpr int U = BP >= 4 ? 8 / QB : 16 / BP;
+    for (int64_t i0 = tid; i0 < n; i0 += (int64_t)nthreads * U) {
         if constexpr (BP >= 4) {
-#pragma unroll 4
-            for (int q = 0; q < BP; q += 4) {
-                float4 t;
-                t.x = q + 0 < b ? src[(q + 0) * ld + i] : 0.f;
-                t.y = q + 1 < b ? src[(q + 1) * ld + i] : 0.f;
-                t.z = q + 2 < b ? src[(q + 2) * ld + i] : 0.f;
-                t.w = q + 3 < b ? src[(q + 3) * ld + i] : 0.f;
-                *reinterpret_cast<float4*>(dst + i * BP + q) = t;
+#pragma unroll
+            for (int qb = 0; qb < Q; qb += QB) {
+                float4 t[U][QB];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = i0 + (int64_t)u * nthreads;
+#pragma unroll
+                    for (int q = 0; q < QB; ++q) {
+                        const int bq = 4 * (qb + q);
+                        const bool ok = i < n;
+                        t[u][q].x = ok && bq + 0 < b ? __ldg(src + (bq + 0) * ld + i) : 0.f;
+                        t[u][q].y = ok && bq + 1 < b ? __ldg(src + (bq + 1) * ld + i) : 0.f;
+                        t[u][q].z = ok && bq + 2 < b ? __ldg(src + (bq + 2) * ld + i) : 0.f;
+                        t[u][q].w = ok && bq + 3 < b ? __ldg(src + (bq + 3) * ld + i) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = i0 + (int64_t)u * nthreads;
+                    if (i < n) {
+#pragma unroll
+                        for (int q = 0; q < QB; ++q)
+                            *reinterpret_cast<float4*>(dst + i * BP + 4 * (qb + q)) = t[u][q];
+                    }
+                }
             }
-        } else if constexpr (BP == 2) {
-            *reinterpret_cast<float2*>(dst + i * 2) =
-                make_float2(src[i], b > 1 ? src[ld + i] : 0.f);
         } else {
-            dst[i] = src[i];
+            float t[U][BP];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * nthreads;
+#pragma unroll
+                for (int q = 0; q < BP; ++q) t[u][q] = (i < n && q < b) ? __ldg(src + q * ld + i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * nthreads;
+                if (i < n) {
+                    if constexpr (BP == 2) *reinterpret_cast<float2*>(dst + i * 2) = make_float2(t[u][0], t[u][1]);
+                    else dst[i] = t[u][0];
+                }
+            }
         }
     }
 }
+
+// Row (segment) boundaries of one chunk, read 32 at a time: lane t holds the
+// start of relative segment base+t and, optionally, that segment's bias.
+// Queried warp-uniformly; moving forward reloads the window.
+struct SegWindow {
+    const int32_t* seg_ptr;
+    const float* bias;
+    int r_begin, nrows, base;
+    uint32_t start;
+    float b;
+    __device__ __forceinline__ void load(int rel, int lane) {
+        base = rel;
+        const int t = rel + lane;
+        start = t <= nrows ? (uint32_t)__ldg(seg_ptr + r_begin + t) : 0u;
+        b = (bias && t < nrows) ? __ldg(bias + r_begin + t) : 0.f;
+    }
+    // start of relative segment i; the window is kept so that segment i-1's
+    // bias stays readable
+    __device__ __forceinline__ uint32_t bnd(int i, int lane) {
+        if (i - base >= 32) load(i - 1, lane);
+        return __shfl_sync(0xffffffffu, start, i - base);
+    }
+    __device__ __forceinline__ float bias_of(int i) {
+        return __shfl_sync(0xffffffffu, b, i - base);
+    }
+};
 
 }  // namespace snk

@@ -11,7 +11,7 @@ namespace snk {
 constexpr int kWarp = 32;
 constexpr int kThreads = 1024;       // SpMM / SDDMM block size: one block per SM
 constexpr int kWarpsPerBlock = kThreads / kWarp;
-constexpr int kChunksPerSm = 64;     // merge-path chunks per SM (2 per warp)
+constexpr int kChunksPerSm = 32;     // merge-path chunks per SM (one per warp)
 constexpr int kMaxBatchTile = 64;    // batch columns handled by one launch
 
 // Device status word bits.

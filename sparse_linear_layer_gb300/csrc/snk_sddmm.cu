@@ -38,13 +38,42 @@ struct SddmmArgs {
     float* db;              // [out] or null
 };
 
+template <int BP>
+__device__ __forceinline__ void load_dy_row(const SddmmArgs& a, int r, int sub,
+                                            float (&d)[Tile<BP>::VEC]) {
+    constexpr int VEC = Tile<BP>::VEC;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        const int beta = sub * VEC + j;
+        d[j] = beta < a.b ? __ldg(a.dY + (int64_t)beta * a.out_f + r) : 0.f;
+    }
+}
+
+// One warp per chunk; the chunk's column indices stream as flat blocks of
+// 4*GPW entries with the next block prefetched.  The dY values of the current
+// row are in registers and the next row's are requested one row ahead.
 template <int BP, bool SMEM>
 __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
+    constexpr uint32_t BLK = 4 * GPW;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
 
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / LPE;
+    const int sub = lane % LPE;
+    const uint32_t nnz = (uint32_t)a.nnz;
+    const uint32_t chunk = (uint32_t)a.chunk;
+    const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const bool active = q < a.n_chunks;
+    uint32_t k0 = 0, k1 = 0;
+    int cc[4] = {0, 0, 0, 0};
+    if (active) {
+        k0 = (uint32_t)q * chunk;
+        k1 = min(k0 + chunk, nnz);
+        stream4(a.col, k0 + 4 * grp, nnz, cc);
+    }
     if (a.db) {
         // bias gradient over the whole batch, sequential in batch order
         for (int64_t o = blockIdx.x * (int64_t)kThreads + threadIdx.x; o < a.out_f;
@@ -58,72 +87,77 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
         stage_transposed<BP>(xs, a.X, a.in_f, a.b, a.in_f, threadIdx.x, kThreads);
         __syncthreads();
     }
+    if (!active) return;
     const float* xsrc = SMEM ? xs : a.xt;
 
-    const int lane = threadIdx.x & 31;
-    const int grp = lane / LPE;
-    const int sub = lane % LPE;
-    const int n_warps = gridDim.x * kWarpsPerBlock;
-    const uint32_t nnz = (uint32_t)a.nnz;
-    for (int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); q < a.n_chunks; q += n_warps) {
-        const uint32_t k0 = (uint32_t)q * (uint32_t)a.chunk;
-        const uint32_t k1 = min(k0 + (uint32_t)a.chunk, nnz);
-        const int lo = a.own[q];
-        const int hi = a.own[q + 1];
-        const int r_begin = (lo > 0 && (uint32_t)a.row_ptr[lo] > k0) ? lo - 1 : lo;
-        for (int r = r_begin; r < hi; ++r) {
-            const uint32_t s = max((uint32_t)a.row_ptr[r], k0);
-            const uint32_t e = min((uint32_t)a.row_ptr[r + 1], k1);
-            if (s >= e) continue;
-            float dyr[VEC];
+    const int lo = a.own[q];
+    const int hi = a.own[q + 1];
+    const int r_begin = (lo > 0 && (uint32_t)a.row_ptr[lo] > k0) ? lo - 1 : lo;
+    SegWindow win{a.row_ptr, nullptr, r_begin, hi - r_begin, 0, 0u, 0.f};
+    win.load(0, lane);
+    int i = 0;
+    uint32_t rs = win.bnd(0, lane), re = win.bnd(1, lane);
+    float dyr[VEC], dyn[VEC];
+    load_dy_row<BP>(a, r_begin, sub, dyr);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                const int beta = sub * VEC + j;
-                dyr[j] = beta < a.b ? __ldg(a.dY + (int64_t)beta * a.out_f + r) : 0.f;
+    for (int j = 0; j < VEC; ++j) dyn[j] = 0.f;
+    if (win.nrows > 1) load_dy_row<BP>(a, r_begin + 1, sub, dyn);
+
+    for (uint32_t base0 = k0; base0 < k1; base0 += BLK) {
+        const uint32_t base = base0 + 4 * grp;
+        int nc[4];
+        if (base0 + BLK < k1) stream4(a.col, base + BLK, nnz, nc);
+        const uint32_t blk_end = min(base0 + BLK, k1);
+        float res[4] = {0.f, 0.f, 0.f, 0.f};
+        while (true) {
+            const uint32_t lo_k = max(rs, base0), hi_k = min(re, blk_end);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t k = base + j;
+                const bool ok = k >= lo_k && k < hi_k;
+                float x[VEC];
+                const float* px = xsrc + (ok ? cc[j] : 0) * BP + sub * VEC;
+                if constexpr (SMEM) VecF<VEC>::load(px, x);
+                else VecF<VEC>::ldg(px, x);
+                float p = 0.f;
+#pragma unroll
+                for (int t = 0; t < VEC; ++t) p = fmaf(dyr[t], x[t], p);
+#pragma unroll
+                for (int o = 1; o < LPE; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                if (ok) res[j] = p;
             }
-            for (uint32_t base0 = s & ~3u; base0 < e; base0 += 4 * GPW) {
-                const uint32_t base = base0 + 4 * grp;
-                int col[4];
-                stream4(a.col, base, nnz, col);
-                float res[4];
+            if (min(re, k1) > blk_end) break;  // row continues in the next block
+            if (++i >= win.nrows) break;
+            rs = re;
+            re = win.bnd(i + 1, lane);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) dyr[j] = dyn[j];
+            if (i + 1 < win.nrows) load_dy_row<BP>(a, r_begin + i + 1, sub, dyn);
+            if (rs >= blk_end) break;
+        }
+        if (sub == 0) {
+            if (base >= k0 && base + 3 < k1) {
+                float4 v = make_float4(res[0], res[1], res[2], res[3]);
+                float4* dst = reinterpret_cast<float4*>(a.dW + base);
+                if (a.accumulate) {
+                    const float4 o4 = *dst;
+                    v.x += o4.x;
+                    v.y += o4.y;
+                    v.z += o4.z;
+                    v.w += o4.w;
+                }
+                *dst = v;
+            } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t k = base + j;
-                    const bool ok = k >= s && k < e;
-                    float x[VEC];
-                    const float* px = xsrc + (ok ? col[j] : 0) * BP + sub * VEC;
-                    if constexpr (SMEM) VecF<VEC>::load(px, x);
-                    else VecF<VEC>::ldg(px, x);
-                    float p = 0.f;
-#pragma unroll
-                    for (int t = 0; t < VEC; ++t) p = fmaf(dyr[t], x[t], p);
-#pragma unroll
-                    for (int o = 1; o < LPE; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                    res[j] = p;
-                }
-                if (sub == 0) {
-                    const bool all4 = base >= s && base + 3 < e;
-                    if (all4) {
-                        float4 v = make_float4(res[0], res[1], res[2], res[3]);
-                        float4* dst = reinterpret_cast<float4*>(a.dW + base);
-                        if (a.accumulate) {
-                            float4 o4 = *dst;
-                            v.x += o4.x;
-                            v.y += o4.y;
-                            v.z += o4.z;
-                            v.w += o4.w;
-                        }
-                        *dst = v;
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t k = base + j;
-                            if (k >= s && k < e)
-                                a.dW[k] = a.accumulate ? a.dW[k] + res[j] : res[j];
-                        }
-                    }
+                    if (k >= k0 && k < k1) a.dW[k] = a.accumulate ? a.dW[k] + res[j] : res[j];
                 }
             }
+        }
+        if (base0 + BLK < k1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cc[j] = nc[j];
         }
     }
 }

@@ -54,117 +54,170 @@ struct SpmmArgs {
     int32_t* cnt;           // [n_seg]
 };
 
+// Finish one output segment: reduce the per-lane partial sums across the
+// warp's groups, then either write the result or, for a segment cut by a
+// chunk boundary, publish this chunk's partial and let the last arriving
+// chunk add all partials in chunk order.
+template <int BP>
+__device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[Tile<BP>::VEC],
+                                               int r, uint32_t rs, uint32_t re, uint32_t k0,
+                                               uint32_t k1, int q, float bo, int lane, int sub) {
+    using TL = Tile<BP>;
+    constexpr int VEC = TL::VEC, LPE = TL::LPE;
+#pragma unroll
+    for (int o = LPE; o < kWarp; o <<= 1) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+    }
+    if (rs >= k0 && re <= k1) {
+        if (lane < LPE) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const int beta = sub * VEC + j;
+                if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = acc[j] + bo;
+            }
+        }
+    } else {
+        const uint32_t chunk = (uint32_t)a.chunk;
+        const int64_t q_first = rs / chunk;
+        const int64_t q_last = (re - 1) / chunk;
+        const int slot = (rs < k0) ? 0 : 1;
+        if (lane < LPE) {
+            float* my = a.part + ((int64_t)q * 2 + slot) * BP + sub * VEC;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) my[j] = acc[j];
+        }
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(a.cnt + r, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == (int)(q_last - q_first)) {
+            __threadfence();
+            if (lane < LPE) {
+                float sum[VEC];
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) sum[j] = 0.f;
+                for (int64_t qq = q_first; qq <= q_last; ++qq) {
+                    const float* pp = a.part + (qq * 2 + (qq == q_first ? 1 : 0)) * BP + sub * VEC;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) sum[j] += __ldcg(pp + j);
+                }
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const int beta = sub * VEC + j;
+                    if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = sum[j] + bo;
+                }
+            }
+            if (lane == 0) a.cnt[r] = 0;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+}
+
+// One warp per chunk.  The chunk's entries [k0, k1) are streamed as a flat
+// sequence of blocks of 4*GPW entries (each group of LPE lanes owns 4
+// consecutive entries of a block), with the next block's loads issued before
+// the current one is consumed.  The segment walk only masks entries; a block
+// that straddles segment boundaries is consumed once per segment it touches.
 template <int BP, bool GATHER, bool SMEM>
 __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
+    constexpr uint32_t BLK = 4 * GPW;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
-    if constexpr (SMEM) {
-        stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, kThreads);
-        __syncthreads();
-    }
-    const float* xsrc = SMEM ? xs : a.xt;
 
     const int lane = threadIdx.x & 31;
     const int grp = lane / LPE;
     const int sub = lane % LPE;
-    const int n_warps = gridDim.x * kWarpsPerBlock;
     const uint32_t nnz = (uint32_t)a.nnz;
-    for (int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); q < a.n_chunks; q += n_warps) {
-        const uint32_t k0 = (uint32_t)q * (uint32_t)a.chunk;
-        const uint32_t k1 = min(k0 + (uint32_t)a.chunk, nnz);
-        const int lo = a.own[q];
-        const int hi = a.own[q + 1];
-        const int r_begin = (lo > 0 && (uint32_t)a.seg_ptr[lo] > k0) ? lo - 1 : lo;
-        for (int r = r_begin; r < hi; ++r) {
-            const uint32_t rs = (uint32_t)a.seg_ptr[r], re = (uint32_t)a.seg_ptr[r + 1];
-            const uint32_t s = max(rs, k0), e = min(re, k1);
-            float acc[VEC];
+    const uint32_t chunk = (uint32_t)a.chunk;
+    const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const bool active = q < a.n_chunks;
+
+    // first block of this warp's chunk, requested before the operand staging
+    // so that HBM is busy while shared memory fills
+    uint32_t k0 = 0, k1 = 0;
+    int cc[4] = {0, 0, 0, 0};
+    float cw[4] = {0.f, 0.f, 0.f, 0.f};
+    int cp[4] = {0, 0, 0, 0};
+    if (active) {
+        k0 = (uint32_t)q * chunk;
+        k1 = min(k0 + chunk, nnz);
+        stream4(a.idx, k0 + 4 * grp, nnz, cc);
+        if constexpr (GATHER) stream4(a.perm, k0 + 4 * grp, nnz, cp);
+        else stream4(a.val, k0 + 4 * grp, nnz, cw);
+    }
+    if constexpr (SMEM) {
+        stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, kThreads);
+        __syncthreads();
+    }
+    if (!active) return;
+    const float* xsrc = SMEM ? xs : a.xt;
+
+    const int lo = a.own[q];
+    const int hi = a.own[q + 1];
+    const int r_begin = (lo > 0 && (uint32_t)a.seg_ptr[lo] > k0) ? lo - 1 : lo;
+    SegWindow win{a.seg_ptr, a.bias, r_begin, hi - r_begin, 0, 0u, 0.f};
+    win.load(0, lane);
+    int i = 0;
+    uint32_t rs = win.bnd(0, lane), re = win.bnd(1, lane);
+    float acc[VEC];
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
-            // warp-uniform trip count: every group runs the same iterations
-            for (uint32_t base0 = s & ~3u; base0 < e; base0 += 4 * GPW) {
-                const uint32_t base = base0 + 4 * grp;
-                float w[4];
-                int col[4];
-                stream4(a.idx, base, nnz, col);
-                if constexpr (!GATHER) {
-                    stream4(a.val, base, nnz, w);
-                } else {
-                    int pm[4];
-                    stream4(a.perm, base, nnz, pm);
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+
+    for (uint32_t base0 = k0; base0 < k1; base0 += BLK) {
+        const uint32_t base = base0 + 4 * grp;
+        if constexpr (GATHER) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t k = base + j;
-                        w[j] = (k >= s && k < e) ? __ldg(a.val + pm[j]) : 0.f;
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t k = base + j;
-                    if (k >= s && k < e) {
-                        float x[VEC];
-                        const float* px = xsrc + col[j] * BP + sub * VEC;
-                        if constexpr (SMEM) VecF<VEC>::load(px, x);
-                        else VecF<VEC>::ldg(px, x);
-#pragma unroll
-                        for (int t = 0; t < VEC; ++t) acc[t] = fmaf(w[j], x[t], acc[t]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int o = LPE; o < kWarp; o <<= 1) {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
-            }
-            const float bo = a.bias ? __ldg(a.bias + r) : 0.f;
-            if (rs >= k0 && re <= k1) {
-                if (lane < LPE) {
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const int beta = sub * VEC + j;
-                        if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = acc[j] + bo;
-                    }
-                }
-            } else {
-                // segment cut by a chunk boundary: publish this chunk's partial,
-                // and let the last arriving chunk sum all of them in chunk order
-                const int64_t q_first = rs / (uint32_t)a.chunk;
-                const int64_t q_last = (re - 1) / (uint32_t)a.chunk;
-                const int slot = (rs < k0) ? 0 : 1;
-                if (lane < LPE) {
-                    float* my = a.part + ((int64_t)q * 2 + slot) * BP + sub * VEC;
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) my[j] = acc[j];
-                }
-                __threadfence();
-                __syncwarp();
-                int old = 0;
-                if (lane == 0) old = atomicAdd(a.cnt + r, 1);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == (int)(q_last - q_first)) {
-                    __threadfence();
-                    if (lane < LPE) {
-                        float sum[VEC];
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) sum[j] = 0.f;
-                        for (int64_t qq = q_first; qq <= q_last; ++qq) {
-                            const float* pp =
-                                a.part + (qq * 2 + (qq == q_first ? 1 : 0)) * BP + sub * VEC;
-#pragma unroll
-                            for (int j = 0; j < VEC; ++j) sum[j] += __ldcg(pp + j);
-                        }
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) {
-                            const int beta = sub * VEC + j;
-                            if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = sum[j] + bo;
-                        }
-                    }
-                    if (lane == 0) a.cnt[r] = 0;
-                }
-            }
+            for (int j = 0; j < 4; ++j) cw[j] = (base + j < k1) ? __ldg(a.val + cp[j]) : 0.f;
         }
+        // prefetch the next block
+        int nc[4], np[4];
+        float nw[4];
+        const uint32_t nbase = base + BLK;
+        if (base0 + BLK < k1) {
+            stream4(a.idx, nbase, nnz, nc);
+            if constexpr (GATHER) stream4(a.perm, nbase, nnz, np);
+            else stream4(a.val, nbase, nnz, nw);
+        }
+        const uint32_t blk_end = min(base0 + BLK, k1);
+        while (true) {
+            const uint32_t lo_k = max(rs, base0), hi_k = min(re, blk_end);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t k = base + j;
+                if (k >= lo_k && k < hi_k) {
+                    float x[VEC];
+                    const float* px = xsrc + cc[j] * BP + sub * VEC;
+                    if constexpr (SMEM) VecF<VEC>::load(px, x);
+                    else VecF<VEC>::ldg(px, x);
+#pragma unroll
+                    for (int t = 0; t < VEC; ++t) acc[t] = fmaf(cw[j], x[t], acc[t]);
+                }
+            }
+            if (min(re, k1) > blk_end) break;  // segment continues in the next block
+            finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub);
+            if (++i >= win.nrows) break;
+            rs = re;
+            re = win.bnd(i + 1, lane);
+            if (rs >= blk_end) break;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            cc[j] = nc[j];
+            if constexpr (GATHER) cp[j] = np[j];
+            else cw[j] = nw[j];
+        }
+    }
+    // segments that start at the end of the chunk (empty here)
+    while (i < win.nrows) {
+        finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub);
+        if (++i >= win.nrows) break;
+        rs = re;
+        re = win.bnd(i + 1, lane);
     }
 }
 
