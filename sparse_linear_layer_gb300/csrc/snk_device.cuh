@@ -86,34 +86,6 @@ __device__ __forceinline__ void stream4(const int32_t* __restrict__ p, uint32_t 
     }
 }
 
-// Bulk L2 prefetch by the TMA engine (no registers, no L1 traffic): the
-// address must be 16-byte aligned and the size a multiple of 16 bytes.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// Sliding-window L2 prefetch of up to three 4-byte streams over the entries
-// [next, end) of one chunk: units of kPfUnit entries, kPfUnits units ahead of
-// the consumer.  Issued by one lane; entries past the last full group of 4
-// before the end of the array are never touched.
-constexpr uint32_t kPfUnit = 512;
-constexpr uint32_t kPfUnits = 4;
-struct StreamPrefetch {
-    uint32_t next, end;   // end is rounded down to a multiple of 4
-    __device__ __forceinline__ void advance(uint32_t upto, int lane, const void* s0,
-                                            const void* s1) {
-        upto = min(upto, end);
-        while (next < upto) {
-            const uint32_t n = min(kPfUnit, end - next);
-            if (lane == 0) {
-                prefetch_l2_bulk(static_cast<const uint32_t*>(s0) + next, n * 4);
-                if (s1) prefetch_l2_bulk(static_cast<const uint32_t*>(s1) + next, n * 4);
-            }
-            next += n;
-        }
-    }
-};
-
 // Stage the operand transposed: dst[i*BP + beta] = src[beta*ld + i] for
 // beta < b, 0 for b <= beta < BP, for i < n.  Reads are coalesced over i;
 // U columns per thread are loaded before any is stored so that enough loads

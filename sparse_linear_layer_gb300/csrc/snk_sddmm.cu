@@ -69,13 +69,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     const bool active = q < a.n_chunks;
     uint32_t k0 = 0, k1 = 0;
     int cc[4] = {0, 0, 0, 0};
-    StreamPrefetch pf{0u, 0u};
     if (active) {
         k0 = (uint32_t)q * chunk;
         k1 = min(k0 + chunk, nnz);
-        pf.next = k0;
-        pf.end = max(k0, min(k1 + 3, nnz) & ~3u);
-        pf.advance(k0 + kPfUnits * kPfUnit, lane, a.col, nullptr);
         stream4(a.col, k0 + 4 * grp, nnz, cc);
     }
     if (a.db) {
@@ -109,7 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
 
     for (uint32_t base0 = k0; base0 < k1; base0 += BLK) {
         const uint32_t base = base0 + 4 * grp;
-        pf.advance(base0 + kPfUnits * kPfUnit, lane, a.col, nullptr);
         int nc[4];
         if (base0 + BLK < k1) stream4(a.col, base + BLK, nnz, nc);
         const uint32_t blk_end = min(base0 + BLK, k1);

@@ -143,14 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     int cc[4] = {0, 0, 0, 0};
     float cw[4] = {0.f, 0.f, 0.f, 0.f};
     int cp[4] = {0, 0, 0, 0};
-    StreamPrefetch pf{0u, 0u};
-    const void* pf_second = GATHER ? (const void*)a.perm : (const void*)a.val;
     if (active) {
         k0 = (uint32_t)q * chunk;
         k1 = min(k0 + chunk, nnz);
-        pf.next = k0;
-        pf.end = max(k0, min(k1 + 3, nnz) & ~3u);
-        pf.advance(k0 + kPfUnits * kPfUnit, lane, a.idx, pf_second);
         stream4(a.idx, k0 + 4 * grp, nnz, cc);
         if constexpr (GATHER) stream4(a.perm, k0 + 4 * grp, nnz, cp);
         else stream4(a.val, k0 + 4 * grp, nnz, cw);
@@ -175,7 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
 
     for (uint32_t base0 = k0; base0 < k1; base0 += BLK) {
         const uint32_t base = base0 + 4 * grp;
-        pf.advance(base0 + kPfUnits * kPfUnit, lane, a.idx, pf_second);
         if constexpr (GATHER) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) cw[j] = (base + j < k1) ? __ldg(a.val + cp[j]) : 0.f;
