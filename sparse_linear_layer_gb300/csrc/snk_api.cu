@@ -24,7 +24,7 @@ static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)
 static void free_layer(Layer* L) {
     if (!L) return;
     free_restructure(L);
-    void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->own_r, L->own_c,
+    void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->c16, L->rc16, L->own_r, L->own_c,
                     L->part, L->cnt, L->xt, L->status, L->sort_keys, L->sort_vals,
                     L->col_keys, L->col_vals, L->tile_hist};
     for (void* p : ptrs)
@@ -99,9 +99,12 @@ int snk_create(snk_handle* handle, int64_t out_f, int64_t in_f, int64_t nnz, flo
     const int64_t n_max = std::max(out_f, in_f);
     const bool wide = (uint64_t)out_f * (uint64_t)in_f > (1ull << 32);
     L->tile_hist_len = topology_hist_len(nnz);
+    L->nnz_pad = ceil_div(nnz, 4) * 4 + kStreamPad;
 
     bool ok = dmalloc(&L->row_ptr, out_f + 1) && dmalloc(&L->col_ptr, in_f + 1) &&
-              dmalloc(&L->rows_c, nnz) && dmalloc(&L->perm, nnz) &&
+              dmalloc(&L->rows_c, L->nnz_pad) && dmalloc(&L->perm, L->nnz_pad) &&
+              (in_f > 65536 || dmalloc(&L->c16, L->nnz_pad)) &&
+              (out_f > 65536 || dmalloc(&L->rc16, L->nnz_pad)) &&
               dmalloc(&L->own_r, (int64_t)L->n_chunks + 1) &&
               dmalloc(&L->own_c, (int64_t)L->n_chunks + 1) &&
               dmalloc(&L->part, (int64_t)std::max(L->n_chunks, 1) * 2 * kMaxBatchTile) &&

@@ -86,6 +86,42 @@ __device__ __forceinline__ void stream4(const int32_t* __restrict__ p, uint32_t 
     }
 }
 
+// Index block of 4 consecutive entries: 16-bit indices (packed in two
+// registers, read from a zero-padded library stream, no end test) or 32-bit
+// indices (read with the end-of-array test).
+template <bool IDX16>
+struct IdxBlk;
+template <>
+struct IdxBlk<true> {
+    uint32_t lo, hi;
+    __device__ __forceinline__ void load(const uint16_t* p, uint32_t a0) {
+        const uint2 t = __ldcs(reinterpret_cast<const uint2*>(p + a0));
+        lo = t.x;
+        hi = t.y;
+    }
+    __device__ __forceinline__ int get(int j) const {
+        const uint32_t w = j < 2 ? lo : hi;
+        return (int)((j & 1) ? (w >> 16) : (w & 0xffffu));
+    }
+};
+template <>
+struct IdxBlk<false> {
+    int c[4];
+    __device__ __forceinline__ void load(const int32_t* p, uint32_t a0, uint32_t n) {
+        stream4(p, a0, n, c);
+    }
+    __device__ __forceinline__ int get(int j) const { return c[j]; }
+};
+
+// Four int32 entries of a zero-padded library stream (no end test).
+__device__ __forceinline__ void padded4(const int32_t* __restrict__ p, uint32_t a0, int (&w)[4]) {
+    const int4 t = __ldcs(reinterpret_cast<const int4*>(p + a0));
+    w[0] = t.x;
+    w[1] = t.y;
+    w[2] = t.z;
+    w[3] = t.w;
+}
+
 // Stage the operand transposed: dst[i*BP + beta] = src[beta*ld + i] for
 // beta < b, 0 for b <= beta < BP, for i < n.  Reads are coalesced over i;
 // U columns per thread are loaded before any is stored so that enough loads
@@ -150,12 +186,11 @@ __device__ __forceinline__ void stage_transposed(float* dst, const float* __rest
 // start of relative segment base+t and, optionally, that segment's bias.
 // Queried warp-uniformly; moving forward reloads the window.
 struct SegWindow {
-    const int32_t* seg_ptr;
-    const float* bias;
     int r_begin, nrows, base;
     uint32_t start;
     float b;
-    __device__ __forceinline__ void load(int rel, int lane) {
+    __device__ __forceinline__ void load(int rel, int lane, const int32_t* seg_ptr,
+                                         const float* bias) {
         base = rel;
         const int t = rel + lane;
         start = t <= nrows ? (uint32_t)__ldg(seg_ptr + r_begin + t) : 0u;
@@ -163,8 +198,9 @@ struct SegWindow {
     }
     // start of relative segment i; the window is kept so that segment i-1's
     // bias stays readable
-    __device__ __forceinline__ uint32_t bnd(int i, int lane) {
-        if (i - base >= 32) load(i - 1, lane);
+    __device__ __forceinline__ uint32_t bnd(int i, int lane, const int32_t* seg_ptr,
+                                            const float* bias) {
+        if (i - base >= 32) load(i - 1, lane, seg_ptr, bias);
         return __shfl_sync(0xffffffffu, start, i - base);
     }
     __device__ __forceinline__ float bias_of(int i) {

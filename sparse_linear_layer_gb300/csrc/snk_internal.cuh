@@ -13,6 +13,7 @@ constexpr int kThreads = 1024;       // SpMM / SDDMM block size: one block per S
 constexpr int kWarpsPerBlock = kThreads / kWarp;
 constexpr int kChunksPerSm = 32;     // merge-path chunks per SM (one per warp)
 constexpr int kMaxBatchTile = 64;    // batch columns handled by one launch
+constexpr int kStreamPad = 128;      // zero entries after library-owned streams
 
 // Device status word bits.
 constexpr int kStatRange = 1;
@@ -36,8 +37,13 @@ struct Layer {
     // topology (rebuilt at create and after each restructure)
     int32_t* row_ptr = nullptr;   // [out+1]
     int32_t* col_ptr = nullptr;   // [in+1]
-    int32_t* rows_c = nullptr;    // [nnz] row of the j-th entry in column order
-    int32_t* perm = nullptr;      // [nnz] canonical slot of the j-th entry in column order
+    int32_t* rows_c = nullptr;    // [nnz_pad] row of the j-th entry in column order
+    int32_t* perm = nullptr;      // [nnz_pad] canonical slot of the j-th entry in column order
+    // 16-bit copies of the index streams (when the dimension allows), read by
+    // the shared-memory kernels; padded with zeros so blocks never test the end
+    uint16_t* c16 = nullptr;      // [nnz_pad] canonical columns, if in <= 65536
+    uint16_t* rc16 = nullptr;     // [nnz_pad] rows in column order, if out <= 65536
+    int64_t nnz_pad = 0;          // round_up(nnz, 4) + kStreamPad
 
     // merge-path chunking of the canonical (row) and column orders
     int32_t chunk = 0;            // nnz per chunk

@@ -23,6 +23,7 @@ namespace snk {
 
 struct SddmmArgs {
     const int32_t* col;     // canonical column indices
+    const uint16_t* col16;  // the same as 16-bit, zero padded (shared-memory path)
     const int32_t* row_ptr; // [out+1]
     const int32_t* own;     // [n_chunks+1]
     int64_t nnz, out_f, in_f;
@@ -50,13 +51,17 @@ __device__ __forceinline__ void load_dy_row(const SddmmArgs& a, int r, int sub,
 }
 
 // One warp per chunk; the chunk's column indices stream as flat blocks of
-// 4*GPW entries with the next block prefetched.  The dY values of the current
-// row are in registers and the next row's are requested one row ahead.
+// 4*GPW entries held in D+1 register slots (D blocks in flight while one is
+// consumed; the slot loop is unrolled so slot indices are constants).  The dY
+// values of the current row are in registers and the next row's are
+// requested one row ahead.
 template <int BP, bool SMEM>
 __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
+    constexpr int D = 4;
+    constexpr int NS = D + 1;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
 
@@ -68,11 +73,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const bool active = q < a.n_chunks;
     uint32_t k0 = 0, k1 = 0;
-    int cc[4] = {0, 0, 0, 0};
+    IdxBlk<SMEM> ib[NS];
+    auto issue = [&](int s, uint32_t blk0) {
+        const uint32_t base = blk0 + 4 * grp;
+        if constexpr (SMEM) ib[s].load(a.col16, base);
+        else ib[s].load(a.col, base, nnz);
+    };
     if (active) {
         k0 = (uint32_t)q * chunk;
         k1 = min(k0 + chunk, nnz);
-        stream4(a.col, k0 + 4 * grp, nnz, cc);
+#pragma unroll
+        for (int s = 0; s < NS; ++s)
+            if (k0 + s * BLK < k1) issue(s, k0 + s * BLK);
     }
     if (a.db) {
         // bias gradient over the whole batch, sequential in batch order
@@ -93,30 +105,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     const int lo = a.own[q];
     const int hi = a.own[q + 1];
     const int r_begin = (lo > 0 && (uint32_t)a.row_ptr[lo] > k0) ? lo - 1 : lo;
-    SegWindow win{a.row_ptr, nullptr, r_begin, hi - r_begin, 0, 0u, 0.f};
-    win.load(0, lane);
+    SegWindow win{r_begin, hi - r_begin, 0, 0u, 0.f};
+    win.load(0, lane, a.row_ptr, nullptr);
     int i = 0;
-    uint32_t rs = win.bnd(0, lane), re = win.bnd(1, lane);
+    uint32_t rs = win.bnd(0, lane, a.row_ptr, nullptr), re = win.bnd(1, lane, a.row_ptr, nullptr);
     float dyr[VEC], dyn[VEC];
     load_dy_row<BP>(a, r_begin, sub, dyr);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) dyn[j] = 0.f;
     if (win.nrows > 1) load_dy_row<BP>(a, r_begin + 1, sub, dyn);
 
-    for (uint32_t base0 = k0; base0 < k1; base0 += BLK) {
-        const uint32_t base = base0 + 4 * grp;
-        int nc[4];
-        if (base0 + BLK < k1) stream4(a.col, base + BLK, nnz, nc);
-        const uint32_t blk_end = min(base0 + BLK, k1);
+    auto consume = [&](int s, uint32_t blk0) {
+        const uint32_t base = blk0 + 4 * grp;
+        const uint32_t blk_end = min(blk0 + BLK, k1);
         float res[4] = {0.f, 0.f, 0.f, 0.f};
         while (true) {
-            const uint32_t lo_k = max(rs, base0), hi_k = min(re, blk_end);
+            const uint32_t lo_k = max(rs, blk0), hi_k = min(re, blk_end);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t k = base + j;
                 const bool ok = k >= lo_k && k < hi_k;
                 float x[VEC];
-                const float* px = xsrc + (ok ? cc[j] : 0) * BP + sub * VEC;
+                const float* px = xsrc + (ok ? ib[s].get(j) : 0) * BP + sub * VEC;
                 if constexpr (SMEM) VecF<VEC>::load(px, x);
                 else VecF<VEC>::ldg(px, x);
                 float p = 0.f;
@@ -129,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
             if (min(re, k1) > blk_end) break;  // row continues in the next block
             if (++i >= win.nrows) break;
             rs = re;
-            re = win.bnd(i + 1, lane);
+            re = win.bnd(i + 1, lane, a.row_ptr, nullptr);
 #pragma unroll
             for (int j = 0; j < VEC; ++j) dyr[j] = dyn[j];
             if (i + 1 < win.nrows) load_dy_row<BP>(a, r_begin + i + 1, sub, dyn);
@@ -155,9 +165,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
                 }
             }
         }
-        if (base0 + BLK < k1) {
+    };
+
+    for (uint32_t base0 = k0; base0 < k1; base0 += NS * BLK) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) cc[j] = nc[j];
+        for (int s = 0; s < NS; ++s) {
+            const uint32_t blk0 = base0 + s * BLK;
+            if (blk0 < k1) {
+                consume(s, blk0);
+                if (blk0 + NS * BLK < k1) issue(s, blk0 + NS * BLK);
+            }
         }
     }
 }
@@ -182,7 +199,7 @@ template <int BP>
 static int launch_bp(Layer* L, SddmmArgs a, cudaStream_t s) {
     const size_t smem = (size_t)a.in_f * BP * sizeof(float);
     const int grid = (int)std::min<int64_t>(L->num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
-    if (smem <= (size_t)L->max_smem) {
+    if (smem <= (size_t)L->max_smem && a.col16) {
         auto fn = k_sddmm<BP, true>;
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -208,6 +225,7 @@ int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b,
     }
     SddmmArgs a{};
     a.col = L->c;
+    a.col16 = L->c16;
     a.row_ptr = L->row_ptr;
     a.own = L->own_r;
     a.nnz = L->nnz;

@@ -38,6 +38,7 @@ struct SpmmArgs {
     const float* val;       // stored values, canonical order
     const int32_t* perm;    // column-order -> canonical slot (transposed product) or null
     const int32_t* idx;     // operand index per stored entry (col, or row in column order)
+    const uint16_t* idx16;  // the same as 16-bit, zero padded (shared-memory path)
     const int32_t* seg_ptr; // [n_seg+1]
     const int32_t* own;     // [n_chunks+1]
     int64_t nnz;
@@ -118,14 +119,19 @@ __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[T
 
 // One warp per chunk.  The chunk's entries [k0, k1) are streamed as a flat
 // sequence of blocks of 4*GPW entries (each group of LPE lanes owns 4
-// consecutive entries of a block), with the next block's loads issued before
-// the current one is consumed.  The segment walk only masks entries; a block
-// that straddles segment boundaries is consumed once per segment it touches.
+// consecutive entries of a block).  Blocks sit in D+1 register slots: while
+// block j is consumed, blocks j+1 .. j+D are in flight (and, for the
+// transposed product, the values of block j+1 are being gathered).  The loop
+// over slots is unrolled so every slot index is a compile-time constant.  The
+// segment walk only masks entries; a block that straddles segment
+// boundaries is consumed once per segment it touches.
 template <int BP, bool GATHER, bool SMEM>
 __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
+    constexpr int D = GATHER ? 1 : 2;
+    constexpr int NS = D + 1;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
 
@@ -136,19 +142,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     const uint32_t chunk = (uint32_t)a.chunk;
     const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const bool active = q < a.n_chunks;
-
-    // first block of this warp's chunk, requested before the operand staging
-    // so that HBM is busy while shared memory fills
     uint32_t k0 = 0, k1 = 0;
-    int cc[4] = {0, 0, 0, 0};
-    float cw[4] = {0.f, 0.f, 0.f, 0.f};
-    int cp[4] = {0, 0, 0, 0};
+
+    IdxBlk<SMEM> ib[NS];
+    float wb[NS][4];
+    int pb[NS][4];
+    auto issue = [&](int s, uint32_t blk0) {
+        const uint32_t base = blk0 + 4 * grp;
+        if constexpr (SMEM) ib[s].load(a.idx16, base);
+        else ib[s].load(a.idx, base, nnz);
+        if constexpr (GATHER) padded4(a.perm, base, pb[s]);
+        else stream4(a.val, base, nnz, wb[s]);
+    };
+    auto gather = [&](int s, uint32_t blk0) {
+        const uint32_t base = blk0 + 4 * grp;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wb[s][j] = (base + j < k1) ? __ldg(a.val + pb[s][j]) : 0.f;
+    };
+
+    // the first blocks of this warp's chunk are requested before the operand
+    // staging, so that HBM is busy while shared memory fills
     if (active) {
         k0 = (uint32_t)q * chunk;
         k1 = min(k0 + chunk, nnz);
-        stream4(a.idx, k0 + 4 * grp, nnz, cc);
-        if constexpr (GATHER) stream4(a.perm, k0 + 4 * grp, nnz, cp);
-        else stream4(a.val, k0 + 4 * grp, nnz, cw);
+#pragma unroll
+        for (int s = 0; s < NS; ++s)
+            if (k0 + s * BLK < k1) issue(s, k0 + s * BLK);
     }
     if constexpr (SMEM) {
         stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, kThreads);
@@ -156,60 +175,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     }
     if (!active) return;
     const float* xsrc = SMEM ? xs : a.xt;
+    if constexpr (GATHER) gather(0, k0);
 
     const int lo = a.own[q];
     const int hi = a.own[q + 1];
     const int r_begin = (lo > 0 && (uint32_t)a.seg_ptr[lo] > k0) ? lo - 1 : lo;
-    SegWindow win{a.seg_ptr, a.bias, r_begin, hi - r_begin, 0, 0u, 0.f};
-    win.load(0, lane);
+    SegWindow win{r_begin, hi - r_begin, 0, 0u, 0.f};
+    win.load(0, lane, a.seg_ptr, a.bias);
     int i = 0;
-    uint32_t rs = win.bnd(0, lane), re = win.bnd(1, lane);
+    uint32_t rs = win.bnd(0, lane, a.seg_ptr, a.bias), re = win.bnd(1, lane, a.seg_ptr, a.bias);
     float acc[VEC];
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
 
-    for (uint32_t base0 = k0; base0 < k1; base0 += BLK) {
-        const uint32_t base = base0 + 4 * grp;
-        if constexpr (GATHER) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) cw[j] = (base + j < k1) ? __ldg(a.val + cp[j]) : 0.f;
-        }
-        // prefetch the next block
-        int nc[4], np[4];
-        float nw[4];
-        const uint32_t nbase = base + BLK;
-        if (base0 + BLK < k1) {
-            stream4(a.idx, nbase, nnz, nc);
-            if constexpr (GATHER) stream4(a.perm, nbase, nnz, np);
-            else stream4(a.val, nbase, nnz, nw);
-        }
-        const uint32_t blk_end = min(base0 + BLK, k1);
+    auto consume = [&](int s, uint32_t blk0) {
+        const uint32_t base = blk0 + 4 * grp;
+        const uint32_t blk_end = min(blk0 + BLK, k1);
         while (true) {
-            const uint32_t lo_k = max(rs, base0), hi_k = min(re, blk_end);
+            const uint32_t lo_k = max(rs, blk0), hi_k = min(re, blk_end);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t k = base + j;
                 if (k >= lo_k && k < hi_k) {
                     float x[VEC];
-                    const float* px = xsrc + cc[j] * BP + sub * VEC;
+                    const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
                     if constexpr (SMEM) VecF<VEC>::load(px, x);
                     else VecF<VEC>::ldg(px, x);
 #pragma unroll
-                    for (int t = 0; t < VEC; ++t) acc[t] = fmaf(cw[j], x[t], acc[t]);
+                    for (int t = 0; t < VEC; ++t) acc[t] = fmaf(wb[s][j], x[t], acc[t]);
                 }
             }
             if (min(re, k1) > blk_end) break;  // segment continues in the next block
             finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub);
             if (++i >= win.nrows) break;
             rs = re;
-            re = win.bnd(i + 1, lane);
+            re = win.bnd(i + 1, lane, a.seg_ptr, a.bias);
             if (rs >= blk_end) break;
         }
+    };
+
+    for (uint32_t base0 = k0; base0 < k1; base0 += NS * BLK) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            cc[j] = nc[j];
-            if constexpr (GATHER) cp[j] = np[j];
-            else cw[j] = nw[j];
+        for (int s = 0; s < NS; ++s) {
+            const uint32_t blk0 = base0 + s * BLK;
+            if (blk0 < k1) {
+                if constexpr (GATHER) {
+                    if (blk0 + BLK < k1) gather((s + 1) % NS, blk0 + BLK);
+                }
+                consume(s, blk0);
+                if (blk0 + NS * BLK < k1) issue(s, blk0 + NS * BLK);
+            }
         }
     }
     // segments that start at the end of the chunk (empty here)
@@ -217,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
         finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub);
         if (++i >= win.nrows) break;
         rs = re;
-        re = win.bnd(i + 1, lane);
+        re = win.bnd(i + 1, lane, a.seg_ptr, a.bias);
     }
 }
 
@@ -239,7 +254,7 @@ template <int BP, bool GATHER>
 static int launch_bp(Layer* L, SpmmArgs a, cudaStream_t s) {
     const size_t smem = (size_t)a.n_src * BP * sizeof(float);
     const int grid = (int)std::min<int64_t>(L->num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
-    if (smem <= (size_t)L->max_smem) {
+    if (smem <= (size_t)L->max_smem && a.idx16) {
         auto fn = k_spmm<BP, GATHER, true>;
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -293,6 +308,7 @@ int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float
     a.val = L->v;
     a.perm = nullptr;
     a.idx = L->c;
+    a.idx16 = L->c16;
     a.seg_ptr = L->row_ptr;
     a.own = L->own_r;
     a.nnz = L->nnz;
@@ -313,6 +329,7 @@ int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaS
     a.val = L->v;
     a.perm = L->perm;
     a.idx = L->rows_c;
+    a.idx16 = L->rc16;
     a.seg_ptr = L->col_ptr;
     a.own = L->own_c;
     a.nnz = L->nnz;

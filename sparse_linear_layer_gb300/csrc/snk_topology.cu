@@ -335,6 +335,14 @@ __global__ void k_gather_rows(const uint32_t* __restrict__ perm_u, const int32_t
     }
 }
 
+// 16-bit copy of an index stream, zero-padded to n_pad entries.
+__global__ void k_narrow16(const int32_t* __restrict__ src, int64_t n, int64_t n_pad,
+                           uint16_t* __restrict__ dst) {
+    for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n_pad;
+         k += (int64_t)gridDim.x * blockDim.x)
+        dst[k] = k < n ? (uint16_t)src[k] : (uint16_t)0;
+}
+
 // own[q] = first segment whose start pointer is >= q*chunk (n_seg if none);
 // own[n_chunks] = n_seg.
 __global__ void k_own(const int32_t* __restrict__ ptr, int64_t n_seg, int32_t chunk,
@@ -428,6 +436,17 @@ int build_topology(Layer* L, cudaStream_t s, bool validate) {
     } else {
         k_fill_ptr<<<1, T, 0, s>>>(L->r, 0, L->in_f, L->col_ptr);
     }
+
+    // zero padding after the library-owned streams, and their 16-bit copies
+    if (L->nnz_pad > n) {
+        cudaMemsetAsync(L->perm + n, 0, (L->nnz_pad - n) * sizeof(int32_t), s);
+        cudaMemsetAsync(L->rows_c + n, 0, (L->nnz_pad - n) * sizeof(int32_t), s);
+    }
+    if (L->c16)
+        k_narrow16<<<grid_for(L->nnz_pad, T, L->num_sms), T, 0, s>>>(L->c, n, L->nnz_pad, L->c16);
+    if (L->rc16)
+        k_narrow16<<<grid_for(L->nnz_pad, T, L->num_sms), T, 0, s>>>(L->rows_c, n, L->nnz_pad,
+                                                                     L->rc16);
 
     if (L->n_chunks > 0) {
         k_own<<<grid_for(L->n_chunks + 1, T, L->num_sms), T, 0, s>>>(L->row_ptr, L->out_f, L->chunk,
