@@ -9,9 +9,11 @@
 namespace snk {
 
 constexpr int kWarp = 32;
-constexpr int kThreads = 1024;       // SpMM / SDDMM block size: one block per SM
+// SpMM / SDDMM blocks: one per SM, 16 warps of up to 128 registers, so each
+// warp can keep several blocks of its stream in flight in registers.
+constexpr int kThreads = 512;
 constexpr int kWarpsPerBlock = kThreads / kWarp;
-constexpr int kChunksPerSm = 32;     // merge-path chunks per SM (one per warp)
+constexpr int kChunksPerSm = kWarpsPerBlock;   // merge-path chunks per SM (one per warp)
 constexpr int kMaxBatchTile = 64;    // batch columns handled by one launch
 constexpr int kStreamPad = 128;      // zero entries after library-owned streams
 

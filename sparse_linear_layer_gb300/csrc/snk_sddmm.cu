@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
-    constexpr int D = 4;
+    constexpr int D = 8;
     constexpr int NS = D + 1;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
