@@ -46,9 +46,9 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, verbose: bool, obj_dir: str, extra) -> str:
+    obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,19 +59,24 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=None, out: str | None = None) -> str:
+    """Compile libsnk.so.  extra_flags (e.g. ["-DSNK_PIPE_FWD=3"]) and out
+    (another library path) build a variant beside the default library."""
+    extra = list(extra_flags or [])
+    lib = out or LIB
+    if not force and not extra and out is None and up_to_date():
         return LIB
-    os.makedirs(OBJ, exist_ok=True)
+    obj_dir = OBJ if out is None else out + ".objs"
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, obj_dir, extra), srcs))
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -9,9 +9,25 @@
 namespace snk {
 
 constexpr int kWarp = 32;
-// SpMM / SDDMM blocks: one per SM, 16 warps of up to 128 registers, so each
-// warp can keep several blocks of its stream in flight in registers.
-constexpr int kThreads = 512;
+// Tuning parameters (compile-time; the defaults are the measured best on
+// GB300 for 10000x10000 layers at batch 1..64).
+#ifndef SNK_THREADS
+#define SNK_THREADS 1024   // SpMM / SDDMM block size; one block per SM
+#endif
+#ifndef SNK_PIPE_FWD
+#define SNK_PIPE_FWD 2     // stream blocks in flight ahead of the consumed one (forward)
+#endif
+#ifndef SNK_PIPE_DX
+#define SNK_PIPE_DX 1      // the same for the transposed product
+#endif
+#ifndef SNK_PIPE_DW
+#define SNK_PIPE_DW 4      // the same for the weight gradient
+#endif
+#ifndef SNK_IDX16
+#define SNK_IDX16 1        // read 16-bit index copies on the shared-memory path
+#endif
+
+constexpr int kThreads = SNK_THREADS;
 constexpr int kWarpsPerBlock = kThreads / kWarp;
 constexpr int kChunksPerSm = kWarpsPerBlock;   // merge-path chunks per SM (one per warp)
 constexpr int kMaxBatchTile = 64;    // batch columns handled by one launch

@@ -57,10 +57,11 @@ __device__ __forceinline__ void load_dy_row(const SddmmArgs& a, int r, int sub,
 // requested one row ahead.
 template <int BP, bool SMEM>
 __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
+    constexpr bool I16 = SMEM && SNK_IDX16;
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
-    constexpr int D = 8;
+    constexpr int D = SNK_PIPE_DW;
     constexpr int NS = D + 1;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
@@ -73,10 +74,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const bool active = q < a.n_chunks;
     uint32_t k0 = 0, k1 = 0;
-    IdxBlk<SMEM> ib[NS];
+    IdxBlk<I16> ib[NS];
     auto issue = [&](int s, uint32_t blk0) {
         const uint32_t base = blk0 + 4 * grp;
-        if constexpr (SMEM) ib[s].load(a.col16, base);
+        if constexpr (I16) ib[s].load(a.col16, base);
         else ib[s].load(a.col, base, nnz);
     };
     if (active) {
@@ -119,7 +120,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
         const uint32_t base = blk0 + 4 * grp;
         const uint32_t blk_end = min(blk0 + BLK, k1);
         float res[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool interior = rs <= blk0 && blk0 + BLK < re && blk0 + BLK <= k1;
         while (true) {
+            if (interior) {
+                // every entry of the block belongs to the current row, which
+                // continues past the block
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float x[VEC];
+                    const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
+                    if constexpr (SMEM) VecF<VEC>::load(px, x);
+                    else VecF<VEC>::ldg(px, x);
+                    float p = 0.f;
+#pragma unroll
+                    for (int t = 0; t < VEC; ++t) p = fmaf(dyr[t], x[t], p);
+#pragma unroll
+                    for (int o = 1; o < LPE; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                    res[j] = p;
+                }
+                break;
+            }
             const uint32_t lo_k = max(rs, blk0), hi_k = min(re, blk_end);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {

@@ -127,10 +127,11 @@ __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[T
 // boundaries is consumed once per segment it touches.
 template <int BP, bool GATHER, bool SMEM>
 __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
+    constexpr bool I16 = SMEM && SNK_IDX16;
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
-    constexpr int D = GATHER ? 3 : 6;
+    constexpr int D = GATHER ? SNK_PIPE_DX : SNK_PIPE_FWD;
     constexpr int NS = D + 1;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
@@ -144,12 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     const bool active = q < a.n_chunks;
     uint32_t k0 = 0, k1 = 0;
 
-    IdxBlk<SMEM> ib[NS];
+    IdxBlk<I16> ib[NS];
     float wb[NS][4];
     int pb[NS][4];
     auto issue = [&](int s, uint32_t blk0) {
         const uint32_t base = blk0 + 4 * grp;
-        if constexpr (SMEM) ib[s].load(a.idx16, base);
+        if constexpr (I16) ib[s].load(a.idx16, base);
         else ib[s].load(a.idx, base, nnz);
         if constexpr (GATHER) padded4(a.perm, base, pb[s]);
         else stream4(a.val, base, nnz, wb[s]);
@@ -190,6 +191,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
 
     auto consume = [&](int s, uint32_t blk0) {
         const uint32_t base = blk0 + 4 * grp;
+        if (rs <= blk0 && blk0 + BLK < re && blk0 + BLK <= k1) {
+            // interior block: every entry belongs to the current segment,
+            // which continues past the block
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float x[VEC];
+                const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
+                if constexpr (SMEM) VecF<VEC>::load(px, x);
+                else VecF<VEC>::ldg(px, x);
+#pragma unroll
+                for (int t = 0; t < VEC; ++t) acc[t] = fmaf(wb[s][j], x[t], acc[t]);
+            }
+            return;
+        }
         const uint32_t blk_end = min(blk0 + BLK, k1);
         while (true) {
             const uint32_t lo_k = max(rs, blk0), hi_k = min(re, blk_end);
