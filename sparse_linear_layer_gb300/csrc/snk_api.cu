@@ -24,7 +24,7 @@ static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)
 static void free_layer(Layer* L) {
     if (!L) return;
     free_restructure(L);
-    void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->c16, L->rc16, L->own_r, L->own_c,
+    void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->c16, L->rc16, L->desc_r, L->desc_c,
                     L->part, L->cnt, L->xt, L->status, L->sort_keys, L->sort_vals,
                     L->col_keys, L->col_vals, L->tile_hist};
     for (void* p : ptrs)
@@ -105,8 +105,8 @@ int snk_create(snk_handle* handle, int64_t out_f, int64_t in_f, int64_t nnz, flo
               dmalloc(&L->rows_c, L->nnz_pad) && dmalloc(&L->perm, L->nnz_pad) &&
               (in_f > 65536 || dmalloc(&L->c16, L->nnz_pad)) &&
               (out_f > 65536 || dmalloc(&L->rc16, L->nnz_pad)) &&
-              dmalloc(&L->own_r, (int64_t)L->n_chunks + 1) &&
-              dmalloc(&L->own_c, (int64_t)L->n_chunks + 1) &&
+              dmalloc(&L->desc_r, (int64_t)L->n_chunks) &&
+              dmalloc(&L->desc_c, (int64_t)L->n_chunks) &&
               dmalloc(&L->part, (int64_t)std::max(L->n_chunks, 1) * 2 * kMaxBatchTile) &&
               dmalloc(&L->cnt, n_max) && dmalloc(&L->xt, n_max * kMaxBatchTile) &&
               dmalloc(&L->status, 1) &&

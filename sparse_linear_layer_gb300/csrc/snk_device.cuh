@@ -123,62 +123,78 @@ __device__ __forceinline__ void padded4(const int32_t* __restrict__ p, uint32_t 
 }
 
 // Stage the operand transposed: dst[i*BP + beta] = src[beta*ld + i] for
-// beta < b, 0 for b <= beta < BP, for i < n.  Reads are coalesced over i;
-// U columns per thread are loaded before any is stored so that enough loads
-// are in flight to hide the latency of the (L2-resident) source.
+// beta < b, 0 for b <= beta < BP, for i < n.  When the rows of src are
+// 16-byte aligned, groups of 4 columns are read with 128-bit loads (one per
+// source row) and transposed in registers, so each thread issues 4x fewer
+// loads; the remaining columns (and unaligned sources) use 32-bit loads.
+// Several groups are loaded before any is stored, to keep loads in flight.
 template <int BP>
 __device__ __forceinline__ void stage_transposed(float* dst, const float* __restrict__ src,
                                                  int64_t ld, int b, int64_t n, int tid,
                                                  int nthreads) {
-    // at most 8 float4 (BP >= 4) or 16 floats (BP < 4) are held per thread
-    constexpr int Q = BP >= 4 ? BP / 4 : 1;   // float4 per column
-    constexpr int QB = Q < 8 ? Q : 8;          // float4 per column per batch
-    constexpr int U = BP >= 4 ? 8 / QB : 16 / BP;
-    for (int64_t i0 = tid; i0 < n; i0 += (int64_t)nthreads * U) {
-        if constexpr (BP >= 4) {
-#pragma unroll
-            for (int qb = 0; qb < Q; qb += QB) {
-                float4 t[U][QB];
+    int64_t n_vec = 0;
+    if ((((uintptr_t)src) & 15) == 0 && (ld & 3) == 0) n_vec = n & ~(int64_t)3;
+    const int64_t groups = n_vec >> 2;
+    if constexpr (BP >= 4) {
+        constexpr int U = 2;
+        for (int qb = 0; qb < BP / 4; ++qb) {
+            const int r0 = 4 * qb;
+            for (int64_t g0 = tid; g0 < groups; g0 += (int64_t)nthreads * U) {
+                float4 t[U][4];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int64_t i = i0 + (int64_t)u * nthreads;
+                    const int64_t g = g0 + (int64_t)u * nthreads;
 #pragma unroll
-                    for (int q = 0; q < QB; ++q) {
-                        const int bq = 4 * (qb + q);
-                        const bool ok = i < n;
-                        t[u][q].x = ok && bq + 0 < b ? __ldg(src + (bq + 0) * ld + i) : 0.f;
-                        t[u][q].y = ok && bq + 1 < b ? __ldg(src + (bq + 1) * ld + i) : 0.f;
-                        t[u][q].z = ok && bq + 2 < b ? __ldg(src + (bq + 2) * ld + i) : 0.f;
-                        t[u][q].w = ok && bq + 3 < b ? __ldg(src + (bq + 3) * ld + i) : 0.f;
-                    }
+                    for (int rr = 0; rr < 4; ++rr)
+                        t[u][rr] = (g < groups && r0 + rr < b)
+                                       ? __ldg(reinterpret_cast<const float4*>(src + (r0 + rr) * ld) + g)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int64_t i = i0 + (int64_t)u * nthreads;
-                    if (i < n) {
-#pragma unroll
-                        for (int q = 0; q < QB; ++q)
-                            *reinterpret_cast<float4*>(dst + i * BP + 4 * (qb + q)) = t[u][q];
+                    const int64_t g = g0 + (int64_t)u * nthreads;
+                    if (g < groups) {
+                        float* d = dst + 4 * g * BP + r0;
+                        *reinterpret_cast<float4*>(d + 0 * BP) = make_float4(t[u][0].x, t[u][1].x, t[u][2].x, t[u][3].x);
+                        *reinterpret_cast<float4*>(d + 1 * BP) = make_float4(t[u][0].y, t[u][1].y, t[u][2].y, t[u][3].y);
+                        *reinterpret_cast<float4*>(d + 2 * BP) = make_float4(t[u][0].z, t[u][1].z, t[u][2].z, t[u][3].z);
+                        *reinterpret_cast<float4*>(d + 3 * BP) = make_float4(t[u][0].w, t[u][1].w, t[u][2].w, t[u][3].w);
                     }
-                }
-            }
-        } else {
-            float t[U][BP];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t i = i0 + (int64_t)u * nthreads;
-#pragma unroll
-                for (int q = 0; q < BP; ++q) t[u][q] = (i < n && q < b) ? __ldg(src + q * ld + i) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t i = i0 + (int64_t)u * nthreads;
-                if (i < n) {
-                    if constexpr (BP == 2) *reinterpret_cast<float2*>(dst + i * 2) = make_float2(t[u][0], t[u][1]);
-                    else dst[i] = t[u][0];
                 }
             }
         }
+    } else {
+        constexpr int U = BP == 2 ? 4 : 8;
+        for (int64_t g0 = tid; g0 < groups; g0 += (int64_t)nthreads * U) {
+            float4 t0[U], t1[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = g0 + (int64_t)u * nthreads;
+                t0[u] = g < groups ? __ldg(reinterpret_cast<const float4*>(src) + g)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (BP == 2)
+                    t1[u] = (g < groups && b > 1) ? __ldg(reinterpret_cast<const float4*>(src + ld) + g)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = g0 + (int64_t)u * nthreads;
+                if (g < groups) {
+                    if constexpr (BP == 2) {
+                        float4* d = reinterpret_cast<float4*>(dst + 8 * g);
+                        d[0] = make_float4(t0[u].x, t1[u].x, t0[u].y, t1[u].y);
+                        d[1] = make_float4(t0[u].z, t1[u].z, t0[u].w, t1[u].w);
+                    } else {
+                        reinterpret_cast<float4*>(dst)[g] = t0[u];
+                    }
+                }
+            }
+        }
+    }
+    // remaining columns, 32-bit loads
+    for (int64_t i = n_vec + tid; i < n; i += nthreads) {
+#pragma unroll
+        for (int beta = 0; beta < BP; ++beta) dst[i * BP + beta] = beta < b ? __ldg(src + beta * ld + i) : 0.f;
     }
 }
 

@@ -66,8 +66,8 @@ struct Layer {
     // merge-path chunking of the canonical (row) and column orders
     int32_t chunk = 0;            // nnz per chunk
     int32_t n_chunks = 0;         // ceil(nnz / chunk)
-    int32_t* own_r = nullptr;     // [n_chunks+1] first row whose start lies in chunk q
-    int32_t* own_c = nullptr;     // [n_chunks+1] same for columns
+    int2* desc_r = nullptr;       // [n_chunks] (first row touched by chunk q, end of its rows)
+    int2* desc_c = nullptr;       // [n_chunks] the same for columns
 
     // scratch of the SpMM kernels
     float* part = nullptr;        // [n_chunks * 2 * kMaxBatchTile] split-segment partials

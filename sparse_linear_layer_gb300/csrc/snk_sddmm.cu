@@ -25,7 +25,7 @@ struct SddmmArgs {
     const int32_t* col;     // canonical column indices
     const uint16_t* col16;  // the same as 16-bit, zero padded (shared-memory path)
     const int32_t* row_ptr; // [out+1]
-    const int32_t* own;     // [n_chunks+1]
+    const int2* desc;       // [n_chunks] (first row touched, one past the last)
     int64_t nnz, out_f, in_f;
     int b;                  // batch columns of this tile
     int chunk, n_chunks;
@@ -80,12 +80,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
         if constexpr (I16) ib[s].load(a.col16, base);
         else ib[s].load(a.col, base, nnz);
     };
+    SegWindow win{0, 0, 0, 0u, 0.f};
     if (active) {
         k0 = (uint32_t)q * chunk;
         k1 = min(k0 + chunk, nnz);
 #pragma unroll
         for (int s = 0; s < NS; ++s)
             if (k0 + s * BLK < k1) issue(s, k0 + s * BLK);
+        const int2 dsc = a.desc[q];
+        win.r_begin = dsc.x;
+        win.nrows = dsc.y - dsc.x;
+        win.load(0, lane, a.row_ptr, nullptr);
     }
     if (a.db) {
         // bias gradient over the whole batch, sequential in batch order
@@ -103,11 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     if (!active) return;
     const float* xsrc = SMEM ? xs : a.xt;
 
-    const int lo = a.own[q];
-    const int hi = a.own[q + 1];
-    const int r_begin = (lo > 0 && (uint32_t)a.row_ptr[lo] > k0) ? lo - 1 : lo;
-    SegWindow win{r_begin, hi - r_begin, 0, 0u, 0.f};
-    win.load(0, lane, a.row_ptr, nullptr);
+    const int r_begin = win.r_begin;
     int i = 0;
     uint32_t rs = win.bnd(0, lane, a.row_ptr, nullptr), re = win.bnd(1, lane, a.row_ptr, nullptr);
     float dyr[VEC], dyn[VEC];
@@ -247,7 +248,7 @@ int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b,
     a.col = L->c;
     a.col16 = L->c16;
     a.row_ptr = L->row_ptr;
-    a.own = L->own_r;
+    a.desc = L->desc_r;
     a.nnz = L->nnz;
     a.out_f = L->out_f;
     a.in_f = L->in_f;

@@ -40,7 +40,7 @@ struct SpmmArgs {
     const int32_t* idx;     // operand index per stored entry (col, or row in column order)
     const uint16_t* idx16;  // the same as 16-bit, zero padded (shared-memory path)
     const int32_t* seg_ptr; // [n_seg+1]
-    const int32_t* own;     // [n_chunks+1]
+    const int2* desc;       // [n_chunks] (first segment touched, one past the last)
     int64_t nnz;
     int64_t n_seg;          // output length per batch row
     int64_t n_src;          // operand length per batch row
@@ -55,14 +55,23 @@ struct SpmmArgs {
     int32_t* cnt;           // [n_seg]
 };
 
+// A segment cut by a chunk boundary, whose partial sum this chunk has
+// written to its slot (0: the segment entered from the previous chunk,
+// 1: the segment that leaves into the next one).
+struct Pending {
+    int r;
+    uint32_t rs, re;
+};
+
 // Finish one output segment: reduce the per-lane partial sums across the
-// warp's groups, then either write the result or, for a segment cut by a
-// chunk boundary, publish this chunk's partial and let the last arriving
-// chunk add all partials in chunk order.
+// warp's groups; write the result, or, for a segment cut by a chunk boundary,
+// store this chunk's partial in its slot and remember the segment so that the
+// arrival is announced once, after the chunk's last block.
 template <int BP>
 __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[Tile<BP>::VEC],
                                                int r, uint32_t rs, uint32_t re, uint32_t k0,
-                                               uint32_t k1, int q, float bo, int lane, int sub) {
+                                               uint32_t k1, int q, float bo, int lane, int sub,
+                                               Pending (&pend)[2]) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE;
 #pragma unroll
@@ -79,42 +88,60 @@ __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[T
             }
         }
     } else {
-        const uint32_t chunk = (uint32_t)a.chunk;
-        const int64_t q_first = rs / chunk;
-        const int64_t q_last = (re - 1) / chunk;
         const int slot = (rs < k0) ? 0 : 1;
         if (lane < LPE) {
             float* my = a.part + ((int64_t)q * 2 + slot) * BP + sub * VEC;
 #pragma unroll
             for (int j = 0; j < VEC; ++j) my[j] = acc[j];
         }
-        __threadfence();
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(a.cnt + r, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == (int)(q_last - q_first)) {
-            __threadfence();
-            if (lane < LPE) {
-                float sum[VEC];
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) sum[j] = 0.f;
-                for (int64_t qq = q_first; qq <= q_last; ++qq) {
-                    const float* pp = a.part + (qq * 2 + (qq == q_first ? 1 : 0)) * BP + sub * VEC;
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j) sum[j] += __ldcg(pp + j);
-                }
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const int beta = sub * VEC + j;
-                    if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = sum[j] + bo;
-                }
-            }
-            if (lane == 0) a.cnt[r] = 0;
-        }
+        pend[slot] = Pending{r, rs, re};
     }
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+}
+
+// After the chunk: one fence makes this chunk's partials visible, then each
+// cut segment counts its arrival; the chunk that arrives last adds all
+// partials of the segment in chunk order (so the sum does not depend on
+// timing), writes the output and resets the counter.
+template <int BP>
+__device__ __forceinline__ void publish_partials(const SpmmArgs& a, const Pending (&pend)[2],
+                                                 int lane, int sub) {
+    using TL = Tile<BP>;
+    constexpr int VEC = TL::VEC, LPE = TL::LPE;
+    if (pend[0].r < 0 && pend[1].r < 0) return;
+    __threadfence();
+    __syncwarp();
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        if (pend[p].r < 0) continue;
+        const int r = pend[p].r;
+        const uint32_t chunk = (uint32_t)a.chunk;
+        const int64_t q_first = pend[p].rs / chunk;
+        const int64_t q_last = (pend[p].re - 1) / chunk;
+        int old = 0;
+        if (lane == 0) old = atomicAdd(a.cnt + r, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != (int)(q_last - q_first)) continue;
+        __threadfence();
+        if (lane < LPE) {
+            float sum[VEC];
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) sum[j] = 0.f;
+            for (int64_t qq = q_first; qq <= q_last; ++qq) {
+                const float* pp = a.part + (qq * 2 + (qq == q_first ? 1 : 0)) * BP + sub * VEC;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) sum[j] += __ldcg(pp + j);
+            }
+            const float bo = a.bias ? __ldg(a.bias + r) : 0.f;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const int beta = sub * VEC + j;
+                if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = sum[j] + bo;
+            }
+        }
+        if (lane == 0) a.cnt[r] = 0;
+    }
 }
 
 // One warp per chunk.  The chunk's entries [k0, k1) are streamed as a flat
@@ -122,9 +149,9 @@ __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[T
 // consecutive entries of a block).  Blocks sit in D+1 register slots: while
 // block j is consumed, blocks j+1 .. j+D are in flight (and, for the
 // transposed product, the values of block j+1 are being gathered).  The loop
-// over slots is unrolled so every slot index is a compile-time constant.  The
-// segment walk only masks entries; a block that straddles segment
-// boundaries is consumed once per segment it touches.
+// over slots is unrolled so every slot index is a compile-time constant.  A
+// block inside one segment is consumed without masks; a block that straddles
+// segment boundaries is consumed once per segment it touches.
 template <int BP, bool GATHER, bool SMEM>
 __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     constexpr bool I16 = SMEM && SNK_IDX16;
@@ -161,14 +188,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
         for (int j = 0; j < 4; ++j) wb[s][j] = (base + j < k1) ? __ldg(a.val + pb[s][j]) : 0.f;
     };
 
-    // the first blocks of this warp's chunk are requested before the operand
-    // staging, so that HBM is busy while shared memory fills
+    // Everything that only depends on the chunk is requested before the
+    // operand staging: the first blocks of the stream, the chunk descriptor
+    // and the first window of segment starts (and biases).
+    SegWindow win{0, 0, 0, 0u, 0.f};
     if (active) {
         k0 = (uint32_t)q * chunk;
         k1 = min(k0 + chunk, nnz);
 #pragma unroll
         for (int s = 0; s < NS; ++s)
             if (k0 + s * BLK < k1) issue(s, k0 + s * BLK);
+        const int2 dsc = a.desc[q];
+        win.r_begin = dsc.x;
+        win.nrows = dsc.y - dsc.x;
+        win.load(0, lane, a.seg_ptr, a.bias);
     }
     if constexpr (SMEM) {
         stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, kThreads);
@@ -178,16 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     const float* xsrc = SMEM ? xs : a.xt;
     if constexpr (GATHER) gather(0, k0);
 
-    const int lo = a.own[q];
-    const int hi = a.own[q + 1];
-    const int r_begin = (lo > 0 && (uint32_t)a.seg_ptr[lo] > k0) ? lo - 1 : lo;
-    SegWindow win{r_begin, hi - r_begin, 0, 0u, 0.f};
-    win.load(0, lane, a.seg_ptr, a.bias);
+    const int r_begin = win.r_begin;
     int i = 0;
     uint32_t rs = win.bnd(0, lane, a.seg_ptr, a.bias), re = win.bnd(1, lane, a.seg_ptr, a.bias);
     float acc[VEC];
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+    Pending pend[2] = {Pending{-1, 0u, 0u}, Pending{-1, 0u, 0u}};
 
     auto consume = [&](int s, uint32_t blk0) {
         const uint32_t base = blk0 + 4 * grp;
@@ -221,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
                 }
             }
             if (min(re, k1) > blk_end) break;  // segment continues in the next block
-            finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub);
+            finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub,
+                               pend);
             if (++i >= win.nrows) break;
             rs = re;
             re = win.bnd(i + 1, lane, a.seg_ptr, a.bias);
@@ -244,11 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     }
     // segments that start at the end of the chunk (empty here)
     while (i < win.nrows) {
-        finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub);
+        finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub, pend);
         if (++i >= win.nrows) break;
         rs = re;
         re = win.bnd(i + 1, lane, a.seg_ptr, a.bias);
     }
+    publish_partials<BP>(a, pend, lane, sub);
 }
 
 // Transposed copy of the operand for the global-memory path.
@@ -325,7 +357,7 @@ int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float
     a.idx = L->c;
     a.idx16 = L->c16;
     a.seg_ptr = L->row_ptr;
-    a.own = L->own_r;
+    a.desc = L->desc_r;
     a.nnz = L->nnz;
     a.n_seg = L->out_f;
     a.n_src = L->in_f;
@@ -346,7 +378,7 @@ int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaS
     a.idx = L->rows_c;
     a.idx16 = L->rc16;
     a.seg_ptr = L->col_ptr;
-    a.own = L->own_c;
+    a.desc = L->desc_c;
     a.nnz = L->nnz;
     a.n_seg = L->in_f;
     a.n_src = L->out_f;

@@ -343,23 +343,28 @@ __global__ void k_narrow16(const int32_t* __restrict__ src, int64_t n, int64_t n
         dst[k] = k < n ? (uint16_t)src[k] : (uint16_t)0;
 }
 
-// own[q] = first segment whose start pointer is >= q*chunk (n_seg if none);
-// own[n_chunks] = n_seg.
-__global__ void k_own(const int32_t* __restrict__ ptr, int64_t n_seg, int32_t chunk,
-                      int32_t n_chunks, int32_t* __restrict__ own) {
-    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q <= n_chunks; q += gridDim.x * blockDim.x) {
-        if (q == n_chunks) {
-            own[q] = (int32_t)n_seg;
-            continue;
-        }
-        int64_t target = (int64_t)q * chunk;
-        int64_t lo = 0, hi = n_seg;
-        while (lo < hi) {
-            int64_t mid = (lo + hi) >> 1;
-            if ((int64_t)ptr[mid] < target) lo = mid + 1;
-            else hi = mid;
-        }
-        own[q] = (int32_t)lo;
+// Chunk descriptor: chunk q covers entries [q*chunk, (q+1)*chunk).  It owns
+// the segments whose start lies in that range (the last chunk also owns the
+// empty segments at the very end) and continues the segment that runs into
+// it from before.  desc[q] = (first segment it touches, one past its last).
+__device__ __forceinline__ int64_t lower_bound_ptr(const int32_t* ptr, int64_t n_seg, int64_t t) {
+    int64_t lo = 0, hi = n_seg;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)ptr[mid] < t) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void k_desc(const int32_t* __restrict__ ptr, int64_t n_seg, int32_t chunk,
+                       int32_t n_chunks, int2* __restrict__ desc) {
+    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n_chunks; q += gridDim.x * blockDim.x) {
+        const int64_t k0 = (int64_t)q * chunk;
+        const int64_t lo = lower_bound_ptr(ptr, n_seg, k0);
+        const int64_t hi = (q + 1 == n_chunks) ? n_seg : lower_bound_ptr(ptr, n_seg, k0 + chunk);
+        const int64_t first = (lo > 0 && (int64_t)ptr[lo] > k0) ? lo - 1 : lo;
+        desc[q] = make_int2((int)first, (int)hi);
     }
 }
 
@@ -449,10 +454,10 @@ int build_topology(Layer* L, cudaStream_t s, bool validate) {
                                                                      L->rc16);
 
     if (L->n_chunks > 0) {
-        k_own<<<grid_for(L->n_chunks + 1, T, L->num_sms), T, 0, s>>>(L->row_ptr, L->out_f, L->chunk,
-                                                                     L->n_chunks, L->own_r);
-        k_own<<<grid_for(L->n_chunks + 1, T, L->num_sms), T, 0, s>>>(L->col_ptr, L->in_f, L->chunk,
-                                                                     L->n_chunks, L->own_c);
+        k_desc<<<grid_for(L->n_chunks, T, L->num_sms), T, 0, s>>>(L->row_ptr, L->out_f, L->chunk,
+                                                                  L->n_chunks, L->desc_r);
+        k_desc<<<grid_for(L->n_chunks, T, L->num_sms), T, 0, s>>>(L->col_ptr, L->in_f, L->chunk,
+                                                                  L->n_chunks, L->desc_c);
     }
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SNK_ERR_CUDA;
