@@ -12,7 +12,7 @@ constexpr int kWarp = 32;
 // Tuning parameters (compile-time; the defaults are the measured best on
 // GB300 for 10000x10000 layers at batch 1..64).
 #ifndef SNK_THREADS
-#define SNK_THREADS 1024   // SpMM / SDDMM block size; one block per SM
+#define SNK_THREADS 768    // SpMM / SDDMM block size; one block per SM
 #endif
 #ifndef SNK_PIPE_FWD
 #define SNK_PIPE_FWD 2     // stream blocks in flight ahead of the consumed one (forward)

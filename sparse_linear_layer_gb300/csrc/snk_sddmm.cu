@@ -220,6 +220,8 @@ template <int BP>
 static int launch_bp(Layer* L, SddmmArgs a, cudaStream_t s) {
     const size_t smem = (size_t)a.in_f * BP * sizeof(float);
     const int grid = (int)std::min<int64_t>(L->num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
+    // every chunk needs its own warp (the kernels take one chunk per warp)
+    if ((int64_t)grid * kWarpsPerBlock < a.n_chunks) return SNK_ERR_ARG;
     if (smem <= (size_t)L->max_smem && a.col16) {
         auto fn = k_sddmm<BP, true>;
         if (smem > 48 * 1024 &&
