@@ -58,7 +58,8 @@ extern "C" {
 #define SNK_ERR_CUDA 4    /* a CUDA call or kernel launch failed               */
 #define SNK_ERR_OOM 5     /* workspace allocation failed                       */
 #define SNK_ERR_NOSPACE 6 /* fewer free positions than entries to regrow       */
-#define SNK_ERR_LIMIT 7   /* the regrow draw limit (64 k + 1024) was reached   */
+#define SNK_ERR_LIMIT 7   /* a limit was reached: regrow draws (64 k + 1024),  */
+                          /* or the fixed scratch of the allocation-free call */
 
 typedef struct snk_layer* snk_handle;
 
@@ -179,6 +180,43 @@ int snk_get_shape(snk_handle handle, int64_t* out_features, int64_t* in_features
  */
 int snk_copy_topology(snk_handle handle, int32_t* row_ptr, int32_t* col_ptr, int32_t* rows_c,
                       int32_t* perm, void* stream);
+
+/*
+ * snk_forward_csr_noalloc - the forward product Y = X W^T + bias for callers
+ * that cannot let the library allocate device memory.  The pages have no
+ * counterpart to this entry point.
+ *
+ * Who needs it: a program whose device memory is owned entirely by its own
+ * arena, or whose hot path must never reach cudaMalloc/cudaFree (they
+ * synchronise the device and can stall other streams, and an allocation
+ * failure there cannot be handled).  Such a caller cannot use snk_create,
+ * which allocates the layer's workspace; this call takes the matrix as a
+ * ready CSR and allocates nothing.
+ *
+ * Arguments (device pointers on the current device):
+ *   row_ptr [out+1]  CSR row pointer (row_ptr[0] = 0, non-decreasing,
+ *                    row_ptr[out] = nnz), 4-byte aligned;
+ *   cols [nnz], values [nnz]  column index and value of each entry, rows
+ *                    stored one after another, 16-byte aligned;
+ *   X [batch, in], bias [out] or NULL, Y [batch, out]  as for snk_forward.
+ * The CSR is not validated: indices must lie in range (snk_create is the
+ * validating path).
+ * Scratch: a fixed array inside the library image (4 MiB + 32 KiB per GPU,
+ * held for the life of the process).  Limits: out <= 524,288 and
+ * in * (batch rounded up to a power of two, at most 64) * 4 bytes no larger
+ * than a block's shared memory; larger requests return SNK_ERR_LIMIT before
+ * any work is queued.  Every call shares the scratch and starts by clearing
+ * the part it needs; calls whose kernels overlap on the GPU (other streams or
+ * threads) race on it and must be serialised by the caller.
+ * The first call on a device looks the scratch address up (once per device,
+ * with that device current); make that first call before any stream
+ * capture.
+ * Errors: SNK_ERR_ARG, SNK_ERR_LIMIT, SNK_ERR_CUDA.  Asynchronous on stream.
+ */
+int snk_forward_csr_noalloc(int64_t out_features, int64_t in_features, int64_t nnz,
+                            const int32_t* row_ptr, const int32_t* cols, const float* values,
+                            const float* X, int64_t batch, const float* bias, float* Y,
+                            void* stream);
 
 #ifdef __cplusplus
 }

@@ -53,8 +53,10 @@ def lib():
         L.snk_get_shape.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                     ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.snk_copy_topology.argtypes = [P, P, P, P, P, P]
+        L.snk_forward_csr_noalloc.argtypes = [i64, i64, i64, P, P, P, P, i64, P, P, P]
         for name in ("snk_create", "snk_forward", "snk_backward_input", "snk_backward_weight",
-                     "snk_prune_regrow", "snk_destroy", "snk_get_shape", "snk_copy_topology"):
+                     "snk_prune_regrow", "snk_destroy", "snk_get_shape", "snk_copy_topology",
+                     "snk_forward_csr_noalloc"):
             getattr(L, name).restype = I
         _lib = L
         return L
@@ -142,6 +144,17 @@ def snk_copy_topology(handle: int, row_ptr=None, col_ptr=None, rows_c=None, perm
                       stream=None):
     _check(lib().snk_copy_topology(handle, _ptr(row_ptr), _ptr(col_ptr), _ptr(rows_c),
                                    _ptr(perm), _stream(stream)), "snk_copy_topology")
+
+
+def snk_forward_csr_noalloc(out_features: int, in_features: int, row_ptr, cols, values, X, bias,
+                            Y, stream=None, batch: int | None = None):
+    """Forward product on a caller's CSR without any device allocation (the
+    library's fixed scratch array is used instead)."""
+    b = X.shape[0] if batch is None else batch
+    nnz = values.numel() if hasattr(values, "numel") else 0
+    _check(lib().snk_forward_csr_noalloc(out_features, in_features, nnz, _ptr(row_ptr), _ptr(cols),
+                                         _ptr(values), _ptr(X), b, _ptr(bias), _ptr(Y),
+                                         _stream(stream)), "snk_forward_csr_noalloc")
 
 
 class SparseLinear:

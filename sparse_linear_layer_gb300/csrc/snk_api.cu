@@ -59,7 +59,7 @@ const char* snk_status_string(int status) {
         case SNK_ERR_CUDA: return "CUDA error";
         case SNK_ERR_OOM: return "out of device memory for the workspace";
         case SNK_ERR_NOSPACE: return "fewer free positions than entries to regrow";
-        case SNK_ERR_LIMIT: return "regrow draw limit reached";
+        case SNK_ERR_LIMIT: return "limit reached (regrow draws, or the fixed scratch size)";
         default: return "unknown status";
     }
 }

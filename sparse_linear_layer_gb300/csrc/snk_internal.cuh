@@ -112,6 +112,12 @@ int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaS
 int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b, float* dW,
                            float* db, cudaStream_t s);
 int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s);
+int launch_chunk_desc(const int32_t* ptr, int64_t n_seg, int32_t chunk, int32_t n_chunks,
+                      int2* desc, int num_sms, cudaStream_t s);
+int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row_ptr,
+                       const int2* desc, int64_t nnz, int64_t out_f, int64_t in_f, int chunk,
+                       int n_chunks, const float* X, int64_t b, const float* bias, float* Y,
+                       float* part, int32_t* cnt, int num_sms, int max_smem, cudaStream_t s);
 void free_restructure(Layer* L);
 
 }  // namespace snk

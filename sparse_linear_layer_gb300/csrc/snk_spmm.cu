@@ -152,9 +152,8 @@ __device__ __forceinline__ void publish_partials(const SpmmArgs& a, const Pendin
 // over slots is unrolled so every slot index is a compile-time constant.  A
 // block inside one segment is consumed without masks; a block that straddles
 // segment boundaries is consumed once per segment it touches.
-template <int BP, bool GATHER, bool SMEM>
+template <int BP, bool GATHER, bool SMEM, bool I16 = SMEM && SNK_IDX16>
 __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
-    constexpr bool I16 = SMEM && SNK_IDX16;
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
@@ -346,6 +345,66 @@ static int run_spmm(Layer* L, SpmmArgs a, int64_t b, cudaStream_t s) {
             continue;
         }
         int st = launch_tile<GATHER>(L, a, batch_tile(bt), s);
+        if (st != SNK_OK) return st;
+    }
+    return SNK_OK;
+}
+
+// Forward SpMM on a caller's CSR (32-bit column indices) with scratch supplied
+// by the caller: chunk descriptors, split-segment partials and zeroed arrival
+// counters.  Shared-memory operand path only.
+template <int BP>
+static int launch_csr_bp(SpmmArgs a, int num_sms, int max_smem, cudaStream_t s) {
+    const size_t smem = (size_t)a.n_src * BP * sizeof(float);
+    if (smem > (size_t)max_smem) return SNK_ERR_LIMIT;
+    const int grid = (int)std::min<int64_t>(num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
+    if ((int64_t)grid * kWarpsPerBlock < a.n_chunks) return SNK_ERR_ARG;
+    auto fn = k_spmm<BP, false, true, false>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+        return SNK_ERR_CUDA;
+    fn<<<grid, kThreads, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+}
+
+int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row_ptr,
+                       const int2* desc, int64_t nnz, int64_t out_f, int64_t in_f, int chunk,
+                       int n_chunks, const float* X, int64_t b, const float* bias, float* Y,
+                       float* part, int32_t* cnt, int num_sms, int max_smem, cudaStream_t s) {
+    SpmmArgs a{};
+    a.val = val;
+    a.idx = cols;
+    a.seg_ptr = row_ptr;
+    a.desc = desc;
+    a.nnz = nnz;
+    a.n_seg = out_f;
+    a.n_src = in_f;
+    a.chunk = chunk;
+    a.n_chunks = n_chunks;
+    a.bias = bias;
+    a.part = part;
+    a.cnt = cnt;
+    for (int64_t t0 = 0; t0 < b; t0 += kMaxBatchTile) {
+        const int64_t bt = std::min<int64_t>(kMaxBatchTile, b - t0);
+        a.b = (int)bt;
+        a.X = X + t0 * in_f;
+        a.Y = Y + t0 * out_f;
+        int st;
+        if (nnz == 0) {
+            k_fill_bias<<<num_sms * 4, 256, 0, s>>>(a.Y, bt, out_f, bias);
+            st = cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+        } else {
+            switch (batch_tile(bt)) {
+                case 1: st = launch_csr_bp<1>(a, num_sms, max_smem, s); break;
+                case 2: st = launch_csr_bp<2>(a, num_sms, max_smem, s); break;
+                case 4: st = launch_csr_bp<4>(a, num_sms, max_smem, s); break;
+                case 8: st = launch_csr_bp<8>(a, num_sms, max_smem, s); break;
+                case 16: st = launch_csr_bp<16>(a, num_sms, max_smem, s); break;
+                case 32: st = launch_csr_bp<32>(a, num_sms, max_smem, s); break;
+                default: st = launch_csr_bp<64>(a, num_sms, max_smem, s); break;
+            }
+        }
         if (st != SNK_OK) return st;
     }
     return SNK_OK;

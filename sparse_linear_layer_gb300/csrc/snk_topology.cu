@@ -368,6 +368,16 @@ __global__ void k_desc(const int32_t* __restrict__ ptr, int64_t n_seg, int32_t c
     }
 }
 
+int launch_chunk_desc(const int32_t* ptr, int64_t n_seg, int32_t chunk, int32_t n_chunks,
+                      int2* desc, int num_sms, cudaStream_t s) {
+    if (n_chunks <= 0) return SNK_OK;
+    const int T = 256;
+    const unsigned g = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>(ceil_div(n_chunks, T), (int64_t)num_sms * 8));
+    k_desc<<<g, T, 0, s>>>(ptr, n_seg, chunk, n_chunks, desc);
+    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+}
+
 static unsigned grid_for(int64_t n, int threads, int num_sms) {
     int64_t g = std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, threads), (int64_t)num_sms * 8));
     return (unsigned)g;
