@@ -15,10 +15,12 @@ device time, over all ranks (GB/s).  L2 is flushed (a 512 MB write) before
 every kernel, outside the timed interval; each kernel is bracketed by CUDA
 events on the stream it is launched on.
 
-Algorithmic bytes per launch (what each kernel must move at least):
-  forward  nnz*8 (values, cols) + (out+1)*4 (row_ptr) + b*in*4 (X) + b*out*4 (Y) + out*4 (bias)
-  dX       nnz*12 (rows_c, perm, values) + (in+1)*4 (col_ptr) + b*out*4 (dY) + b*in*4 (dX)
-  dW       nnz*8 (cols read, dW written) + (out+1)*4 + b*(in+out)*4 (X, dY) + out*4 (db)
+Algorithmic bytes per launch (what each kernel must move at least; i is the
+width of the index copy it reads: 2 bytes on the shared-memory operand path,
+else 4):
+  forward  nnz*(4+i) (values, cols) + (out+1)*4 (row_ptr) + b*in*4 (X) + b*out*4 (Y) + out*4 (bias)
+  dX       nnz*(i+4+4) (rows in column order, perm, values) + (in+1)*4 + b*out*4 + b*in*4
+  dW       nnz*(i+4) (cols read, dW written) + (out+1)*4 + b*(in+out)*4 (X, dY) + out*4 (db)
 The contract formula bytes (nnz*12 + b*(in+out)*4, plus nnz*4 for dW) are
 reported beside them as ``formula``.
 
@@ -92,11 +94,25 @@ def aggregate_gbs(world, bytes_per_step, steps, max_ms):
     return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
 
 
-def op_bytes(out_f, in_f, nnz, b):
+def index_bytes(n_src, b, max_smem=232448):
+    """Bytes per index the kernels stream: 16-bit copies on the shared-memory
+    operand path (which implies n_src <= 65536), 32-bit otherwise."""
+    bt = min(b, 64)
+    bp = 1
+    while bp < bt:
+        bp <<= 1
+    return 2 if (n_src * bp * 4 <= max_smem and n_src <= 65536) else 4
+
+
+def op_bytes(out_f, in_f, nnz, b, max_smem=232448):
+    """Algorithmic bytes per launch (what each kernel must move at least, with
+    the index width it actually reads) and the contract formula bytes."""
+    ic = index_bytes(in_f, b, max_smem)    # column indices (forward, dW)
+    ir = index_bytes(out_f, b, max_smem)   # row indices in column order (dX)
     alg = {
-        "fwd": nnz * 8 + (out_f + 1) * 4 + b * in_f * 4 + b * out_f * 4 + out_f * 4,
-        "dx": nnz * 12 + (in_f + 1) * 4 + b * out_f * 4 + b * in_f * 4,
-        "dw": nnz * 8 + (out_f + 1) * 4 + b * (in_f + out_f) * 4 + out_f * 4,
+        "fwd": nnz * (4 + ic) + (out_f + 1) * 4 + b * in_f * 4 + b * out_f * 4 + out_f * 4,
+        "dx": nnz * (ir + 4 + 4) + (in_f + 1) * 4 + b * out_f * 4 + b * in_f * 4,
+        "dw": nnz * (ic + 4) + (out_f + 1) * 4 + b * (in_f + out_f) * 4 + out_f * 4,
     }
     formula = {
         "fwd": nnz * 12 + b * (in_f + out_f) * 4,
@@ -370,7 +386,8 @@ def run_sweep(args, dev):
                 db = torch.empty(args.out, device=dev)
                 ms = time_ops(binding, g, X, dY, bias, Y, dX, dW, db, flush, stream,
                               args.steps, args.warmup)
-                alg, formula = op_bytes(args.out, args.inp, lay.nnz, b)
+                alg, formula = op_bytes(args.out, args.inp, lay.nnz, b,
+                                        torch.cuda.get_device_properties(dev).shared_memory_per_block_optin)
                 row = {"out": args.out, "in": args.inp, "sparsity_pct": sp, "nnz": lay.nnz,
                        "batch": b, "peak_gbs": peak, "peak_kind": peak_kind,
                        "ops": summarize(ms, alg, formula, peak)}
@@ -420,7 +437,8 @@ def run_ours(args, workload, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     total_ms = reduce_max_ms(sum(sum(v) for v in per_op_ms.values()), dev)
-    alg, formula = op_bytes(out_f, in_f, nnz, b)
+    max_smem = torch.cuda.get_device_properties(dev).shared_memory_per_block_optin
+    alg, formula = op_bytes(out_f, in_f, nnz, b, max_smem)
     step_bytes = sum(alg[n] for n in per_op_ms)
     value = aggregate_gbs(world, step_bytes, args.steps, total_ms)
     peak, peak_kind = measured_peaks()
@@ -484,7 +502,6 @@ def run_ours(args, workload, rank, world, local):
                        "us_median_host_timed": statistics.median(ts),
                        "note": "synchronous call (it reads device counts back); wall-clock µs"}
 
-    max_smem = torch.cuda.get_device_properties(dev).shared_memory_per_block_optin
     per_op_launch = {"fwd": launches_per_op(in_f, b, max_smem),
                      "dx": launches_per_op(out_f, b, max_smem),
                      "dw": launches_per_op(in_f, b, max_smem)}
