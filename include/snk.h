@@ -201,11 +201,11 @@ int snk_copy_topology(snk_handle handle, int32_t* row_ptr, int32_t* col_ptr, int
  *   X [batch, in], bias [out] or NULL, Y [batch, out]  as for snk_forward.
  * The CSR is not validated: indices must lie in range (snk_create is the
  * validating path).
- * Scratch: a fixed array inside the library image (4 MiB + 32 KiB per GPU,
- * held for the life of the process).  Limits: out <= 524,288 and
- * in * (batch rounded up to a power of two, at most 64) * 4 bytes no larger
- * than a block's shared memory; larger requests return SNK_ERR_LIMIT before
- * any work is queued.  Every call shares the scratch and starts by clearing
+ * Scratch: a fixed array inside the library image (2,574,352 bytes per GPU,
+ * held for the life of the process).  Limits: out <= 524,288, at most 512
+ * SMs, and the operand, in * (batch rounded up to a power of two, at most
+ * 64) * 4 bytes, must fit one block's shared memory; larger requests return
+ * SNK_ERR_LIMIT before any work is queued.  Every call shares the scratch and starts by clearing
  * the part it needs; calls whose kernels overlap on the GPU (other streams or
  * threads) race on it and must be serialised by the caller.
  * The first call on a device looks the scratch address up (once per device,

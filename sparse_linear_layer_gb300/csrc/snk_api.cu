@@ -24,7 +24,8 @@ static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)
 static void free_layer(Layer* L) {
     if (!L) return;
     free_restructure(L);
-    void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->c16, L->rc16, L->desc_r, L->desc_c,
+    void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->c16, L->rc16, L->bnd_r, L->bnd_c, L->cdesc_r, L->cdesc_c,
+                    L->bdesc_r, L->bdesc_c,
                     L->part, L->cnt, L->xt, L->status, L->sort_keys, L->sort_vals,
                     L->col_keys, L->col_vals, L->tile_hist};
     for (void* p : ptrs)
@@ -90,12 +91,9 @@ int snk_create(snk_handle* handle, int64_t out_f, int64_t in_f, int64_t nnz, flo
         delete L;
         return SNK_ERR_CUDA;
     }
-    // merge-path chunks: kChunksPerSm per SM, a multiple of 4 entries each
-    const int64_t want = (int64_t)L->num_sms * kChunksPerSm;
-    int64_t chunk = std::max<int64_t>(32, ceil_div(std::max<int64_t>(nnz, 1), want));
-    chunk = ceil_div(chunk, 4) * 4;
-    L->chunk = (int32_t)chunk;
-    L->n_chunks = (int32_t)ceil_div(nnz, chunk);
+    // one block per SM, one chunk per warp
+    L->n_blocks = L->num_sms;
+    L->n_chunks = L->n_blocks * kWarpsPerBlock;
     const int64_t n_max = std::max(out_f, in_f);
     const bool wide = (uint64_t)out_f * (uint64_t)in_f > (1ull << 32);
     L->tile_hist_len = topology_hist_len(nnz);
@@ -105,9 +103,13 @@ int snk_create(snk_handle* handle, int64_t out_f, int64_t in_f, int64_t nnz, flo
               dmalloc(&L->rows_c, L->nnz_pad) && dmalloc(&L->perm, L->nnz_pad) &&
               (in_f > 65536 || dmalloc(&L->c16, L->nnz_pad)) &&
               (out_f > 65536 || dmalloc(&L->rc16, L->nnz_pad)) &&
-              dmalloc(&L->desc_r, (int64_t)L->n_chunks) &&
-              dmalloc(&L->desc_c, (int64_t)L->n_chunks) &&
-              dmalloc(&L->part, (int64_t)std::max(L->n_chunks, 1) * 2 * kMaxBatchTile) &&
+              dmalloc(&L->bnd_r, (int64_t)L->n_blocks + 1) &&
+              dmalloc(&L->bnd_c, (int64_t)L->n_blocks + 1) &&
+              dmalloc(&L->cdesc_r, (int64_t)L->n_chunks) &&
+              dmalloc(&L->cdesc_c, (int64_t)L->n_chunks) &&
+              dmalloc(&L->bdesc_r, (int64_t)L->n_blocks) &&
+              dmalloc(&L->bdesc_c, (int64_t)L->n_blocks) &&
+              dmalloc(&L->part, (int64_t)L->n_blocks * 2 * kMaxBatchTile) &&
               dmalloc(&L->cnt, n_max) && dmalloc(&L->xt, n_max * kMaxBatchTile) &&
               dmalloc(&L->status, 1) &&
               dmalloc((char**)&L->sort_keys, 2 * nnz * (wide ? 8 : 4)) &&

@@ -40,6 +40,17 @@ constexpr int kStatLimit = 4;
 
 struct RestructureWs;
 
+// Per block: its entry range [k0, k1), and for the segment that enters the
+// block from before (head) and the one that leaves it (tail) the first and
+// last block holding entries of that segment, with the number of non-empty
+// blocks from there to this block (head) and from this block to there (tail).
+struct BlockDesc {
+    int k0, k1;
+    int head_first, tail_last;
+    int n_head, n_tail;
+    int pad0, pad1;
+};
+
 // Library-owned state behind an snk_handle.
 struct Layer {
     int64_t out_f = 0, in_f = 0, nnz = 0;
@@ -63,14 +74,20 @@ struct Layer {
     uint16_t* rc16 = nullptr;     // [nnz_pad] rows in column order, if out <= 65536
     int64_t nnz_pad = 0;          // round_up(nnz, 4) + kStreamPad
 
-    // merge-path chunking of the canonical (row) and column orders
-    int32_t chunk = 0;            // nnz per chunk
-    int32_t n_chunks = 0;         // ceil(nnz / chunk)
-    int2* desc_r = nullptr;       // [n_chunks] (first row touched by chunk q, end of its rows)
-    int2* desc_c = nullptr;       // [n_chunks] the same for columns
+    // work partition of the canonical (row) and column orders: one block per
+    // SM owns a range of entries aligned to segment boundaries, split into one
+    // chunk per warp
+    int32_t n_blocks = 0;         // blocks (= SMs)
+    int32_t n_chunks = 0;         // n_blocks * kWarpsPerBlock
+    int32_t* bnd_r = nullptr;     // [n_blocks+1] first entry of each block (rows)
+    int32_t* bnd_c = nullptr;     // [n_blocks+1] the same (columns)
+    int4* cdesc_r = nullptr;      // [n_chunks] (k0, k1, first segment touched, one past last)
+    int4* cdesc_c = nullptr;      // [n_chunks]
+    BlockDesc* bdesc_r = nullptr; // [n_blocks] segments cut by block boundaries
+    BlockDesc* bdesc_c = nullptr; // [n_blocks]
 
     // scratch of the SpMM kernels
-    float* part = nullptr;        // [n_chunks * 2 * kMaxBatchTile] split-segment partials
+    float* part = nullptr;        // [n_blocks * 2 * kMaxBatchTile] cross-block partial sums
     int32_t* cnt = nullptr;       // [max(out,in)] arrival counters, all zero between calls
     float* xt = nullptr;          // [max(out,in) * kMaxBatchTile] transposed operand
 
@@ -112,12 +129,16 @@ int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaS
 int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b, float* dW,
                            float* db, cudaStream_t s);
 int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s);
-int launch_chunk_desc(const int32_t* ptr, int64_t n_seg, int32_t chunk, int32_t n_chunks,
-                      int2* desc, int num_sms, cudaStream_t s);
+// Partition nnz entries with segment pointer ptr[n_seg+1] over n_blocks
+// blocks of kWarpsPerBlock chunks (block boundaries on segment boundaries
+// except inside segments longer than half a block's share).
+int build_partition(const int32_t* ptr, int64_t n_seg, int64_t nnz, int n_blocks, int32_t* bnd,
+                    int4* cdesc, BlockDesc* bdesc, cudaStream_t s);
 int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row_ptr,
-                       const int2* desc, int64_t nnz, int64_t out_f, int64_t in_f, int chunk,
-                       int n_chunks, const float* X, int64_t b, const float* bias, float* Y,
-                       float* part, int32_t* cnt, int num_sms, int max_smem, cudaStream_t s);
+                       const int4* cdesc, const BlockDesc* bdesc, const int32_t* bnd, int64_t nnz,
+                       int64_t out_f, int64_t in_f, int n_blocks, const float* X, int64_t b,
+                       const float* bias, float* Y, float* part, int32_t* cnt, int max_smem,
+                       cudaStream_t s);
 void free_restructure(Layer* L);
 
 }  // namespace snk

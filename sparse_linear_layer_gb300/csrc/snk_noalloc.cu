@@ -10,10 +10,11 @@
 // in a fixed, statically sized device array that is part of the library
 // image.
 //
-// The scratch array: chunk descriptors, split-row partial sums and per-row
-// arrival counters of the merge-path kernel.  It is sized for at most
-// kNaMaxChunks chunks and kNaMaxOut output rows; larger requests are refused
-// with SNK_ERR_LIMIT.  Every GPU that loads the library keeps this array for
+// The scratch array: the work partition (block boundaries, chunk and block
+// descriptors), cross-block partial sums and per-row arrival counters of the
+// merge-path kernel.  It is sized for at most kNaMaxBlocks blocks (one per
+// SM) and kNaMaxOut output rows; larger requests are refused with
+// SNK_ERR_LIMIT.  Every GPU that loads the library keeps this array for
 // the life of the process.  All calls share it and it keeps the previous
 // call's contents, so each call first clears the counters it uses, and two
 // calls whose kernels overlap on the GPU (two streams, or two threads) race
@@ -25,12 +26,15 @@
 namespace snk {
 namespace {
 
-constexpr int kNaMaxChunks = 4096;
+constexpr int kNaMaxBlocks = 512;                // blocks of the partition (one per SM)
 constexpr int64_t kNaMaxOut = int64_t(1) << 19;  // 524,288 output rows
-constexpr size_t kNaDescBytes = (size_t)kNaMaxChunks * sizeof(int2);                    // 32 KiB
-constexpr size_t kNaPartBytes = (size_t)kNaMaxChunks * 2 * kMaxBatchTile * sizeof(float);  // 2 MiB
-constexpr size_t kNaCntBytes = (size_t)kNaMaxOut * sizeof(int32_t);                    // 2 MiB
-constexpr size_t kNaScratchBytes = kNaDescBytes + kNaPartBytes + kNaCntBytes;
+constexpr size_t kNaBndBytes = (size_t)(kNaMaxBlocks + 1) * sizeof(int32_t) + 12;  // 16-B padded
+constexpr size_t kNaCdescBytes = (size_t)kNaMaxBlocks * kWarpsPerBlock * sizeof(int4);
+constexpr size_t kNaBdescBytes = (size_t)kNaMaxBlocks * sizeof(BlockDesc);
+constexpr size_t kNaPartBytes = (size_t)kNaMaxBlocks * 2 * kMaxBatchTile * sizeof(float);
+constexpr size_t kNaCntBytes = (size_t)kNaMaxOut * sizeof(int32_t);
+constexpr size_t kNaScratchBytes =
+    kNaBndBytes + kNaCdescBytes + kNaBdescBytes + kNaPartBytes + kNaCntBytes;
 constexpr int kNaMaxDevices = 64;
 
 }  // namespace
@@ -96,28 +100,26 @@ extern "C" int snk_forward_csr_noalloc(int64_t out_features, int64_t in_features
     if ((int64_t)in_features * batch_tile(tile) * (int64_t)sizeof(float) > max_smem)
         return SNK_ERR_LIMIT;
 
-    // one chunk per warp of one block per SM, capped by the scratch size
-    const int64_t want = std::min<int64_t>((int64_t)num_sms * kChunksPerSm, kNaMaxChunks);
-    int64_t chunk = std::max<int64_t>(32, ceil_div(std::max<int64_t>(nnz, 1), want));
-    chunk = ceil_div(chunk, 4) * 4;
-    const int64_t n_chunks = ceil_div(nnz, chunk);
-    if (n_chunks > kNaMaxChunks) return SNK_ERR_LIMIT;
+    // one block per SM, one chunk per warp
+    const int n_blocks = num_sms;
+    if (n_blocks > kNaMaxBlocks) return SNK_ERR_LIMIT;
 
     unsigned char* base = nullptr;
     int st = scratch_address(dev, &base);
     if (st != SNK_OK) return st;
-    int2* desc = reinterpret_cast<int2*>(base);
-    float* part = reinterpret_cast<float*>(base + kNaDescBytes);
-    int32_t* cnt = reinterpret_cast<int32_t*>(base + kNaDescBytes + kNaPartBytes);
+    int32_t* bnd = reinterpret_cast<int32_t*>(base);
+    int4* cdesc = reinterpret_cast<int4*>(base + kNaBndBytes);
+    BlockDesc* bdesc = reinterpret_cast<BlockDesc*>(base + kNaBndBytes + kNaCdescBytes);
+    float* part = reinterpret_cast<float*>(base + kNaBndBytes + kNaCdescBytes + kNaBdescBytes);
+    int32_t* cnt =
+        reinterpret_cast<int32_t*>(base + kNaBndBytes + kNaCdescBytes + kNaBdescBytes + kNaPartBytes);
 
     // the arrival counters must start at zero; the previous call's state is
     // not trusted
     if (cudaMemsetAsync(cnt, 0, (size_t)out_features * sizeof(int32_t), s) != cudaSuccess)
         return SNK_ERR_CUDA;
-    st = launch_chunk_desc(row_ptr, out_features, (int32_t)chunk, (int32_t)n_chunks, desc, num_sms,
-                           s);
+    st = build_partition(row_ptr, out_features, nnz, n_blocks, bnd, cdesc, bdesc, s);
     if (st != SNK_OK) return st;
-    return launch_forward_csr(values, cols, row_ptr, desc, nnz, out_features, in_features,
-                              (int)chunk, (int)n_chunks, X, batch, bias, Y, part, cnt, num_sms,
-                              max_smem, s);
+    return launch_forward_csr(values, cols, row_ptr, cdesc, bdesc, bnd, nnz, out_features,
+                              in_features, n_blocks, X, batch, bias, Y, part, cnt, max_smem, s);
 }

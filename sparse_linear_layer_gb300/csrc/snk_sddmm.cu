@@ -25,10 +25,10 @@ struct SddmmArgs {
     const int32_t* col;     // canonical column indices
     const uint16_t* col16;  // the same as 16-bit, zero padded (shared-memory path)
     const int32_t* row_ptr; // [out+1]
-    const int2* desc;       // [n_chunks] (first row touched, one past the last)
+    const int4* cdesc;      // [n_blocks * kWarpsPerBlock] (k0, k1, first row, end row)
     int64_t nnz, out_f, in_f;
     int b;                  // batch columns of this tile
-    int chunk, n_chunks;
+    int n_blocks;
     const float* X;         // [b, in] (tile)
     const float* xt;        // [in][BP] (global path)
     const float* dY;        // [b, out] (tile)
@@ -70,26 +70,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     const int grp = lane / LPE;
     const int sub = lane % LPE;
     const uint32_t nnz = (uint32_t)a.nnz;
-    const uint32_t chunk = (uint32_t)a.chunk;
-    const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const bool active = q < a.n_chunks;
-    uint32_t k0 = 0, k1 = 0;
+    const int4 cd = a.cdesc[blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)];
+    const uint32_t k0 = (uint32_t)cd.x, k1 = (uint32_t)cd.y;
+    const uint32_t base_first = k0 & ~3u;
     IdxBlk<I16> ib[NS];
     auto issue = [&](int s, uint32_t blk0) {
         const uint32_t base = blk0 + 4 * grp;
         if constexpr (I16) ib[s].load(a.col16, base);
         else ib[s].load(a.col, base, nnz);
     };
-    SegWindow win{0, 0, 0, 0u, 0.f};
-    if (active) {
-        k0 = (uint32_t)q * chunk;
-        k1 = min(k0 + chunk, nnz);
+    SegWindow win{cd.z, cd.w - cd.z, 0, 0u, 0.f};
+    if (k0 < k1) {
 #pragma unroll
         for (int s = 0; s < NS; ++s)
-            if (k0 + s * BLK < k1) issue(s, k0 + s * BLK);
-        const int2 dsc = a.desc[q];
-        win.r_begin = dsc.x;
-        win.nrows = dsc.y - dsc.x;
+            if (base_first + s * BLK < k1) issue(s, base_first + s * BLK);
         win.load(0, lane, a.row_ptr, nullptr);
     }
     if (a.db) {
@@ -105,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
         stage_transposed<BP>(xs, a.X, a.in_f, a.b, a.in_f, threadIdx.x, kThreads);
         __syncthreads();
     }
-    if (!active) return;
+    if (k0 >= k1) return;  // no entries in this chunk (rows without entries need no output)
     const float* xsrc = SMEM ? xs : a.xt;
 
     const int r_begin = win.r_begin;
@@ -121,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
         const uint32_t base = blk0 + 4 * grp;
         const uint32_t blk_end = min(blk0 + BLK, k1);
         float res[4] = {0.f, 0.f, 0.f, 0.f};
-        const bool interior = rs <= blk0 && blk0 + BLK < re && blk0 + BLK <= k1;
+        const bool interior = rs <= blk0 && k0 <= blk0 && blk0 + BLK < re && blk0 + BLK <= k1;
         while (true) {
             if (interior) {
                 // every entry of the block belongs to the current row, which
@@ -141,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
                 }
                 break;
             }
-            const uint32_t lo_k = max(rs, blk0), hi_k = min(re, blk_end);
+            const uint32_t lo_k = max(max(rs, k0), blk0), hi_k = min(re, blk_end);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t k = base + j;
@@ -188,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
         }
     };
 
-    for (uint32_t base0 = k0; base0 < k1; base0 += NS * BLK) {
+    for (uint32_t base0 = base_first; base0 < k1; base0 += NS * BLK) {
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
             const uint32_t blk0 = base0 + s * BLK;
@@ -219,9 +213,7 @@ __global__ void k_bias_grad_only(const float* __restrict__ dY, int64_t b, int64_
 template <int BP>
 static int launch_bp(Layer* L, SddmmArgs a, cudaStream_t s) {
     const size_t smem = (size_t)a.in_f * BP * sizeof(float);
-    const int grid = (int)std::min<int64_t>(L->num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
-    // every chunk needs its own warp (the kernels take one chunk per warp)
-    if ((int64_t)grid * kWarpsPerBlock < a.n_chunks) return SNK_ERR_ARG;
+    const int grid = a.n_blocks;
     if (smem <= (size_t)L->max_smem && a.col16) {
         auto fn = k_sddmm<BP, true>;
         if (smem > 48 * 1024 &&
@@ -250,12 +242,11 @@ int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b,
     a.col = L->c;
     a.col16 = L->c16;
     a.row_ptr = L->row_ptr;
-    a.desc = L->desc_r;
+    a.cdesc = L->cdesc_r;
     a.nnz = L->nnz;
     a.out_f = L->out_f;
     a.in_f = L->in_f;
-    a.chunk = L->chunk;
-    a.n_chunks = L->n_chunks;
+    a.n_blocks = L->n_blocks;
     a.dW = dW;
     a.b_all = b;
     a.dY_all = dY;

@@ -16,11 +16,15 @@
 //     Y[beta, o] = bias[o] + sum_{k in seg(o)} w_k * X[beta, idx_k].
 //
 // GB300 design
-//  * Load balance: the nnz stream is cut into equal chunks (merge path), 64
-//    per SM, two per warp, so skewed row lengths cost nothing.  A segment cut
-//    by a chunk boundary is finished by whichever of its chunks arrives last
-//    (an arrival counter per segment); the partials are summed in chunk order,
-//    so the result does not depend on timing.  Counters return to zero.
+//  * Load balance: one block per SM owns an equal share of the entries,
+//    with its boundaries moved to the nearest segment boundary (unless that
+//    segment is longer than half a share), and its warps split the share
+//    into equal chunks (merge path), so skewed segments cost nothing.
+//    Segments cut between warps are added in shared memory after one block
+//    barrier, in warp order.  Only a segment cut between blocks (a very long
+//    one) goes through global memory: each block stores its partial, the
+//    last block to arrive (an arrival counter per segment) adds them in
+//    block order and resets the counter.  No result depends on timing.
 //  * The dense operand is staged once per block in shared memory transposed,
 //    [idx][BP], so one 128-bit shared load serves 4 batch columns of one
 //    entry; when it does not fit, a transposed copy in global memory is read
@@ -35,43 +39,53 @@
 namespace snk {
 
 struct SpmmArgs {
-    const float* val;       // stored values, canonical order
-    const int32_t* perm;    // column-order -> canonical slot (transposed product) or null
-    const int32_t* idx;     // operand index per stored entry (col, or row in column order)
-    const uint16_t* idx16;  // the same as 16-bit, zero padded (shared-memory path)
-    const int32_t* seg_ptr; // [n_seg+1]
-    const int2* desc;       // [n_chunks] (first segment touched, one past the last)
+    const float* val;        // stored values, canonical order
+    const int32_t* perm;     // column-order -> canonical slot (transposed product) or null
+    const int32_t* idx;      // operand index per stored entry (col, or row in column order)
+    const uint16_t* idx16;   // the same as 16-bit, zero padded (shared-memory path)
+    const int32_t* seg_ptr;  // [n_seg+1]
+    const int4* cdesc;       // [n_blocks * kWarpsPerBlock] (k0, k1, first seg, end seg)
+    const BlockDesc* bdesc;  // [n_blocks]
+    const int32_t* bnd;      // [n_blocks+1] first entry of each block
     int64_t nnz;
-    int64_t n_seg;          // output length per batch row
-    int64_t n_src;          // operand length per batch row
-    int b;                  // batch columns of this tile (<= BP)
-    int chunk;
-    int n_chunks;
-    const float* X;         // [b, n_src] row-major
-    const float* xt;        // [n_src][BP] transposed copy (global-memory path)
-    const float* bias;      // [n_seg] or null
-    float* Y;               // [b, n_seg] row-major
-    float* part;            // [n_chunks][2][BP]
-    int32_t* cnt;           // [n_seg]
+    int64_t n_seg;           // output length per batch row
+    int64_t n_src;           // operand length per batch row
+    int b;                   // batch columns of this tile (<= BP)
+    int n_blocks;
+    const float* X;          // [b, n_src] row-major
+    const float* xt;         // [n_src][BP] transposed copy (global-memory path)
+    const float* bias;       // [n_seg] or null
+    float* Y;                // [b, n_seg] row-major
+    float* part;             // [n_blocks][2][BP] cross-block partial sums
+    int32_t* cnt;            // [n_seg] arrival counters
 };
 
-// A segment cut by a chunk boundary, whose partial sum this chunk has
-// written to its slot (0: the segment entered from the previous chunk,
-// 1: the segment that leaves into the next one).
+// A segment cut by a chunk boundary, whose partial sum this warp stored in
+// its shared-memory slot (0: the segment entered the chunk from before,
+// 1: it starts in the chunk and leaves it).
 struct Pending {
     int r;
     uint32_t rs, re;
 };
 
+// Shared memory: [transposed operand (shared-memory path)][partials
+// [warps][2][BP]][segment ids [warps][2]].
+template <int BP>
+__host__ __device__ constexpr size_t spmm_slot_bytes() {
+    return (size_t)kWarpsPerBlock * 2 * BP * sizeof(float) + (size_t)kWarpsPerBlock * 2 * sizeof(int);
+}
+__host__ __device__ inline size_t operand_floats(int64_t n_src, int bp) {
+    return ((size_t)n_src * bp + 3) & ~(size_t)3;
+}
+
 // Finish one output segment: reduce the per-lane partial sums across the
 // warp's groups; write the result, or, for a segment cut by a chunk boundary,
-// store this chunk's partial in its slot and remember the segment so that the
-// arrival is announced once, after the chunk's last block.
+// store this warp's partial in its shared slot.
 template <int BP>
 __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[Tile<BP>::VEC],
                                                int r, uint32_t rs, uint32_t re, uint32_t k0,
-                                               uint32_t k1, int q, float bo, int lane, int sub,
-                                               Pending (&pend)[2]) {
+                                               uint32_t k1, float bo, int lane, int sub,
+                                               float* my_slots, Pending (&pend)[2]) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE;
 #pragma unroll
@@ -90,9 +104,8 @@ __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[T
     } else {
         const int slot = (rs < k0) ? 0 : 1;
         if (lane < LPE) {
-            float* my = a.part + ((int64_t)q * 2 + slot) * BP + sub * VEC;
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) my[j] = acc[j];
+            for (int j = 0; j < VEC; ++j) my_slots[slot * BP + sub * VEC + j] = acc[j];
         }
         pend[slot] = Pending{r, rs, re};
     }
@@ -100,58 +113,109 @@ __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[T
     for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
 }
 
-// After the chunk: one fence makes this chunk's partials visible, then each
-// cut segment counts its arrival; the chunk that arrives last adds all
-// partials of the segment in chunk order (so the sum does not depend on
-// timing), writes the output and resets the counter.
+// A segment cut between blocks: store this block's partial, count the
+// arrival, and let the last arriving block add the partials of the non-empty
+// blocks first..last in block order (the first block's is in its slot 1).
 template <int BP>
-__device__ __forceinline__ void publish_partials(const SpmmArgs& a, const Pending (&pend)[2],
-                                                 int lane, int sub) {
+__device__ __noinline__ void cross_block(const SpmmArgs& a, int r, int slot,
+                                         const float (&sum)[Tile<BP>::VEC], int first, int last,
+                                         int n_contrib, int lane, int sub) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE;
-    if (pend[0].r < 0 && pend[1].r < 0) return;
+    if (lane < LPE) {
+        float* my = a.part + ((int64_t)blockIdx.x * 2 + slot) * BP + sub * VEC;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) my[j] = sum[j];
+    }
     __threadfence();
     __syncwarp();
+    int old = 0;
+    if (lane == 0) old = atomicAdd(a.cnt + r, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != n_contrib - 1) return;
+    __threadfence();
+    if (lane < LPE) {
+        float tot[VEC];
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        if (pend[p].r < 0) continue;
-        const int r = pend[p].r;
-        const uint32_t chunk = (uint32_t)a.chunk;
-        const int64_t q_first = pend[p].rs / chunk;
-        const int64_t q_last = (pend[p].re - 1) / chunk;
-        int old = 0;
-        if (lane == 0) old = atomicAdd(a.cnt + r, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != (int)(q_last - q_first)) continue;
-        __threadfence();
-        if (lane < LPE) {
-            float sum[VEC];
+        for (int j = 0; j < VEC; ++j) tot[j] = 0.f;
+        for (int c = first; c <= last; ++c) {
+            if (__ldg(a.bnd + c + 1) == __ldg(a.bnd + c)) continue;
+            const float* pp = a.part + ((int64_t)c * 2 + (c == first ? 1 : 0)) * BP + sub * VEC;
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) sum[j] = 0.f;
-            for (int64_t qq = q_first; qq <= q_last; ++qq) {
-                const float* pp = a.part + (qq * 2 + (qq == q_first ? 1 : 0)) * BP + sub * VEC;
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) sum[j] += __ldcg(pp + j);
-            }
-            const float bo = a.bias ? __ldg(a.bias + r) : 0.f;
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                const int beta = sub * VEC + j;
-                if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = sum[j] + bo;
-            }
+            for (int j = 0; j < VEC; ++j) tot[j] += __ldcg(pp + j);
         }
-        if (lane == 0) a.cnt[r] = 0;
+        const float bo = a.bias ? __ldg(a.bias + r) : 0.f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const int beta = sub * VEC + j;
+            if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = tot[j] + bo;
+        }
+    }
+    if (lane == 0) a.cnt[r] = 0;
+}
+
+// After the block barrier: the warp where a cut segment starts adds the
+// partials of the following warps that continue it (warp order) and writes
+// the result, unless the segment leaves the block; warp 0 does the same for
+// the segment that entered the block from before.  Segments that cross a
+// block boundary continue in cross_block.
+template <int BP>
+__device__ __forceinline__ void block_combine(const SpmmArgs& a, const float* sp, const int* srow,
+                                              const Pending (&pend)[2], int warp, int lane,
+                                              int sub) {
+    using TL = Tile<BP>;
+    constexpr int VEC = TL::VEC, LPE = TL::LPE;
+    constexpr int W = kWarpsPerBlock;
+    if (pend[1].r < 0 && !(warp == 0 && pend[0].r >= 0)) return;
+    const BlockDesc bd = a.bdesc[blockIdx.x];
+#pragma unroll
+    for (int which = 1; which >= 0; --which) {
+        const int slot = which;
+        if (slot == 0 && warp != 0) continue;
+        const int r = pend[slot].r;
+        if (r < 0) continue;
+        float sum[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            sum[j] = lane < LPE ? sp[(warp * 2 + slot) * BP + sub * VEC + j] : 0.f;
+        for (int w2 = warp + 1; w2 < W && srow[w2 * 2] == r; ++w2) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                if (lane < LPE) sum[j] += sp[(w2 * 2) * BP + sub * VEC + j];
+        }
+        const bool ends_here = pend[slot].re <= (uint32_t)bd.k1;
+        if (slot == 1) {
+            if (ends_here) {
+                if (lane < LPE) {
+                    const float bo = a.bias ? __ldg(a.bias + r) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const int beta = sub * VEC + j;
+                        if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = sum[j] + bo;
+                    }
+                }
+            } else {
+                cross_block<BP>(a, r, 1, sum, blockIdx.x, bd.tail_last, bd.n_tail, lane, sub);
+            }
+        } else {
+            if (ends_here)
+                cross_block<BP>(a, r, 0, sum, bd.head_first, blockIdx.x, bd.n_head, lane, sub);
+            else
+                cross_block<BP>(a, r, 0, sum, bd.head_first, bd.tail_last,
+                                bd.n_head + bd.n_tail - 1, lane, sub);
+        }
     }
 }
 
 // One warp per chunk.  The chunk's entries [k0, k1) are streamed as a flat
-// sequence of blocks of 4*GPW entries (each group of LPE lanes owns 4
-// consecutive entries of a block).  Blocks sit in D+1 register slots: while
-// block j is consumed, blocks j+1 .. j+D are in flight (and, for the
-// transposed product, the values of block j+1 are being gathered).  The loop
-// over slots is unrolled so every slot index is a compile-time constant.  A
-// block inside one segment is consumed without masks; a block that straddles
-// segment boundaries is consumed once per segment it touches.
+// sequence of blocks of 4*GPW entries from the multiple of 4 at or below k0
+// (each group of LPE lanes owns 4 consecutive entries of a block).  Blocks
+// sit in D+1 register slots: while block j is consumed, blocks j+1 .. j+D
+// are in flight (and, for the transposed product, the values of block j+1
+// are being gathered).  The loop over slots is unrolled so every slot index
+// is a compile-time constant.  A block inside one segment is consumed
+// without masks; a block that straddles segment or chunk boundaries is
+// consumed once per segment it touches, with masks.
 template <int BP, bool GATHER, bool SMEM, bool I16 = SMEM && SNK_IDX16>
 __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     using TL = Tile<BP>;
@@ -161,15 +225,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     constexpr int NS = D + 1;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
+    float* sp = xs + (SMEM ? operand_floats(a.n_src, BP) : 0);
+    int* srow = reinterpret_cast<int*>(sp + kWarpsPerBlock * 2 * BP);
 
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int grp = lane / LPE;
     const int sub = lane % LPE;
     const uint32_t nnz = (uint32_t)a.nnz;
-    const uint32_t chunk = (uint32_t)a.chunk;
-    const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const bool active = q < a.n_chunks;
-    uint32_t k0 = 0, k1 = 0;
+    const int4 cd = a.cdesc[blockIdx.x * kWarpsPerBlock + warp];
+    const uint32_t k0 = (uint32_t)cd.x, k1 = (uint32_t)cd.y;
+    const uint32_t base_first = k0 & ~3u;
+    float* my_slots = sp + warp * 2 * BP;
 
     IdxBlk<I16> ib[NS];
     float wb[NS][4];
@@ -188,59 +255,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     };
 
     // Everything that only depends on the chunk is requested before the
-    // operand staging: the first blocks of the stream, the chunk descriptor
-    // and the first window of segment starts (and biases).
-    SegWindow win{0, 0, 0, 0u, 0.f};
-    if (active) {
-        k0 = (uint32_t)q * chunk;
-        k1 = min(k0 + chunk, nnz);
+    // operand staging: the first blocks of the stream and the first window of
+    // segment starts (and biases).
+    if (k0 < k1) {
 #pragma unroll
         for (int s = 0; s < NS; ++s)
-            if (k0 + s * BLK < k1) issue(s, k0 + s * BLK);
-        const int2 dsc = a.desc[q];
-        win.r_begin = dsc.x;
-        win.nrows = dsc.y - dsc.x;
-        win.load(0, lane, a.seg_ptr, a.bias);
+            if (base_first + s * BLK < k1) issue(s, base_first + s * BLK);
     }
-    if constexpr (SMEM) {
-        stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, kThreads);
-        __syncthreads();
-    }
-    if (!active) return;
+    SegWindow win{cd.z, cd.w - cd.z, 0, 0u, 0.f};
+    if (win.nrows > 0) win.load(0, lane, a.seg_ptr, a.bias);
+    if constexpr (SMEM) stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, kThreads);
+    __syncthreads();
     const float* xsrc = SMEM ? xs : a.xt;
-    if constexpr (GATHER) gather(0, k0);
 
-    const int r_begin = win.r_begin;
-    int i = 0;
-    uint32_t rs = win.bnd(0, lane, a.seg_ptr, a.bias), re = win.bnd(1, lane, a.seg_ptr, a.bias);
-    float acc[VEC];
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
     Pending pend[2] = {Pending{-1, 0u, 0u}, Pending{-1, 0u, 0u}};
-
-    auto consume = [&](int s, uint32_t blk0) {
-        const uint32_t base = blk0 + 4 * grp;
-        if (rs <= blk0 && blk0 + BLK < re && blk0 + BLK <= k1) {
-            // interior block: every entry belongs to the current segment,
-            // which continues past the block
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float x[VEC];
-                const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
-                if constexpr (SMEM) VecF<VEC>::load(px, x);
-                else VecF<VEC>::ldg(px, x);
-#pragma unroll
-                for (int t = 0; t < VEC; ++t) acc[t] = fmaf(wb[s][j], x[t], acc[t]);
-            }
-            return;
+    if (win.nrows > 0) {
+        if constexpr (GATHER) {
+            if (k0 < k1) gather(0, base_first);
         }
-        const uint32_t blk_end = min(blk0 + BLK, k1);
-        while (true) {
-            const uint32_t lo_k = max(rs, blk0), hi_k = min(re, blk_end);
+        const int r_begin = win.r_begin;
+        int i = 0;
+        uint32_t rs = win.bnd(0, lane, a.seg_ptr, a.bias), re = win.bnd(1, lane, a.seg_ptr, a.bias);
+        float acc[VEC];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t k = base + j;
-                if (k >= lo_k && k < hi_k) {
+        for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+
+        auto consume = [&](int s, uint32_t blk0) {
+            const uint32_t base = blk0 + 4 * grp;
+            if (rs <= blk0 && k0 <= blk0 && blk0 + BLK < re && blk0 + BLK <= k1) {
+                // interior block: every entry belongs to the current segment,
+                // which continues past the block
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
                     float x[VEC];
                     const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
                     if constexpr (SMEM) VecF<VEC>::load(px, x);
@@ -248,38 +294,63 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
 #pragma unroll
                     for (int t = 0; t < VEC; ++t) acc[t] = fmaf(wb[s][j], x[t], acc[t]);
                 }
+                return;
             }
-            if (min(re, k1) > blk_end) break;  // segment continues in the next block
-            finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub,
-                               pend);
+            const uint32_t blk_end = min(blk0 + BLK, k1);
+            while (true) {
+                const uint32_t lo_k = max(max(rs, k0), blk0), hi_k = min(re, blk_end);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t k = base + j;
+                    if (k >= lo_k && k < hi_k) {
+                        float x[VEC];
+                        const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
+                        if constexpr (SMEM) VecF<VEC>::load(px, x);
+                        else VecF<VEC>::ldg(px, x);
+#pragma unroll
+                        for (int t = 0; t < VEC; ++t) acc[t] = fmaf(wb[s][j], x[t], acc[t]);
+                    }
+                }
+                if (min(re, k1) > blk_end) break;  // segment continues in the next block
+                finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, win.bias_of(i), lane, sub,
+                                   my_slots, pend);
+                if (++i >= win.nrows) break;
+                rs = re;
+                re = win.bnd(i + 1, lane, a.seg_ptr, a.bias);
+                if (rs >= blk_end) break;
+            }
+        };
+
+        if (k0 < k1) {
+            for (uint32_t base0 = base_first; base0 < k1; base0 += NS * BLK) {
+#pragma unroll
+                for (int s = 0; s < NS; ++s) {
+                    const uint32_t blk0 = base0 + s * BLK;
+                    if (blk0 < k1) {
+                        if constexpr (GATHER) {
+                            if (blk0 + BLK < k1) gather((s + 1) % NS, blk0 + BLK);
+                        }
+                        consume(s, blk0);
+                        if (blk0 + NS * BLK < k1) issue(s, blk0 + NS * BLK);
+                    }
+                }
+            }
+        }
+        // segments that start at the end of the chunk (empty here)
+        while (i < win.nrows) {
+            finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, win.bias_of(i), lane, sub,
+                               my_slots, pend);
             if (++i >= win.nrows) break;
             rs = re;
             re = win.bnd(i + 1, lane, a.seg_ptr, a.bias);
-            if (rs >= blk_end) break;
-        }
-    };
-
-    for (uint32_t base0 = k0; base0 < k1; base0 += NS * BLK) {
-#pragma unroll
-        for (int s = 0; s < NS; ++s) {
-            const uint32_t blk0 = base0 + s * BLK;
-            if (blk0 < k1) {
-                if constexpr (GATHER) {
-                    if (blk0 + BLK < k1) gather((s + 1) % NS, blk0 + BLK);
-                }
-                consume(s, blk0);
-                if (blk0 + NS * BLK < k1) issue(s, blk0 + NS * BLK);
-            }
         }
     }
-    // segments that start at the end of the chunk (empty here)
-    while (i < win.nrows) {
-        finish_segment<BP>(a, acc, r_begin + i, rs, re, k0, k1, q, win.bias_of(i), lane, sub, pend);
-        if (++i >= win.nrows) break;
-        rs = re;
-        re = win.bnd(i + 1, lane, a.seg_ptr, a.bias);
+    if (lane == 0) {
+        srow[warp * 2 + 0] = pend[0].r;
+        srow[warp * 2 + 1] = pend[1].r;
     }
-    publish_partials<BP>(a, pend, lane, sub);
+    __syncthreads();
+    block_combine<BP>(a, sp, srow, pend, warp, lane, sub);
 }
 
 // Transposed copy of the operand for the global-memory path.
@@ -296,23 +367,28 @@ __global__ void k_fill_bias(float* Y, int64_t b, int64_t n, const float* bias) {
         Y[i] = bias ? bias[i % n] : 0.f;
 }
 
+template <typename F>
+static int set_smem(F fn, size_t smem) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return SNK_ERR_CUDA;
+    return SNK_OK;
+}
+
 template <int BP, bool GATHER>
 static int launch_bp(Layer* L, SpmmArgs a, cudaStream_t s) {
-    const size_t smem = (size_t)a.n_src * BP * sizeof(float);
-    const int grid = (int)std::min<int64_t>(L->num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
-    // every chunk needs its own warp (the kernels take one chunk per warp)
-    if ((int64_t)grid * kWarpsPerBlock < a.n_chunks) return SNK_ERR_ARG;
+    const size_t slots = spmm_slot_bytes<BP>();
+    const size_t smem = operand_floats(a.n_src, BP) * sizeof(float) + slots;
     if (smem <= (size_t)L->max_smem && a.idx16) {
         auto fn = k_spmm<BP, GATHER, true>;
-        if (smem > 48 * 1024 &&
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-                cudaSuccess)
-            return SNK_ERR_CUDA;
-        fn<<<grid, kThreads, smem, s>>>(a);
+        if (set_smem(fn, smem) != SNK_OK) return SNK_ERR_CUDA;
+        fn<<<a.n_blocks, kThreads, smem, s>>>(a);
     } else {
         k_transpose<BP><<<L->num_sms * 4, 256, 0, s>>>(a.X, a.n_src, a.b, L->xt);
         a.xt = L->xt;
-        k_spmm<BP, GATHER, false><<<grid, kThreads, 0, s>>>(a);
+        auto fn = k_spmm<BP, GATHER, false>;
+        if (set_smem(fn, slots) != SNK_OK) return SNK_ERR_CUDA;
+        fn<<<a.n_blocks, kThreads, slots, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
@@ -350,38 +426,35 @@ static int run_spmm(Layer* L, SpmmArgs a, int64_t b, cudaStream_t s) {
     return SNK_OK;
 }
 
-// Forward SpMM on a caller's CSR (32-bit column indices) with scratch supplied
-// by the caller: chunk descriptors, split-segment partials and zeroed arrival
-// counters.  Shared-memory operand path only.
+// Forward SpMM on a caller's CSR (32-bit column indices) with a partition and
+// scratch supplied by the caller (the allocation-free entry point).  Shared-
+// memory operand path only.
 template <int BP>
-static int launch_csr_bp(SpmmArgs a, int num_sms, int max_smem, cudaStream_t s) {
-    const size_t smem = (size_t)a.n_src * BP * sizeof(float);
+static int launch_csr_bp(SpmmArgs a, int max_smem, cudaStream_t s) {
+    const size_t smem = operand_floats(a.n_src, BP) * sizeof(float) + spmm_slot_bytes<BP>();
     if (smem > (size_t)max_smem) return SNK_ERR_LIMIT;
-    const int grid = (int)std::min<int64_t>(num_sms, ceil_div(a.n_chunks, kWarpsPerBlock));
-    if ((int64_t)grid * kWarpsPerBlock < a.n_chunks) return SNK_ERR_ARG;
     auto fn = k_spmm<BP, false, true, false>;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-        return SNK_ERR_CUDA;
-    fn<<<grid, kThreads, smem, s>>>(a);
+    if (set_smem(fn, smem) != SNK_OK) return SNK_ERR_CUDA;
+    fn<<<a.n_blocks, kThreads, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
 int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row_ptr,
-                       const int2* desc, int64_t nnz, int64_t out_f, int64_t in_f, int chunk,
-                       int n_chunks, const float* X, int64_t b, const float* bias, float* Y,
-                       float* part, int32_t* cnt, int num_sms, int max_smem, cudaStream_t s) {
+                       const int4* cdesc, const BlockDesc* bdesc, const int32_t* bnd, int64_t nnz,
+                       int64_t out_f, int64_t in_f, int n_blocks, const float* X, int64_t b,
+                       const float* bias, float* Y, float* part, int32_t* cnt, int max_smem,
+                       cudaStream_t s) {
     SpmmArgs a{};
     a.val = val;
     a.idx = cols;
     a.seg_ptr = row_ptr;
-    a.desc = desc;
+    a.cdesc = cdesc;
+    a.bdesc = bdesc;
+    a.bnd = bnd;
     a.nnz = nnz;
     a.n_seg = out_f;
     a.n_src = in_f;
-    a.chunk = chunk;
-    a.n_chunks = n_chunks;
+    a.n_blocks = n_blocks;
     a.bias = bias;
     a.part = part;
     a.cnt = cnt;
@@ -392,17 +465,17 @@ int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row
         a.Y = Y + t0 * out_f;
         int st;
         if (nnz == 0) {
-            k_fill_bias<<<num_sms * 4, 256, 0, s>>>(a.Y, bt, out_f, bias);
+            k_fill_bias<<<n_blocks * 4, 256, 0, s>>>(a.Y, bt, out_f, bias);
             st = cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
         } else {
             switch (batch_tile(bt)) {
-                case 1: st = launch_csr_bp<1>(a, num_sms, max_smem, s); break;
-                case 2: st = launch_csr_bp<2>(a, num_sms, max_smem, s); break;
-                case 4: st = launch_csr_bp<4>(a, num_sms, max_smem, s); break;
-                case 8: st = launch_csr_bp<8>(a, num_sms, max_smem, s); break;
-                case 16: st = launch_csr_bp<16>(a, num_sms, max_smem, s); break;
-                case 32: st = launch_csr_bp<32>(a, num_sms, max_smem, s); break;
-                default: st = launch_csr_bp<64>(a, num_sms, max_smem, s); break;
+                case 1: st = launch_csr_bp<1>(a, max_smem, s); break;
+                case 2: st = launch_csr_bp<2>(a, max_smem, s); break;
+                case 4: st = launch_csr_bp<4>(a, max_smem, s); break;
+                case 8: st = launch_csr_bp<8>(a, max_smem, s); break;
+                case 16: st = launch_csr_bp<16>(a, max_smem, s); break;
+                case 32: st = launch_csr_bp<32>(a, max_smem, s); break;
+                default: st = launch_csr_bp<64>(a, max_smem, s); break;
             }
         }
         if (st != SNK_OK) return st;
@@ -410,46 +483,50 @@ int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row
     return SNK_OK;
 }
 
-int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float* Y,
-                   cudaStream_t s) {
+static SpmmArgs layer_args(Layer* L, bool columns) {
     SpmmArgs a{};
     a.val = L->v;
-    a.perm = nullptr;
-    a.idx = L->c;
-    a.idx16 = L->c16;
-    a.seg_ptr = L->row_ptr;
-    a.desc = L->desc_r;
     a.nnz = L->nnz;
-    a.n_seg = L->out_f;
-    a.n_src = L->in_f;
-    a.chunk = L->chunk;
-    a.n_chunks = L->n_chunks;
+    a.n_blocks = L->n_blocks;
+    a.part = L->part;
+    a.cnt = L->cnt;
+    if (!columns) {
+        a.idx = L->c;
+        a.idx16 = L->c16;
+        a.seg_ptr = L->row_ptr;
+        a.cdesc = L->cdesc_r;
+        a.bdesc = L->bdesc_r;
+        a.bnd = L->bnd_r;
+        a.n_seg = L->out_f;
+        a.n_src = L->in_f;
+    } else {
+        a.perm = L->perm;
+        a.idx = L->rows_c;
+        a.idx16 = L->rc16;
+        a.seg_ptr = L->col_ptr;
+        a.cdesc = L->cdesc_c;
+        a.bdesc = L->bdesc_c;
+        a.bnd = L->bnd_c;
+        a.n_seg = L->in_f;
+        a.n_src = L->out_f;
+    }
+    return a;
+}
+
+int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float* Y,
+                   cudaStream_t s) {
+    SpmmArgs a = layer_args(L, false);
     a.X = X;
     a.bias = bias;
     a.Y = Y;
-    a.part = L->part;
-    a.cnt = L->cnt;
     return run_spmm<false>(L, a, b, s);
 }
 
 int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaStream_t s) {
-    SpmmArgs a{};
-    a.val = L->v;
-    a.perm = L->perm;
-    a.idx = L->rows_c;
-    a.idx16 = L->rc16;
-    a.seg_ptr = L->col_ptr;
-    a.desc = L->desc_c;
-    a.nnz = L->nnz;
-    a.n_seg = L->in_f;
-    a.n_src = L->out_f;
-    a.chunk = L->chunk;
-    a.n_chunks = L->n_chunks;
+    SpmmArgs a = layer_args(L, true);
     a.X = dY;
     a.bias = nullptr;
     a.Y = dX;
-    a.part = L->part;
-    a.cnt = L->cnt;
     return run_spmm<true>(L, a, b, s);
 }
 

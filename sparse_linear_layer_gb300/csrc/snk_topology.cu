@@ -343,12 +343,9 @@ __global__ void k_narrow16(const int32_t* __restrict__ src, int64_t n, int64_t n
         dst[k] = k < n ? (uint16_t)src[k] : (uint16_t)0;
 }
 
-// Chunk descriptor: chunk q covers entries [q*chunk, (q+1)*chunk).  It owns
-// the segments whose start lies in that range (the last chunk also owns the
-// empty segments at the very end) and continues the segment that runs into
-// it from before.  desc[q] = (first segment it touches, one past its last).
-__device__ __forceinline__ int64_t lower_bound_ptr(const int32_t* ptr, int64_t n_seg, int64_t t) {
-    int64_t lo = 0, hi = n_seg;
+// ---- work partition -----------------------------------------------------
+__device__ __forceinline__ int64_t lower_bound_ptr(const int32_t* ptr, int64_t n, int64_t t) {
+    int64_t lo = 0, hi = n;
     while (lo < hi) {
         const int64_t mid = (lo + hi) >> 1;
         if ((int64_t)ptr[mid] < t) lo = mid + 1;
@@ -356,25 +353,89 @@ __device__ __forceinline__ int64_t lower_bound_ptr(const int32_t* ptr, int64_t n
     }
     return lo;
 }
-
-__global__ void k_desc(const int32_t* __restrict__ ptr, int64_t n_seg, int32_t chunk,
-                       int32_t n_chunks, int2* __restrict__ desc) {
-    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n_chunks; q += gridDim.x * blockDim.x) {
-        const int64_t k0 = (int64_t)q * chunk;
-        const int64_t lo = lower_bound_ptr(ptr, n_seg, k0);
-        const int64_t hi = (q + 1 == n_chunks) ? n_seg : lower_bound_ptr(ptr, n_seg, k0 + chunk);
-        const int64_t first = (lo > 0 && (int64_t)ptr[lo] > k0) ? lo - 1 : lo;
-        desc[q] = make_int2((int)first, (int)hi);
+// largest i with a[i] <= t (a non-decreasing, a[0] <= t)
+__device__ __forceinline__ int64_t last_le(const int32_t* a, int64_t n, int64_t t) {
+    int64_t lo = 0, hi = n;  // first index with a[i] > t
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)a[mid] <= t) lo = mid + 1;
+        else hi = mid;
     }
+    return lo - 1;
 }
 
-int launch_chunk_desc(const int32_t* ptr, int64_t n_seg, int32_t chunk, int32_t n_chunks,
-                      int2* desc, int num_sms, cudaStream_t s) {
-    if (n_chunks <= 0) return SNK_OK;
+// Block boundaries: the even split point c*nnz/n_blocks (rounded down to a
+// multiple of 4), moved to the nearer boundary of the segment it falls in,
+// unless that segment is longer than half a block's share (then it is cut).
+__global__ void k_block_bounds(const int32_t* __restrict__ ptr, int64_t n_seg, int64_t nnz,
+                               int n_blocks, int32_t* __restrict__ bnd) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c > n_blocks) return;
+    if (c == 0 || c == n_blocks) {
+        bnd[c] = c == 0 ? 0 : (int32_t)nnz;
+        return;
+    }
+    const int64_t t = ((int64_t)c * nnz / n_blocks) & ~(int64_t)3;
+    int64_t r = last_le(ptr, n_seg + 1, t);
+    if (r > n_seg - 1) r = n_seg - 1;
+    const int64_t lo = ptr[r], hi = ptr[r + 1];
+    const int64_t share = nnz / n_blocks;
+    int64_t k;
+    if (hi - lo > share / 2) k = t;
+    else k = (t - lo <= hi - t) ? lo : hi;
+    bnd[c] = (int32_t)k;
+}
+
+// Chunk q = (block c, warp w): an equal share of the block's range, rounded
+// to a multiple of 4 entries; (k0, k1, first segment touched, one past the
+// last segment it owns).  A chunk owns the segments whose start lies in
+// [k0, k1) (the very last chunk also owns the empty segments at the end) and
+// continues the segment that runs into it, if it holds any entry.  Thread
+// w = 0 of each block also fills the block descriptor.
+__global__ void k_chunk_desc(const int32_t* __restrict__ ptr, int64_t n_seg,
+                             const int32_t* __restrict__ bnd, int n_blocks, int warps,
+                             int4* __restrict__ cdesc, BlockDesc* __restrict__ bdesc) {
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= n_blocks * warps) return;
+    const int c = q / warps, w = q % warps;
+    const int64_t kc = bnd[c], kn = bnd[c + 1];
+    const int64_t len = kn - kc;
+    const int64_t sz = len > 0 ? ((len + warps - 1) / warps + 3) / 4 * 4 : 0;
+    const int64_t k0 = min(kc + w * sz, kn);
+    const int64_t k1 = (w == warps - 1) ? kn : min(kc + (w + 1) * sz, kn);
+    const bool last = (q == n_blocks * warps - 1);
+    const int64_t lo = lower_bound_ptr(ptr, n_seg, k0);
+    const int64_t hi = last ? n_seg : lower_bound_ptr(ptr, n_seg, k1);
+    const int64_t first = (k1 > k0 && lo > 0 && (int64_t)ptr[lo] > k0) ? lo - 1 : lo;
+    cdesc[q] = make_int4((int)k0, (int)k1, (int)first, (int)hi);
+    if (w != 0) return;
+    BlockDesc d;
+    d.k0 = (int)kc;
+    d.k1 = (int)kn;
+    d.head_first = c;
+    d.tail_last = c;
+    d.pad0 = d.pad1 = 0;
+    if (kn > kc) {
+        const int64_t r = last_le(ptr, n_seg + 1, kc);
+        if ((int64_t)ptr[r] < kc) d.head_first = (int)last_le(bnd, n_blocks + 1, ptr[r]);
+        const int64_t r2 = last_le(ptr, n_seg + 1, kn - 1);
+        if ((int64_t)ptr[r2 + 1] > kn) d.tail_last = (int)last_le(bnd, n_blocks + 1, ptr[r2 + 1] - 1);
+    }
+    int nh = 0, nt = 0;
+    for (int x = d.head_first; x <= c; ++x) nh += bnd[x + 1] > bnd[x];
+    for (int x = c; x <= d.tail_last; ++x) nt += bnd[x + 1] > bnd[x];
+    d.n_head = nh;
+    d.n_tail = nt;
+    bdesc[c] = d;
+}
+
+int build_partition(const int32_t* ptr, int64_t n_seg, int64_t nnz, int n_blocks, int32_t* bnd,
+                    int4* cdesc, BlockDesc* bdesc, cudaStream_t s) {
     const int T = 256;
-    const unsigned g = (unsigned)std::max<int64_t>(
-        1, std::min<int64_t>(ceil_div(n_chunks, T), (int64_t)num_sms * 8));
-    k_desc<<<g, T, 0, s>>>(ptr, n_seg, chunk, n_chunks, desc);
+    k_block_bounds<<<(unsigned)ceil_div(n_blocks + 1, T), T, 0, s>>>(ptr, n_seg, nnz, n_blocks, bnd);
+    const int64_t nq = (int64_t)n_blocks * kWarpsPerBlock;
+    k_chunk_desc<<<(unsigned)ceil_div(nq, T), T, 0, s>>>(ptr, n_seg, bnd, n_blocks, kWarpsPerBlock,
+                                                         cdesc, bdesc);
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
@@ -463,12 +524,11 @@ int build_topology(Layer* L, cudaStream_t s, bool validate) {
         k_narrow16<<<grid_for(L->nnz_pad, T, L->num_sms), T, 0, s>>>(L->rows_c, n, L->nnz_pad,
                                                                      L->rc16);
 
-    if (L->n_chunks > 0) {
-        k_desc<<<grid_for(L->n_chunks, T, L->num_sms), T, 0, s>>>(L->row_ptr, L->out_f, L->chunk,
-                                                                  L->n_chunks, L->desc_r);
-        k_desc<<<grid_for(L->n_chunks, T, L->num_sms), T, 0, s>>>(L->col_ptr, L->in_f, L->chunk,
-                                                                  L->n_chunks, L->desc_c);
-    }
+    if (build_partition(L->row_ptr, L->out_f, n, L->n_blocks, L->bnd_r, L->cdesc_r, L->bdesc_r, s) !=
+            SNK_OK ||
+        build_partition(L->col_ptr, L->in_f, n, L->n_blocks, L->bnd_c, L->cdesc_c, L->bdesc_c, s) !=
+            SNK_OK)
+        return SNK_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SNK_ERR_CUDA;
     L->topology_version += 1;
