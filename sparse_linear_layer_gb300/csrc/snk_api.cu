@@ -93,7 +93,7 @@ int snk_create(snk_handle* handle, int64_t out_f, int64_t in_f, int64_t nnz, flo
     }
     // one block per SM, one chunk per warp
     L->n_blocks = L->num_sms;
-    L->n_chunks = L->n_blocks * kWarpsPerBlock;
+    L->n_chunks = L->n_blocks * std::max(kWarpsPerBlock, kWarpsPerBlockDx);
     const int64_t n_max = std::max(out_f, in_f);
     const bool wide = (uint64_t)out_f * (uint64_t)in_f > (1ull << 32);
     L->tile_hist_len = topology_hist_len(nnz);

@@ -20,6 +20,12 @@ constexpr int kWarp = 32;
 #ifndef SNK_PIPE_DX
 #define SNK_PIPE_DX 1      // the same for the transposed product
 #endif
+#ifndef SNK_GATHER_LEAD
+#define SNK_GATHER_LEAD 1  // transposed product: blocks whose values are gathered ahead
+#endif
+#ifndef SNK_THREADS_DX
+#define SNK_THREADS_DX SNK_THREADS  // block size of the transposed product
+#endif
 #ifndef SNK_PIPE_DW
 #define SNK_PIPE_DW 4      // the same for the weight gradient
 #endif
@@ -29,6 +35,8 @@ constexpr int kWarp = 32;
 
 constexpr int kThreads = SNK_THREADS;
 constexpr int kWarpsPerBlock = kThreads / kWarp;
+constexpr int kThreadsDx = SNK_THREADS_DX;
+constexpr int kWarpsPerBlockDx = kThreadsDx / kWarp;
 constexpr int kChunksPerSm = kWarpsPerBlock;   // merge-path chunks per SM (one per warp)
 constexpr int kMaxBatchTile = 64;    // batch columns handled by one launch
 constexpr int kStreamPad = 128;      // zero entries after library-owned streams
@@ -78,7 +86,7 @@ struct Layer {
     // SM owns a range of entries aligned to segment boundaries, split into one
     // chunk per warp
     int32_t n_blocks = 0;         // blocks (= SMs)
-    int32_t n_chunks = 0;         // n_blocks * kWarpsPerBlock
+    int32_t n_chunks = 0;         // n_blocks * (warps per block of the larger kernel)
     int32_t* bnd_r = nullptr;     // [n_blocks+1] first entry of each block (rows)
     int32_t* bnd_c = nullptr;     // [n_blocks+1] the same (columns)
     int4* cdesc_r = nullptr;      // [n_chunks] (k0, k1, first segment touched, one past last)
@@ -132,8 +140,8 @@ int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s);
 // Partition nnz entries with segment pointer ptr[n_seg+1] over n_blocks
 // blocks of kWarpsPerBlock chunks (block boundaries on segment boundaries
 // except inside segments longer than half a block's share).
-int build_partition(const int32_t* ptr, int64_t n_seg, int64_t nnz, int n_blocks, int32_t* bnd,
-                    int4* cdesc, BlockDesc* bdesc, cudaStream_t s);
+int build_partition(const int32_t* ptr, int64_t n_seg, int64_t nnz, int n_blocks, int warps,
+                    int32_t* bnd, int4* cdesc, BlockDesc* bdesc, cudaStream_t s);
 int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row_ptr,
                        const int4* cdesc, const BlockDesc* bdesc, const int32_t* bnd, int64_t nnz,
                        int64_t out_f, int64_t in_f, int n_blocks, const float* X, int64_t b,

@@ -118,7 +118,7 @@ extern "C" int snk_forward_csr_noalloc(int64_t out_features, int64_t in_features
     // not trusted
     if (cudaMemsetAsync(cnt, 0, (size_t)out_features * sizeof(int32_t), s) != cudaSuccess)
         return SNK_ERR_CUDA;
-    st = build_partition(row_ptr, out_features, nnz, n_blocks, bnd, cdesc, bdesc, s);
+    st = build_partition(row_ptr, out_features, nnz, n_blocks, kWarpsPerBlock, bnd, cdesc, bdesc, s);
     if (st != SNK_OK) return st;
     return launch_forward_csr(values, cols, row_ptr, cdesc, bdesc, bnd, nnz, out_features,
                               in_features, n_blocks, X, batch, bias, Y, part, cnt, max_smem, s);

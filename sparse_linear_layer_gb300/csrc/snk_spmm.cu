@@ -70,9 +70,15 @@ struct Pending {
 
 // Shared memory: [transposed operand (shared-memory path)][partials
 // [warps][2][BP]][segment ids [warps][2]].
-template <int BP>
+template <bool GATHER>
+struct SpmmShape {
+    static constexpr int kNT = GATHER ? kThreadsDx : kThreads;
+    static constexpr int kW = kNT / kWarp;
+};
+template <int BP, bool GATHER>
 __host__ __device__ constexpr size_t spmm_slot_bytes() {
-    return (size_t)kWarpsPerBlock * 2 * BP * sizeof(float) + (size_t)kWarpsPerBlock * 2 * sizeof(int);
+    return (size_t)SpmmShape<GATHER>::kW * 2 * BP * sizeof(float) +
+           (size_t)SpmmShape<GATHER>::kW * 2 * sizeof(int);
 }
 __host__ __device__ inline size_t operand_floats(int64_t n_src, int bp) {
     return ((size_t)n_src * bp + 3) & ~(size_t)3;
@@ -159,13 +165,12 @@ __device__ __noinline__ void cross_block(const SpmmArgs& a, int r, int slot,
 // the result, unless the segment leaves the block; warp 0 does the same for
 // the segment that entered the block from before.  Segments that cross a
 // block boundary continue in cross_block.
-template <int BP>
+template <int BP, int W>
 __device__ __forceinline__ void block_combine(const SpmmArgs& a, const float* sp, const int* srow,
                                               const Pending (&pend)[2], int warp, int lane,
                                               int sub) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE;
-    constexpr int W = kWarpsPerBlock;
     if (pend[1].r < 0 && !(warp == 0 && pend[0].r >= 0)) return;
     const BlockDesc bd = a.bdesc[blockIdx.x];
 #pragma unroll
@@ -211,29 +216,34 @@ __device__ __forceinline__ void block_combine(const SpmmArgs& a, const float* sp
 // sequence of blocks of 4*GPW entries from the multiple of 4 at or below k0
 // (each group of LPE lanes owns 4 consecutive entries of a block).  Blocks
 // sit in D+1 register slots: while block j is consumed, blocks j+1 .. j+D
-// are in flight (and, for the transposed product, the values of block j+1
-// are being gathered).  The loop over slots is unrolled so every slot index
+// are in flight (and, for the transposed product, the values of blocks
+// j+1 .. j+G are being gathered).  The loop over slots is unrolled so every slot index
 // is a compile-time constant.  A block inside one segment is consumed
 // without masks; a block that straddles segment or chunk boundaries is
 // consumed once per segment it touches, with masks.
 template <int BP, bool GATHER, bool SMEM, bool I16 = SMEM && SNK_IDX16>
-__global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
+__global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmArgs a) {
+    constexpr int NT = SpmmShape<GATHER>::kNT;
+    constexpr int W = SpmmShape<GATHER>::kW;
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
     constexpr int D = GATHER ? SNK_PIPE_DX : SNK_PIPE_FWD;
     constexpr int NS = D + 1;
+    // blocks whose values are gathered ahead of the consumed one (the
+    // permutation of a block arrives NS - G blocks before its gather)
+    constexpr int G = GATHER ? (SNK_GATHER_LEAD < D ? SNK_GATHER_LEAD : D) : 0;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
     float* sp = xs + (SMEM ? operand_floats(a.n_src, BP) : 0);
-    int* srow = reinterpret_cast<int*>(sp + kWarpsPerBlock * 2 * BP);
+    int* srow = reinterpret_cast<int*>(sp + W * 2 * BP);
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int grp = lane / LPE;
     const int sub = lane % LPE;
     const uint32_t nnz = (uint32_t)a.nnz;
-    const int4 cd = a.cdesc[blockIdx.x * kWarpsPerBlock + warp];
+    const int4 cd = a.cdesc[blockIdx.x * W + warp];
     const uint32_t k0 = (uint32_t)cd.x, k1 = (uint32_t)cd.y;
     const uint32_t base_first = k0 & ~3u;
     float* my_slots = sp + warp * 2 * BP;
@@ -264,14 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
     }
     SegWindow win{cd.z, cd.w - cd.z, 0, 0u, 0.f};
     if (win.nrows > 0) win.load(0, lane, a.seg_ptr, a.bias);
-    if constexpr (SMEM) stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, kThreads);
+    if constexpr (SMEM) stage_transposed<BP>(xs, a.X, a.n_src, a.b, a.n_src, threadIdx.x, NT);
     __syncthreads();
     const float* xsrc = SMEM ? xs : a.xt;
 
     Pending pend[2] = {Pending{-1, 0u, 0u}, Pending{-1, 0u, 0u}};
     if (win.nrows > 0) {
         if constexpr (GATHER) {
-            if (k0 < k1) gather(0, base_first);
+#pragma unroll
+            for (int s = 0; s < G; ++s)
+                if (k0 < k1 && base_first + s * BLK < k1) gather(s, base_first + s * BLK);
         }
         const int r_begin = win.r_begin;
         int i = 0;
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
                     const uint32_t blk0 = base0 + s * BLK;
                     if (blk0 < k1) {
                         if constexpr (GATHER) {
-                            if (blk0 + BLK < k1) gather((s + 1) % NS, blk0 + BLK);
+                            if (blk0 + G * BLK < k1) gather((s + G) % NS, blk0 + G * BLK);
                         }
                         consume(s, blk0);
                         if (blk0 + NS * BLK < k1) issue(s, blk0 + NS * BLK);
@@ -350,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_spmm(const SpmmArgs a) {
         srow[warp * 2 + 1] = pend[1].r;
     }
     __syncthreads();
-    block_combine<BP>(a, sp, srow, pend, warp, lane, sub);
+    block_combine<BP, W>(a, sp, srow, pend, warp, lane, sub);
 }
 
 // Transposed copy of the operand for the global-memory path.
@@ -377,18 +389,19 @@ static int set_smem(F fn, size_t smem) {
 
 template <int BP, bool GATHER>
 static int launch_bp(Layer* L, SpmmArgs a, cudaStream_t s) {
-    const size_t slots = spmm_slot_bytes<BP>();
+    constexpr int NT = SpmmShape<GATHER>::kNT;
+    const size_t slots = spmm_slot_bytes<BP, GATHER>();
     const size_t smem = operand_floats(a.n_src, BP) * sizeof(float) + slots;
     if (smem <= (size_t)L->max_smem && a.idx16) {
         auto fn = k_spmm<BP, GATHER, true>;
         if (set_smem(fn, smem) != SNK_OK) return SNK_ERR_CUDA;
-        fn<<<a.n_blocks, kThreads, smem, s>>>(a);
+        fn<<<a.n_blocks, NT, smem, s>>>(a);
     } else {
         k_transpose<BP><<<L->num_sms * 4, 256, 0, s>>>(a.X, a.n_src, a.b, L->xt);
         a.xt = L->xt;
         auto fn = k_spmm<BP, GATHER, false>;
         if (set_smem(fn, slots) != SNK_OK) return SNK_ERR_CUDA;
-        fn<<<a.n_blocks, kThreads, slots, s>>>(a);
+        fn<<<a.n_blocks, NT, slots, s>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
@@ -431,7 +444,7 @@ static int run_spmm(Layer* L, SpmmArgs a, int64_t b, cudaStream_t s) {
 // memory operand path only.
 template <int BP>
 static int launch_csr_bp(SpmmArgs a, int max_smem, cudaStream_t s) {
-    const size_t smem = operand_floats(a.n_src, BP) * sizeof(float) + spmm_slot_bytes<BP>();
+    const size_t smem = operand_floats(a.n_src, BP) * sizeof(float) + spmm_slot_bytes<BP, false>();
     if (smem > (size_t)max_smem) return SNK_ERR_LIMIT;
     auto fn = k_spmm<BP, false, true, false>;
     if (set_smem(fn, smem) != SNK_OK) return SNK_ERR_CUDA;

@@ -429,13 +429,13 @@ __global__ void k_chunk_desc(const int32_t* __restrict__ ptr, int64_t n_seg,
     bdesc[c] = d;
 }
 
-int build_partition(const int32_t* ptr, int64_t n_seg, int64_t nnz, int n_blocks, int32_t* bnd,
-                    int4* cdesc, BlockDesc* bdesc, cudaStream_t s) {
+int build_partition(const int32_t* ptr, int64_t n_seg, int64_t nnz, int n_blocks, int warps,
+                    int32_t* bnd, int4* cdesc, BlockDesc* bdesc, cudaStream_t s) {
     const int T = 256;
     k_block_bounds<<<(unsigned)ceil_div(n_blocks + 1, T), T, 0, s>>>(ptr, n_seg, nnz, n_blocks, bnd);
-    const int64_t nq = (int64_t)n_blocks * kWarpsPerBlock;
-    k_chunk_desc<<<(unsigned)ceil_div(nq, T), T, 0, s>>>(ptr, n_seg, bnd, n_blocks, kWarpsPerBlock,
-                                                         cdesc, bdesc);
+    const int64_t nq = (int64_t)n_blocks * warps;
+    k_chunk_desc<<<(unsigned)ceil_div(nq, T), T, 0, s>>>(ptr, n_seg, bnd, n_blocks, warps, cdesc,
+                                                         bdesc);
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
@@ -524,10 +524,10 @@ int build_topology(Layer* L, cudaStream_t s, bool validate) {
         k_narrow16<<<grid_for(L->nnz_pad, T, L->num_sms), T, 0, s>>>(L->rows_c, n, L->nnz_pad,
                                                                      L->rc16);
 
-    if (build_partition(L->row_ptr, L->out_f, n, L->n_blocks, L->bnd_r, L->cdesc_r, L->bdesc_r, s) !=
-            SNK_OK ||
-        build_partition(L->col_ptr, L->in_f, n, L->n_blocks, L->bnd_c, L->cdesc_c, L->bdesc_c, s) !=
-            SNK_OK)
+    if (build_partition(L->row_ptr, L->out_f, n, L->n_blocks, kWarpsPerBlock, L->bnd_r, L->cdesc_r,
+                        L->bdesc_r, s) != SNK_OK ||
+        build_partition(L->col_ptr, L->in_f, n, L->n_blocks, kWarpsPerBlockDx, L->bnd_c, L->cdesc_c,
+                        L->bdesc_c, s) != SNK_OK)
         return SNK_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SNK_ERR_CUDA;
