@@ -66,6 +66,10 @@ def parse():
     p.add_argument("--sweep", default=None, metavar="FILE",
                    help="instead of the single line, write one JSON object per "
                         "(sparsity, batch) of the 10000x10000 sweep to FILE")
+    p.add_argument("--latency", default=None, metavar="FILE",
+                   help="instead of the single line, write one JSON object per layer of the "
+                        "batch-1 inference-latency set (forward only; cold, warm and "
+                        "CUDA-graph replay) to FILE")
     return p.parse_args()
 
 
@@ -396,6 +400,107 @@ def run_sweep(args, dev):
             g.close()
 
 
+# Batch-1 forward layers of the pages' latency tables: the GAMLP-shaped 5000 x 5000
+# layer ([SNACK] Table 6, latency in ms) and the 12500 x 10000 layer ([SNACK]
+# Table 10, CUDA time in us), with the pages' own numbers (other hardware).
+LATENCY_SET = [
+    (5000, 5000, 90, {"source": "[SNACK] Table 6", "inference_latency_ms": 0.25}),
+    (5000, 5000, 95, {"source": "[SNACK] Table 6", "inference_latency_ms": 0.21}),
+    (5000, 5000, 99, {"source": "[SNACK] Table 6", "inference_latency_ms": 0.21}),
+    (12500, 10000, 90, {"source": "[SNACK] Table 10", "cuda_us": 163.1}),
+    (12500, 10000, 95, {"source": "[SNACK] Table 10", "cuda_us": 83.0}),
+    (12500, 10000, 99, None),
+    (2500, 10000, 90, None),
+    (7500, 10000, 90, None),
+]
+
+
+def run_latency(args, dev):
+    """Forward latency at batch 1: one call after an L2 flush (cold,
+    event-timed); back-to-back direct calls and back-to-back replays of a CUDA
+    graph holding one forward call (warm: the layer stays in L2, as in
+    repeated inference; device time per call); and one call at a time, issue
+    to completion on the host clock, direct and as a graph replay."""
+    import torch
+
+    from sparse_linear_layer_gb300 import binding, synth
+    flush = L2Flush(torch, dev, args.flush_mb) if args.flush_mb else None
+    stream = torch.cuda.current_stream(dev)
+    n = max(args.steps, 20)
+    with open(args.latency, "w") as fo:
+        for out_f, in_f, sp, pages in LATENCY_SET:
+            lay, g, _, _, _, _, bias = make_device_layer(torch, binding, synth, dev, out_f, in_f,
+                                                         sp, 1)
+            X = torch.randn(1, in_f, device=dev)
+            Y = torch.empty(1, out_f, device=dev)
+            fwd = lambda: binding.snk_forward(g.handle, X, bias, Y, stream.cuda_stream)
+            for _ in range(args.warmup):
+                fwd()
+            torch.cuda.synchronize()
+            # cold
+            cold = []
+            for _ in range(n):
+                if flush is not None:
+                    flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fwd()
+                e1.record(stream)
+                e1.synchronize()
+                cold.append(e0.elapsed_time(e1) * 1e3)
+            # warm, direct calls back to back
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(n):
+                fwd()
+            e1.record(stream)
+            e1.synchronize()
+            warm = e0.elapsed_time(e1) * 1e3 / n
+            # warm, graph replays
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                binding.snk_forward(g.handle, X, bias, Y, side.cuda_stream)
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                binding.snk_forward(g.handle, X, bias, Y)
+            torch.cuda.synchronize()
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(torch.cuda.current_stream(dev))
+            for _ in range(n):
+                graph.replay()
+            e1.record(torch.cuda.current_stream(dev))
+            e1.synchronize()
+            replay = e0.elapsed_time(e1) * 1e3 / n
+            # one call at a time, host wall clock from issue to completion
+            sync = {}
+            for name, call in (("direct", fwd), ("graph", graph.replay)):
+                ts = []
+                for _ in range(n):
+                    t0 = time.perf_counter()
+                    call()
+                    torch.cuda.current_stream(dev).synchronize()
+                    ts.append((time.perf_counter() - t0) * 1e6)
+                sync[name] = statistics.median(ts)
+            row = {"out": out_f, "in": in_f, "sparsity_pct": sp, "nnz": lay.nnz, "batch": 1,
+                   "op": "forward", "calls": n,
+                   "us_cold_mean": statistics.mean(cold), "us_cold_median": statistics.median(cold),
+                   "us_warm_direct": warm, "us_warm_graph_replay": replay,
+                   "us_wall_sync_direct_median": sync["direct"],
+                   "us_wall_sync_graph_median": sync["graph"],
+                   "pages": pages}
+            fo.write(json.dumps(row) + "\n")
+            fo.flush()
+            del graph
+            g.close()
+
+
 def run_ours(args, workload, rank, world, local):
     import numpy as np
     import torch
@@ -406,6 +511,9 @@ def run_ours(args, workload, rank, world, local):
     dev = torch.device("cuda", local)
     if args.sweep:
         run_sweep(args, dev)
+        return
+    if args.latency:
+        run_latency(args, dev)
         return
     if world > 1:
         import torch.distributed as dist

@@ -34,6 +34,13 @@
  *     no-op that returns SNK_OK.
  *   - A handle is used by one stream at a time; calls on one handle that
  *     overlap on the GPU race on its workspace.
+ *   - snk_forward, snk_backward_input and snk_backward_weight only enqueue
+ *     kernels (no allocation, no host synchronisation), and their kernels
+ *     leave the handle's scratch as they found it.  They may therefore be
+ *     captured into a CUDA graph (the inference-latency mode); a replay gives
+ *     the same bits as a direct call.  A graph stays valid across
+ *     snk_prune_regrow (nnz and the workspace addresses do not change) and
+ *     becomes invalid at snk_destroy.
  *   - Nothing crosses the ABI as an exception; every entry point returns a
  *     status code (snk_status_string gives its text).
  *   - Limits: 1 <= out, in <= 2^31 - 1; 0 <= nnz <= min(out*in, 2^31 - 1);

@@ -243,3 +243,17 @@ def test_full_size_10000(torch, sp, b):
 def test_full_size_5000(torch, sp):
     lay = synth.make_layer(5000, 5000, sp, 0.01, 11, 12)
     check_all_products(torch, lay, 2, bias=False, seed=13)
+
+
+@pytest.mark.parametrize("out_f,in_f,sp,b", [
+    (12500, 10000, 90, 1),   # [SNACK] Table 10 layer, batch 1
+    (12500, 10000, 99, 1),
+    (2500, 10000, 90, 2),    # [SNACK] Fig. 5 layer
+    (7500, 10000, 95, 4),    # [SNACK] Fig. 7 layer
+    (5000, 5000, 95, 1),     # [SNACK] Table 6 (GAMLP-shaped) layer, batch 1
+])
+def test_full_size_rectangular(torch, out_f, in_f, sp, b):
+    """The non-square layers of the pages' latency tables and figures, every
+    output element compared with the oracle."""
+    lay = synth.make_layer(out_f, in_f, sp, 0.01, 71, 72)
+    check_all_products(torch, lay, b, bias=True, seed=73)
