@@ -606,9 +606,18 @@ def run_ours(args, workload, rank, world, local):
             g.prune_regrow(0.3, 0x5E7 + i)
             torch.cuda.synchronize()
             ts.append((time.perf_counter() - t0) * 1e6)
+        tg = []
+        for i in range(3):
+            t0 = time.perf_counter()
+            g.prune_regrow_gradient(0.3, X, dY)
+            torch.cuda.synchronize()
+            tg.append((time.perf_counter() - t0) * 1e6)
         restructure = {"op": "prune_regrow", "zeta": 0.3,
                        "us_median_host_timed": statistics.median(ts),
-                       "note": "synchronous call (it reads device counts back); wall-clock µs"}
+                       "gradient_grow_us_median_host_timed": statistics.median(tg),
+                       "note": "synchronous calls (they read device counts back); wall-clock µs; "
+                               "the gradient variant ranks all out*in - kept candidates by the "
+                               "batch's |dY^T X|"}
 
     per_op_launch = {"fwd": launches_per_op(in_f, b, max_smem),
                      "dx": launches_per_op(out_f, b, max_smem),

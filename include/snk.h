@@ -10,7 +10,8 @@
  *                      (the weight gradient on supp(W) only: an SDDMM)
  *   prune_regrow       magnitude prune of a fraction zeta, then a seeded
  *                      uniform regrow of as many new zero-valued entries
- *                      (nnz unchanged)
+ *                      (nnz unchanged); prune_regrow_gradient grows at the
+ *                      largest-|gradient| positions instead
  * with hand-written CUDA kernels.  The caller owns every buffer it passes;
  * the library owns only the workspace behind the handle.
  *
@@ -160,6 +161,34 @@ int snk_backward_weight(snk_handle handle, const float* X, const float* dY, int6
  *   On every error the caller's arrays and the topology are left unchanged.
  */
 int snk_prune_regrow(snk_handle handle, float zeta, uint64_t seed, void* stream);
+
+/*
+ * snk_prune_regrow_gradient - one RigL-style restructure, nnz fixed: the same
+ * magnitude prune as snk_prune_regrow, then growth at the positions with the
+ * largest gradient magnitude instead of random ones.
+ *   [PCSR] sec. 4.3 (the typical dynamic-sparse-training update, e.g. RigL:
+ *   drop a fraction of the live entries, grow as many "at high-gradient
+ *   locations"); [SNACK] Tables 8-9 (RigL trained with the truly sparse
+ *   layer).  The pages fix no arithmetic or tie order; this library fixes:
+ *   Gradient of position (r, c): g = sum over beta of dY[beta, r] * X[beta, c],
+ *     evaluated in fp32 as the fused multiply-add chain
+ *     g = fma(dY[b-1,r], X[b-1,c], ... fma(dY[0,r], X[0,c], 0.0f)).
+ *   Candidates: every position not held by a kept entry (a position pruned in
+ *     this call is a candidate, as in snk_prune_regrow).
+ *   Grown: the k candidates with the largest bit pattern of |g| (NaN above
+ *     every number), ties going to the smaller r*in + c.  New values +0.0f.
+ *   The whole triple is then re-emitted in canonical order and the topology
+ *   rebuilt.  No out x in array is ever stored.
+ * X [batch, in], dY [batch, out]: the batch whose gradient ranks the
+ *   candidates (device, row-major fp32, 4-byte aligned); batch >= 1.
+ * zeta in [0, 1).  Limits: out * in <= 2^32.
+ * The call synchronises the stream (it reads device counts back).
+ * Errors: SNK_ERR_ARG, SNK_ERR_NOSPACE, SNK_ERR_LIMIT (out * in > 2^32),
+ *   SNK_ERR_OOM, SNK_ERR_CUDA.  On every error the caller's arrays and the
+ *   topology are left unchanged.
+ */
+int snk_prune_regrow_gradient(snk_handle handle, float zeta, const float* X, const float* dY,
+                              int64_t batch, void* stream);
 
 /*
  * snk_destroy - free the library-owned workspace (never the caller's arrays).

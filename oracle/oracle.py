@@ -18,6 +18,8 @@ import numpy as np
 __all__ = [
     "OracleError", "build", "canonicalize", "forward", "backward_input",
     "backward_weight", "prune_count", "prune", "regrow", "prune_regrow",
+    "grad_at", "grad_key", "grad_keys", "grow_gradient", "grad_count_below",
+    "prune_regrow_gradient",
     "splitmix64_nth", "mulhi64", "candidate", "regrow_limit",
     "ORC_OK", "ORC_ERR_ARG", "ORC_ERR_DUP", "ORC_ERR_RANGE", "ORC_ERR_OOM",
     "ORC_ERR_NOSPACE", "ORC_ERR_LIMIT",
@@ -77,6 +79,18 @@ def _load():
         lib.orc_regrow.restype = ctypes.c_int
         lib.orc_prune_regrow.argtypes = [i64, i64, i64, P, P, P, f32, u64]
         lib.orc_prune_regrow.restype = ctypes.c_int
+        lib.orc_grad_at.argtypes = [i64, i64, P, P, i64, i64, i64]
+        lib.orc_grad_at.restype = ctypes.c_float
+        lib.orc_grad_key.argtypes = [ctypes.c_float, u64]
+        lib.orc_grad_key.restype = u64
+        lib.orc_grad_keys.argtypes = [i64, i64, P, P, i64, P, i64, P]
+        lib.orc_grad_keys.restype = None
+        lib.orc_grow_gradient.argtypes = [i64, i64, i64, P, P, P, P, i64, i64, P]
+        lib.orc_grow_gradient.restype = ctypes.c_int
+        lib.orc_grad_count_below.argtypes = [i64, i64, i64, P, P, P, P, i64, u64]
+        lib.orc_grad_count_below.restype = i64
+        lib.orc_prune_regrow_gradient.argtypes = [i64, i64, i64, P, P, P, f32, P, P, i64]
+        lib.orc_prune_regrow_gradient.restype = ctypes.c_int
         lib.orc_splitmix64_nth.argtypes = [u64, u64]
         lib.orc_splitmix64_nth.restype = u64
         lib.orc_mulhi64.argtypes = [u64, u64]
@@ -199,6 +213,61 @@ def prune_regrow(out_f: int, in_f: int, v, r, c, zeta: float, seed: int):
                               float(np.float32(zeta)), ctypes.c_uint64(seed & (2**64 - 1)))
     if st != ORC_OK:
         raise OracleError(st, "prune_regrow")
+    return v, r, c
+
+
+def grad_at(out_f: int, in_f: int, X, dY, row: int, col: int) -> float:
+    """The fp32 gradient of position (row, col) as the fmaf chain over the batch."""
+    X, dY = _f32(X), _f32(dY)
+    return float(_load().orc_grad_at(out_f, in_f, _ptr(X), _ptr(dY), X.shape[0], row, col))
+
+
+def grad_key(g: float, lin: int) -> int:
+    return int(_load().orc_grad_key(ctypes.c_float(g), ctypes.c_uint64(lin)))
+
+
+def grad_keys(out_f: int, in_f: int, X, dY, lin) -> np.ndarray:
+    """Ranking keys (complement of bits(|g|) << 32 | position) of positions."""
+    X, dY = _f32(X), _f32(dY)
+    lin = np.ascontiguousarray(lin, np.int64)
+    keys = np.zeros(len(lin), np.uint64)
+    _load().orc_grad_keys(out_f, in_f, _ptr(X), _ptr(dY), X.shape[0], _ptr(lin), len(lin),
+                          _ptr(keys))
+    return keys
+
+
+def grow_gradient(out_f: int, in_f: int, r_kept, c_kept, X, dY, k: int):
+    """The k candidate positions with the largest |gradient| (ties: smaller
+    position), ascending."""
+    lib = _load()
+    r_kept, c_kept, X, dY = _i32(r_kept), _i32(c_kept), _f32(X), _f32(dY)
+    new_lin = np.zeros(max(k, 1), np.int64)[:k]
+    st = lib.orc_grow_gradient(out_f, in_f, r_kept.shape[0], _ptr(r_kept), _ptr(c_kept),
+                               _ptr(X), _ptr(dY), X.shape[0], k, _ptr(new_lin))
+    if st != ORC_OK:
+        raise OracleError(st, "grow_gradient")
+    return new_lin
+
+
+def grad_count_below(out_f: int, in_f: int, r_kept, c_kept, X, dY, theta: int) -> int:
+    lib = _load()
+    r_kept, c_kept, X, dY = _i32(r_kept), _i32(c_kept), _f32(X), _f32(dY)
+    n = lib.orc_grad_count_below(out_f, in_f, r_kept.shape[0], _ptr(r_kept), _ptr(c_kept),
+                                 _ptr(X), _ptr(dY), X.shape[0], ctypes.c_uint64(theta))
+    if n < 0:
+        raise OracleError(ORC_ERR_OOM, "grad_count_below")
+    return int(n)
+
+
+def prune_regrow_gradient(out_f: int, in_f: int, v, r, c, zeta: float, X, dY):
+    """Prune + gradient grow + canonical re-emission; returns new (v, r, c)."""
+    lib = _load()
+    v, r, c = _f32(v).copy(), _i32(r).copy(), _i32(c).copy()
+    X, dY = _f32(X), _f32(dY)
+    st = lib.orc_prune_regrow_gradient(out_f, in_f, v.shape[0], _ptr(v), _ptr(r), _ptr(c),
+                                       ctypes.c_float(zeta), _ptr(X), _ptr(dY), X.shape[0])
+    if st != ORC_OK:
+        raise OracleError(st, "prune_regrow_gradient")
     return v, r, c
 
 

@@ -31,6 +31,12 @@
  * Procedural parts (canonical order, prune, regrow) follow the steps in the
  * order the pages give them; where the pages leave a step open the plainest
  * reading is taken and named at the function.
+ *
+ * The gradient grow ([PCSR] sec. 4.3, RigL: grow "at high-gradient
+ * locations") ranks positions by an fp32 value, so here, where floating point
+ * decides which integers are chosen, the oracle takes the decision in the
+ * same precision as the library: each gradient is the fp32 fused
+ * multiply-add chain over the batch in order (C99 fmaf, correctly rounded).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -376,6 +382,93 @@ int orc_regrow(int64_t out_f, int64_t in_f, int64_t n_kept,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gradient grow (RigL, [PCSR] sec. 4.3: "grow ... new entries at            */
+/* high-gradient locations").  The gradient of the loss with respect to the   */
+/* weight at (r, c) is sum_beta dY[beta, r] * X[beta, c] ([PCSR] sec. 7.1,    */
+/* evaluated at every position instead of only the live ones).  It is taken   */
+/* as the fp32 chain g = fmaf(dY[b-1,r], X[b-1,c], ... fmaf(dY[0,r], X[0,c],  */
+/* 0)).  Readings: the candidates are the positions held by no kept entry;    */
+/* larger bits(|g|) first (NaN above every number), ties to the smaller       */
+/* position.  new_lin receives the k chosen positions in ascending order.     */
+/* ------------------------------------------------------------------------ */
+float orc_grad_at(int64_t out_f, int64_t in_f, const float* X, const float* dY, int64_t b,
+                  int64_t row, int64_t col) {
+    float g = 0.0f;
+    for (int64_t beta = 0; beta < b; ++beta)
+        g = fmaf(dY[beta * out_f + row], X[beta * in_f + col], g);
+    return g;
+}
+
+/* The ranking key: ascending key = descending bits(|g|), then ascending lin. */
+uint64_t orc_grad_key(float g, uint64_t lin) {
+    return ((uint64_t)(~orc_abs_bits(g)) << 32) | (lin & 0xffffffffull);
+}
+
+static int orc_cmp_u64(const void* a, const void* b) {
+    uint64_t x = *(const uint64_t*)a, y = *(const uint64_t*)b;
+    return (x > y) - (x < y);
+}
+
+int orc_grow_gradient(int64_t out_f, int64_t in_f, int64_t n_kept, const int32_t* r_kept,
+                      const int32_t* c_kept, const float* X, const float* dY, int64_t b,
+                      int64_t k, int64_t* new_lin) {
+    uint64_t n_pos = (uint64_t)out_f * (uint64_t)in_f;
+    if (n_pos > (1ull << 32)) return ORC_ERR_LIMIT;
+    if ((uint64_t)n_kept + (uint64_t)k > n_pos) return ORC_ERR_NOSPACE;
+    uint8_t* held = (uint8_t*)calloc((size_t)n_pos, 1);
+    uint64_t* keys = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(n_pos - (uint64_t)n_kept + 1));
+    if (!held || !keys) {
+        free(held);
+        free(keys);
+        return ORC_ERR_OOM;
+    }
+    for (int64_t i = 0; i < n_kept; ++i)
+        held[(uint64_t)r_kept[i] * (uint64_t)in_f + (uint64_t)c_kept[i]] = 1;
+    size_t n_cand = 0;
+    for (uint64_t p = 0; p < n_pos; ++p) {
+        if (held[p]) continue;
+        int64_t row = (int64_t)(p / (uint64_t)in_f), col = (int64_t)(p % (uint64_t)in_f);
+        keys[n_cand++] = orc_grad_key(orc_grad_at(out_f, in_f, X, dY, b, row, col), p);
+    }
+    qsort(keys, n_cand, sizeof(uint64_t), orc_cmp_u64);
+    for (int64_t j = 0; j < k; ++j) new_lin[j] = (int64_t)(keys[j] & 0xffffffffull);
+    qsort(new_lin, (size_t)k, sizeof(int64_t), orc_cmp_u64);
+    free(held);
+    free(keys);
+    return ORC_OK;
+}
+
+/* The ranking keys of the given positions. */
+void orc_grad_keys(int64_t out_f, int64_t in_f, const float* X, const float* dY, int64_t b,
+                   const int64_t* lin, int64_t n, uint64_t* keys) {
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t row = lin[i] / in_f, col = lin[i] % in_f;
+        keys[i] = orc_grad_key(orc_grad_at(out_f, in_f, X, dY, b, row, col), (uint64_t)lin[i]);
+    }
+}
+
+/* Number of candidates (positions not held by the kept set) whose key is
+ * below `theta`: the exact rank of a key among all candidates, for checking
+ * a selection on layers too large to sort. */
+int64_t orc_grad_count_below(int64_t out_f, int64_t in_f, int64_t n_kept, const int32_t* r_kept,
+                             const int32_t* c_kept, const float* X, const float* dY, int64_t b,
+                             uint64_t theta) {
+    uint64_t n_pos = (uint64_t)out_f * (uint64_t)in_f;
+    uint8_t* held = (uint8_t*)calloc((size_t)n_pos, 1);
+    if (!held) return -1;
+    for (int64_t i = 0; i < n_kept; ++i)
+        held[(uint64_t)r_kept[i] * (uint64_t)in_f + (uint64_t)c_kept[i]] = 1;
+    int64_t below = 0;
+    for (uint64_t p = 0; p < n_pos; ++p) {
+        if (held[p]) continue;
+        int64_t row = (int64_t)(p / (uint64_t)in_f), col = (int64_t)(p % (uint64_t)in_f);
+        below += orc_grad_key(orc_grad_at(out_f, in_f, X, dY, b, row, col), p) < theta;
+    }
+    free(held);
+    return below;
+}
+
+/* ------------------------------------------------------------------------ */
 /* S5 + S6 together, in place, nnz unchanged: prune k, regrow k at value     */
 /* +0.0f, then re-emit the whole triple in canonical order.  On any error    */
 /* the arrays are left as they were.                                         */
@@ -410,6 +503,59 @@ int orc_prune_regrow(int64_t out_f, int64_t in_f, int64_t nnz,
         ++m;
     }
     rc = orc_regrow(out_f, in_f, m, r2, c2, k, seed, grown, NULL);
+    if (rc != ORC_OK) goto done;
+    for (int64_t j = 0; j < k; ++j) {
+        v2[m + j] = 0.0f;
+        r2[m + j] = (int32_t)((uint64_t)grown[j] / (uint64_t)in_f);
+        c2[m + j] = (int32_t)((uint64_t)grown[j] % (uint64_t)in_f);
+    }
+    rc = orc_canonicalize(out_f, in_f, nnz, v2, r2, c2, NULL, NULL, NULL, NULL);
+    if (rc != ORC_OK) goto done;
+    memcpy(v, v2, sizeof(float) * n);
+    memcpy(r, r2, sizeof(int32_t) * n);
+    memcpy(c, c2, sizeof(int32_t) * n);
+done:
+    free(removed);
+    free(v2);
+    free(r2);
+    free(c2);
+    free(grown);
+    return rc;
+}
+
+/* The RigL restructure: the same prune as orc_prune_regrow, then the
+ * gradient grow instead of the seeded one, then canonical re-emission. */
+int orc_prune_regrow_gradient(int64_t out_f, int64_t in_f, int64_t nnz,
+                              float* v, int32_t* r, int32_t* c, float zeta,
+                              const float* X, const float* dY, int64_t b) {
+    if (out_f <= 0 || in_f <= 0 || nnz < 0 || b < 1) return ORC_ERR_ARG;
+    if (!(zeta >= 0.0f && zeta < 1.0f)) return ORC_ERR_ARG;
+    int64_t k = orc_prune_count(zeta, nnz);
+    uint64_t n_pos = (uint64_t)out_f * (uint64_t)in_f;
+    if (n_pos > (1ull << 32)) return ORC_ERR_LIMIT;
+    if (n_pos - (uint64_t)(nnz - k) < (uint64_t)k) return ORC_ERR_NOSPACE;
+    if (k == 0) return ORC_OK;
+
+    size_t n = (size_t)nnz;
+    uint8_t* removed = (uint8_t*)malloc(n);
+    float* v2 = (float*)malloc(sizeof(float) * n);
+    int32_t* r2 = (int32_t*)malloc(sizeof(int32_t) * n);
+    int32_t* c2 = (int32_t*)malloc(sizeof(int32_t) * n);
+    int64_t* grown = (int64_t*)malloc(sizeof(int64_t) * (size_t)k);
+    int rc = ORC_ERR_OOM;
+    if (!removed || !v2 || !r2 || !c2 || !grown) goto done;
+
+    rc = orc_prune(out_f, in_f, nnz, v, r, c, zeta, removed, NULL);
+    if (rc != ORC_OK) goto done;
+    int64_t m = 0;
+    for (int64_t i = 0; i < nnz; ++i) {
+        if (removed[i]) continue;
+        v2[m] = v[i];
+        r2[m] = r[i];
+        c2[m] = c[i];
+        ++m;
+    }
+    rc = orc_grow_gradient(out_f, in_f, m, r2, c2, X, dY, b, k, grown);
     if (rc != ORC_OK) goto done;
     for (int64_t j = 0; j < k; ++j) {
         v2[m + j] = 0.0f;

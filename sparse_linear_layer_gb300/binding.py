@@ -47,6 +47,7 @@ def lib():
         L.snk_backward_input.argtypes = [P, P, i64, P, P]
         L.snk_backward_weight.argtypes = [P, P, P, i64, P, P, P]
         L.snk_prune_regrow.argtypes = [P, f32, u64, P]
+        L.snk_prune_regrow_gradient.argtypes = [P, f32, P, P, i64, P]
         L.snk_destroy.argtypes = [P]
         L.snk_status_string.argtypes = [I]
         L.snk_status_string.restype = ctypes.c_char_p
@@ -55,8 +56,8 @@ def lib():
         L.snk_copy_topology.argtypes = [P, P, P, P, P, P]
         L.snk_forward_csr_noalloc.argtypes = [i64, i64, i64, P, P, P, P, i64, P, P, P]
         for name in ("snk_create", "snk_forward", "snk_backward_input", "snk_backward_weight",
-                     "snk_prune_regrow", "snk_destroy", "snk_get_shape", "snk_copy_topology",
-                     "snk_forward_csr_noalloc"):
+                     "snk_prune_regrow", "snk_prune_regrow_gradient", "snk_destroy",
+                     "snk_get_shape", "snk_copy_topology", "snk_forward_csr_noalloc"):
             getattr(L, name).restype = I
         _lib = L
         return L
@@ -129,6 +130,13 @@ def snk_prune_regrow(handle: int, zeta: float, seed: int, stream=None):
            "snk_prune_regrow")
 
 
+def snk_prune_regrow_gradient(handle: int, zeta: float, X, dY, stream=None,
+                              batch: int | None = None):
+    b = X.shape[0] if batch is None else batch
+    _check(lib().snk_prune_regrow_gradient(handle, float(zeta), _ptr(X), _ptr(dY), b,
+                                           _stream(stream)), "snk_prune_regrow_gradient")
+
+
 def snk_destroy(handle: int):
     _check(lib().snk_destroy(handle), "snk_destroy")
 
@@ -197,6 +205,9 @@ class SparseLinear:
 
     def prune_regrow(self, zeta: float, seed: int, stream=None):
         snk_prune_regrow(self.handle, zeta, seed, stream)
+
+    def prune_regrow_gradient(self, zeta: float, X, dY, stream=None):
+        snk_prune_regrow_gradient(self.handle, zeta, X, dY, stream)
 
     def topology(self):
         import torch

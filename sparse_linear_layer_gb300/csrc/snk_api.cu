@@ -173,6 +173,16 @@ int snk_prune_regrow(snk_handle h, float zeta, uint64_t seed, void* stream) {
     return run_prune_regrow(L, zeta, seed, (cudaStream_t)stream);
 }
 
+int snk_prune_regrow_gradient(snk_handle h, float zeta, const float* X, const float* dY,
+                              int64_t batch, void* stream) {
+    Layer* L = reinterpret_cast<Layer*>(h);
+    if (!L || batch < 1 || !X || !dY || !aligned(X, 4) || !aligned(dY, 4)) return SNK_ERR_ARG;
+    if (!(zeta >= 0.0f && zeta < 1.0f)) return SNK_ERR_ARG;
+    if (batch > INT32_MAX) return SNK_ERR_ARG;
+    if (fault("launch")) return SNK_ERR_CUDA;
+    return run_prune_regrow_gradient(L, zeta, X, dY, batch, (cudaStream_t)stream);
+}
+
 int snk_destroy(snk_handle h) {
     Layer* L = reinterpret_cast<Layer*>(h);
     if (!L) return SNK_OK;

@@ -137,6 +137,8 @@ int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaS
 int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b, float* dW,
                            float* db, cudaStream_t s);
 int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s);
+int run_prune_regrow_gradient(Layer* L, float zeta, const float* X, const float* dY, int64_t b,
+                              cudaStream_t s);
 // Partition nnz entries with segment pointer ptr[n_seg+1] over n_blocks
 // blocks of kWarpsPerBlock chunks (block boundaries on segment boundaries
 // except inside segments longer than half a block's share).

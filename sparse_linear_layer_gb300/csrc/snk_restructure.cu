@@ -31,6 +31,15 @@
 //    by t with a scan and the first `need` are accepted.  This picks exactly
 //    the positions the sequential definition picks, in the same order, for
 //    any B.
+//  * Gradient grow (the RigL variant, "grow at high-gradient locations",
+//    sec. 4.3 of the Padded-CSR page): the gradient of every candidate
+//    position is recomputed on the fly in each pass (one warp per row, the
+//    row's kept columns marked in a shared-memory bitmap per 1024-column
+//    tile) and never stored; an MSB-first radix select with 12-bit digits
+//    over the 64-bit key (complement of the bits of |g|, then the position)
+//    finds the k-th smallest key, stopping early when a digit bin holds
+//    exactly the remaining count; a last pass collects every candidate at or
+//    below it: exactly k positions, since keys are unique.
 //  * The kept and grown entries are written back into the caller's triple
 //    and the topology build re-sorts it.
 #include <algorithm>
@@ -41,6 +50,10 @@ namespace snk {
 
 constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
 constexpr uint64_t kEmpty = ~0ull;
+constexpr int kGradTile = 1024;            // columns per bitmap tile
+constexpr int kGradDigit = 12;             // digit width of the select passes
+constexpr int kGradBins = 1 << kGradDigit;
+constexpr int kGradWarps = 8;              // warps per block of the gradient passes
 
 struct SelState {
     uint32_t mag;
@@ -70,6 +83,11 @@ struct RestructureWs {
     int64_t cand_cap = 0;
     uint64_t* new_lin = nullptr;
     int32_t* err = nullptr;
+    // gradient grow
+    int32_t* ghist = nullptr;    // [kGradBins]
+    void* gsel = nullptr;        // GradSel
+    int32_t* kept_ptr = nullptr; // [kept_ptr_len] kept entries per row
+    int64_t kept_ptr_len = 0;
 };
 
 static uint64_t next_pow2(uint64_t x) {
@@ -82,7 +100,8 @@ void free_restructure(Layer* L) {
     RestructureWs* w = L->rws;
     if (!w) return;
     void* ptrs[] = {w->hist, w->sel, w->flags, w->scan_tmp, w->total, w->acc, w->kept_lin,
-                    w->kept_val, w->H, w->R_key, w->R_t, w->cand, w->new_lin, w->err};
+                    w->kept_val, w->H, w->R_key, w->R_t, w->cand, w->new_lin, w->err,
+                    w->ghist, w->gsel, w->kept_ptr};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete w;
@@ -340,6 +359,145 @@ __global__ void k_assemble(const uint64_t* __restrict__ kept_lin, const uint32_t
     }
 }
 
+// ---------------------------------------------------------------- gradient grow kernels
+struct GradSel {
+    uint64_t prefix;  // the selected high bits of the k-th smallest key
+    int32_t level;    // how many high key bits are fixed
+    int32_t exact;    // 1 when the selected bin holds exactly the remaining rank
+    int64_t krem;     // rank still to find among keys with that prefix
+};
+
+__global__ void k_grad_init(GradSel* sel, int64_t k) {
+    sel->prefix = 0;
+    sel->level = 0;
+    sel->exact = 0;
+    sel->krem = k;
+}
+
+// kept_ptr[j] = number of kept entries in rows < j, for j in [0, out]
+__global__ void k_kept_row_ptr(const uint64_t* __restrict__ kept, int64_t m, int64_t in_f,
+                               int64_t out_f, int32_t* __restrict__ ptr) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i <= m;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t prev = i == 0 ? -1 : (int64_t)(kept[i - 1] / (uint64_t)in_f);
+        const int64_t cur = i == m ? out_f : (int64_t)(kept[i] / (uint64_t)in_f);
+        for (int64_t j = prev + 1; j <= cur; ++j) ptr[j] = (int32_t)i;
+    }
+}
+
+// The gradient of position (r, c): the fused multiply-add chain over the
+// batch in order, g = fma(dY[b-1,r], X[b-1,c], ... fma(dY[0,r], X[0,c], 0)).
+// Key: complement of the bit pattern of |g| (high 32 bits), then the position.
+__device__ __forceinline__ uint64_t grad_key(const float* __restrict__ X,
+                                             const float* __restrict__ dY, int b, int64_t out_f,
+                                             int64_t in_f, int64_t r, int64_t c, uint32_t p) {
+    float g = 0.f;
+    for (int beta = 0; beta < b; ++beta)
+        g = __fmaf_rn(__ldg(dY + beta * out_f + r), __ldg(X + beta * in_f + c), g);
+    const uint32_t a = __float_as_uint(g) & 0x7fffffffu;
+    return ((uint64_t)(~a) << 32) | (uint64_t)p;
+}
+
+// One pass over every candidate (a position held by no kept entry).  One
+// warp per row; per 1024-column tile the row's kept columns are marked in a
+// shared-memory bitmap, then lane l evaluates columns l, l+32, ...
+//   COLLECT = false: histogram of the digit [shift, shift+width) of the keys
+//     whose top `level` bits equal the selected prefix.
+//   COLLECT = true: every key whose top `level` bits are <= the prefix is
+//     selected; its position is appended to out_lin (at most cap).
+template <bool COLLECT>
+__global__ void __launch_bounds__(kGradWarps * 32) k_grad_pass(
+    const uint64_t* __restrict__ kept, const int32_t* __restrict__ kept_ptr, int64_t out_f,
+    int64_t in_f, const float* __restrict__ X, const float* __restrict__ dY, int b,
+    const GradSel* __restrict__ sel, int shift, int width, int32_t* __restrict__ hist,
+    uint64_t* __restrict__ out_lin, int64_t* __restrict__ n_out, int64_t cap, int32_t* err) {
+    __shared__ int h[COLLECT ? 1 : kGradBins];
+    __shared__ uint32_t bm[kGradWarps][kGradTile / 32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (!COLLECT) {
+        for (int i = threadIdx.x; i < (1 << width); i += blockDim.x) h[i] = 0;
+        __syncthreads();
+    }
+    const uint64_t prefix = sel->prefix;
+    const int level = sel->level;
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int64_t r = (int64_t)blockIdx.x * kGradWarps + w; r < out_f;
+         r += (int64_t)gridDim.x * kGradWarps) {
+        int64_t j = kept_ptr[r];
+        const int64_t j_end = kept_ptr[r + 1];
+        const uint64_t row0 = (uint64_t)r * (uint64_t)in_f;
+        for (int64_t c0 = 0; c0 < in_f; c0 += kGradTile) {
+            const int64_t c1 = min(in_f, c0 + (int64_t)kGradTile);
+            bm[w][lane] = 0u;
+            __syncwarp();
+            // mark the kept columns of [c0, c1): they are kept[j ..] while < row0 + c1
+            while (j < j_end) {
+                const int64_t jj = j + lane;
+                const bool in_tile = jj < j_end && kept[jj] < row0 + (uint64_t)c1;
+                if (in_tile) {
+                    const uint32_t cc = (uint32_t)(kept[jj] - row0 - (uint64_t)c0);
+                    atomicOr(&bm[w][cc >> 5], 1u << (cc & 31u));
+                }
+                const unsigned took = __ballot_sync(0xffffffffu, in_tile);
+                j += __popc(took);
+                if (took != 0xffffffffu) break;
+            }
+            __syncwarp();
+            for (int t = 0; t < kGradTile / 32; ++t) {
+                const int64_t c = c0 + t * 32 + lane;
+                if (c >= c1) break;
+                if ((bm[w][t] >> lane) & 1u) continue;
+                const uint64_t key = grad_key(X, dY, b, out_f, in_f, r, c, (uint32_t)(row0 + (uint64_t)c));
+                if (!COLLECT) {
+                    if (level == 0 || (key >> (64 - level)) == prefix)
+                        atomicAdd(&h[(uint32_t)(key >> shift) & dmask], 1);
+                } else if ((key >> (64 - level)) <= prefix) {
+                    const unsigned long long i = atomicAdd(reinterpret_cast<unsigned long long*>(n_out), 1ull);
+                    if ((int64_t)i < cap) out_lin[i] = row0 + (uint64_t)c;
+                    else atomicOr(err, kStatLimit);
+                }
+            }
+            __syncwarp();
+        }
+    }
+    if (!COLLECT) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < (1 << width); i += blockDim.x)
+            if (h[i]) atomicAdd(&hist[i], h[i]);
+    }
+}
+
+// Pick the digit bin holding the krem-th smallest key; one warp.
+__global__ void k_grad_pick(const int32_t* __restrict__ hist, int width, GradSel* sel) {
+    const int lane = threadIdx.x;
+    const int nb = 1 << width;
+    const int per = (nb + 31) / 32;
+    const int lo = min(nb, lane * per), hi = min(nb, lo + per);
+    int64_t mine = 0;
+    for (int d = lo; d < hi; ++d) mine += hist[d];
+    int64_t incl = mine;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int64_t krem = sel->krem;
+    const int64_t excl = incl - mine;
+    if (excl < krem && krem <= incl) {
+        int64_t cum = excl;
+        for (int d = lo; d < hi; ++d) {
+            if (cum + hist[d] >= krem) {
+                const int64_t left = krem - cum;
+                sel->prefix = (sel->prefix << width) | (uint64_t)d;
+                sel->level += width;
+                sel->krem = left;
+                sel->exact = (hist[d] == left) ? 1 : 0;
+                return;
+            }
+            cum += hist[d];
+        }
+    }
+}
+
 static int bits_for(uint64_t n_values) {
     int b = 0;
     while (b < 64 && (n_values - 1) >> b) ++b;
@@ -350,20 +508,13 @@ static unsigned grid_of(int64_t n, int num_sms) {
     return (unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, 256), (int64_t)num_sms * 8));
 }
 
-int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s) {
-    if (!(zeta >= 0.0f && zeta < 1.0f)) return SNK_ERR_ARG;
-    const int64_t n = L->nnz;
-    const int64_t k = (int64_t)((double)zeta * (double)n);  // floor for non-negative values
-    const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
-    if (n_pos - (uint64_t)(n - k) < (uint64_t)k) return SNK_ERR_NOSPACE;
-    if (k == 0) return SNK_OK;
-    int st = alloc_restructure(L);
-    if (st != SNK_OK) return st;
+// Prune step: the k smallest (|v| bits, lin) are removed; the kept entries
+// are compacted, in canonical order, into kept_lin / kept_val.
+static int prune_step(Layer* L, int64_t k, cudaStream_t s) {
     RestructureWs* w = L->rws;
+    const int64_t n = L->nnz;
+    const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
     const unsigned G = grid_of(n, L->num_sms);
-    cudaMemsetAsync(w->err, 0, sizeof(int32_t), s);
-
-    // ---- prune: radix select of the k-th smallest (|v| bits, lin)
     k_sel_init<<<1, 1, 0, s>>>(w->sel, k);
     for (int shift = 24; shift >= 0; shift -= 8) {
         cudaMemsetAsync(w->hist, 0, 256 * sizeof(int32_t), s);
@@ -378,13 +529,18 @@ int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s) {
     }
     k_keep_flags<<<G, 256, 0, s>>>(L->v, L->r, L->c, n, L->in_f, w->sel, w->flags);
     int32_t* pos = w->flags + w->flag_half;
-    st = exclusive_scan_i32(w->flags, pos, n, w->scan_tmp, w->scan_tmp_len, w->total, s);
+    int st = exclusive_scan_i32(w->flags, pos, n, w->scan_tmp, w->scan_tmp_len, w->total, s);
     if (st != SNK_OK) return st;
     k_compact<<<G, 256, 0, s>>>(L->v, L->r, L->c, n, L->in_f, w->flags, pos, w->kept_lin,
                                 w->kept_val);
-    const int64_t m = n - k;
+    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+}
 
-    // ---- regrow
+// Uniform grow: k seeded draws accepted in draw order into new_lin.
+static int grow_uniform(Layer* L, int64_t k, uint64_t seed, cudaStream_t s) {
+    RestructureWs* w = L->rws;
+    const int64_t m = L->nnz - k;
+    const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
     cudaMemsetAsync(w->H, 0xFF, (w->H_mask + 1) * sizeof(uint64_t), s);
     k_set_fill<<<grid_of(m, L->num_sms), 256, 0, s>>>(w->H, w->H_mask, w->kept_lin, m, w->err);
     cudaMemsetAsync(w->acc, 0, sizeof(int64_t), s);
@@ -403,7 +559,7 @@ int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s) {
         k_draw<<<GB, 256, 0, s>>>(seed, t0, B, n_pos, w->H, w->H_mask, w->R_key, w->R_t, w->R_mask,
                                   w->cand, w->err);
         k_first_flags<<<GB, 256, 0, s>>>(w->cand, B, t0, w->R_key, w->R_t, w->R_mask, surv);
-        st = exclusive_scan_i32(surv, rank, B, w->scan_tmp, w->scan_tmp_len, w->total, s);
+        int st = exclusive_scan_i32(surv, rank, B, w->scan_tmp, w->scan_tmp_len, w->total, s);
         if (st != SNK_OK) return st;
         k_take<<<GB, 256, 0, s>>>(w->cand, surv, rank, B, w->acc, k, w->new_lin, w->H, w->H_mask,
                                   w->err);
@@ -421,12 +577,100 @@ int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s) {
         return SNK_ERR_CUDA;
     if (h_err) return SNK_ERR_LIMIT;
     if (accepted < k) return SNK_ERR_LIMIT;
+    return SNK_OK;
+}
 
-    // ---- write back and rebuild
-    k_assemble<<<G, 256, 0, s>>>(w->kept_lin, w->kept_val, m, w->new_lin, k, L->in_f, L->v, L->r,
-                                 L->c);
+// Gradient grow: the k candidates with the smallest gradient keys into new_lin.
+static int grow_gradient(Layer* L, int64_t k, const float* X, const float* dY, int64_t b,
+                         cudaStream_t s) {
+    RestructureWs* w = L->rws;
+    const int64_t m = L->nnz - k;
+    if (!w->ghist) {
+        w->kept_ptr_len = L->out_f + 1;
+        if (cudaMalloc(&w->ghist, kGradBins * sizeof(int32_t)) != cudaSuccess ||
+            cudaMalloc(&w->gsel, sizeof(GradSel)) != cudaSuccess ||
+            cudaMalloc(&w->kept_ptr, w->kept_ptr_len * sizeof(int32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return SNK_ERR_OOM;
+        }
+    }
+    GradSel* sel = static_cast<GradSel*>(w->gsel);
+    k_kept_row_ptr<<<grid_of(m + 1, L->num_sms), 256, 0, s>>>(w->kept_lin, m, L->in_f, L->out_f,
+                                                              w->kept_ptr);
+    k_grad_init<<<1, 1, 0, s>>>(sel, k);
+    const unsigned G = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>(ceil_div(L->out_f, kGradWarps), (int64_t)L->num_sms * 4));
+    GradSel h{};
+    for (int level = 0; level < 64;) {
+        const int width = std::min(kGradDigit, 64 - level);
+        const int shift = 64 - level - width;
+        cudaMemsetAsync(w->ghist, 0, (size_t)(1 << width) * sizeof(int32_t), s);
+        k_grad_pass<false><<<G, kGradWarps * 32, 0, s>>>(w->kept_lin, w->kept_ptr, L->out_f,
+                                                        L->in_f, X, dY, (int)b, sel, shift, width,
+                                                        w->ghist, nullptr, nullptr, 0, w->err);
+        k_grad_pick<<<1, 32, 0, s>>>(w->ghist, width, sel);
+        if (cudaMemcpyAsync(&h, sel, sizeof(GradSel), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return SNK_ERR_CUDA;
+        if (h.level != level + width) return SNK_ERR_CUDA;  // rank not found: cannot happen
+        level = h.level;
+        if (h.exact) break;
+    }
+    cudaMemsetAsync(w->acc, 0, sizeof(int64_t), s);
+    k_grad_pass<true><<<G, kGradWarps * 32, 0, s>>>(w->kept_lin, w->kept_ptr, L->out_f, L->in_f,
+                                                   X, dY, (int)b, sel, 0, 1, nullptr, w->new_lin,
+                                                   w->acc, k, w->err);
+    int64_t got = 0;
+    int32_t h_err = 0;
+    if (cudaMemcpyAsync(&got, w->acc, sizeof(int64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(&h_err, w->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SNK_ERR_CUDA;
+    if (h_err || got != k) return SNK_ERR_CUDA;  // keys are unique: exactly k are selected
+    return SNK_OK;
+}
+
+static int assemble(Layer* L, int64_t k, cudaStream_t s) {
+    RestructureWs* w = L->rws;
+    const int64_t m = L->nnz - k;
+    k_assemble<<<grid_of(L->nnz, L->num_sms), 256, 0, s>>>(w->kept_lin, w->kept_val, m,
+                                                           w->new_lin, k, L->in_f, L->v, L->r,
+                                                           L->c);
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     return build_topology(L, s, false);
+}
+
+int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s) {
+    if (!(zeta >= 0.0f && zeta < 1.0f)) return SNK_ERR_ARG;
+    const int64_t n = L->nnz;
+    const int64_t k = (int64_t)((double)zeta * (double)n);  // floor for non-negative values
+    const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
+    if (n_pos - (uint64_t)(n - k) < (uint64_t)k) return SNK_ERR_NOSPACE;
+    if (k == 0) return SNK_OK;
+    int st = alloc_restructure(L);
+    if (st != SNK_OK) return st;
+    cudaMemsetAsync(L->rws->err, 0, sizeof(int32_t), s);
+    if ((st = prune_step(L, k, s)) != SNK_OK) return st;
+    if ((st = grow_uniform(L, k, seed, s)) != SNK_OK) return st;
+    return assemble(L, k, s);
+}
+
+int run_prune_regrow_gradient(Layer* L, float zeta, const float* X, const float* dY, int64_t b,
+                              cudaStream_t s) {
+    if (!(zeta >= 0.0f && zeta < 1.0f)) return SNK_ERR_ARG;
+    const int64_t n = L->nnz;
+    const int64_t k = (int64_t)((double)zeta * (double)n);
+    const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
+    if (n_pos > (1ull << 32)) return SNK_ERR_LIMIT;
+    if (n_pos - (uint64_t)(n - k) < (uint64_t)k) return SNK_ERR_NOSPACE;
+    if (k == 0) return SNK_OK;
+    int st = alloc_restructure(L);
+    if (st != SNK_OK) return st;
+    cudaMemsetAsync(L->rws->err, 0, sizeof(int32_t), s);
+    if ((st = prune_step(L, k, s)) != SNK_OK) return st;
+    if ((st = grow_gradient(L, k, X, dY, b, s)) != SNK_OK) return st;
+    return assemble(L, k, s);
 }
 
 }  // namespace snk

@@ -177,3 +177,134 @@ def test_full_size_restructure(torch):
     g = make_gpu_layer(torch, lay)
     restructure_and_compare(torch, g, 10_000, 10_000, 0.3, 0x5E7 + 1)
     g.close()
+
+
+# ---------------------------------------------------------------- gradient grow (RigL)
+
+def gradient_restructure_and_compare(torch, g, out_f, in_f, zeta, X, dY):
+    v0, r0, c0 = host(g.values), host(g.rows), host(g.cols)
+    ver = g.topology_version
+    g.prune_regrow_gradient(zeta, dev(X, torch), dev(dY, torch))
+    ve, re_, ce = oracle.prune_regrow_gradient(out_f, in_f, v0, r0, c0, zeta, X, dY)
+    np.testing.assert_array_equal(host(g.rows), re_)
+    np.testing.assert_array_equal(host(g.cols), ce)
+    np.testing.assert_array_equal(host(g.values).view(np.uint32), ve.view(np.uint32))
+    k = oracle.prune_count(zeta, len(v0))
+    assert g.topology_version == ver + (1 if k > 0 else 0)
+    t = g.topology()
+    can = oracle.canonicalize(out_f, in_f, ve, re_, ce)
+    for key in ("row_ptr", "col_ptr", "rows_c", "perm"):
+        np.testing.assert_array_equal(host(t[key]), can[key], err_msg=key)
+
+
+@pytest.mark.parametrize("out_f,in_f,sp,zeta,b,zipf", [
+    (16, 16, 50, 0.3, 1, None),
+    (500, 500, 95, 0.3, 4, None),
+    (129, 77, 90, 0.5, 3, None),
+    (1000, 700, 90, 0.3, 16, None),
+    (768, 3072, 90, 0.3, 4, 1.2),     # GPT-2 MLP shape, Zipf rows
+    (3072, 768, 99, 0.5, 2, 1.2),
+    (10, 10, 10, 0.9, 2, None),       # nearly full: the whole complement is grown
+])
+def test_prune_regrow_gradient_bit_exact(torch, out_f, in_f, sp, zeta, b, zipf):
+    lay = synth.make_layer(out_f, in_f, sp, 0.05, 5, 6, zipf_s=zipf)
+    X = synth.normal((b, in_f), 1.0, 7)
+    dY = synth.normal((b, out_f), 1.0, 8)
+    g = make_gpu_layer(torch, lay)
+    gradient_restructure_and_compare(torch, g, out_f, in_f, zeta, X, dY)
+    g.close()
+
+
+def test_prune_regrow_gradient_massive_ties(torch):
+    """Most gradients are exactly zero (X is zero outside 3 columns) and many
+    others repeat: the selection has to go down to the position bits."""
+    out_f, in_f, b = 300, 200, 2
+    lay = synth.make_layer(out_f, in_f, 90, 0.05, 11, 12)
+    X = np.zeros((b, in_f), np.float32)
+    X[:, [3, 77, 150]] = np.array([[1.0, -2.0, 0.5], [0.25, 1.0, -0.5]], np.float32)
+    dY = np.ones((b, out_f), np.float32)
+    dY[:, ::3] = -1.0
+    g = make_gpu_layer(torch, lay)
+    for i in range(2):
+        gradient_restructure_and_compare(torch, g, out_f, in_f, 0.3, X, dY)
+    g.close()
+
+
+def test_prune_regrow_gradient_nan_and_errors(torch):
+    out_f, in_f = 40, 50
+    lay = synth.make_layer(out_f, in_f, 80, 0.05, 13, 14)
+    g = make_gpu_layer(torch, lay)
+    X = synth.normal((2, in_f), 1.0, 15)
+    X[1, 7] = np.nan
+    dY = synth.normal((2, out_f), 1.0, 16)
+    gradient_restructure_and_compare(torch, g, out_f, in_f, 0.25, X, dY)
+    snap = host(g.rows).copy(), host(g.cols).copy(), host(g.values).copy()
+    Xd, dYd = dev(X, torch), dev(dY, torch)
+    for zeta in (-0.1, 1.0):
+        with pytest.raises(binding.SnkError) as e:
+            g.prune_regrow_gradient(zeta, Xd, dYd)
+        assert e.value.status == binding.SNK_ERR_ARG
+    with pytest.raises(binding.SnkError) as e:
+        binding.snk_prune_regrow_gradient(g.handle, 0.3, Xd, dYd, batch=0)
+    assert e.value.status == binding.SNK_ERR_ARG
+    with pytest.raises(binding.SnkError) as e:
+        binding.snk_prune_regrow_gradient(g.handle, 0.3, 0, dYd, batch=2)
+    assert e.value.status == binding.SNK_ERR_ARG
+    before = g.topology_version
+    g.prune_regrow_gradient(0.0, Xd, dYd)      # k = 0: nothing happens
+    assert g.topology_version == before
+    np.testing.assert_array_equal(host(g.rows), snap[0])
+    np.testing.assert_array_equal(host(g.cols), snap[1])
+    np.testing.assert_array_equal(host(g.values), snap[2])
+    g.close()
+
+
+def test_rigl_training_stepwise(torch):
+    """A RigL run: SGD steps on an MSE loss, and every 10 steps a restructure
+    that grows where the current batch's gradient is largest; each restructure
+    is compared with the oracle on the GPU's current state."""
+    out_f, in_f, b = 800, 600, 4
+    lay = synth.make_layer(out_f, in_f, 90, 0.01, 41, 42)
+    X = synth.normal((b, in_f), 1.0, 43)
+    T = dev(synth.normal((b, out_f), 1.0, 44), torch)
+    Xd = dev(X, torch)
+    g = make_gpu_layer(torch, lay)
+    for step in range(30):
+        Y = g.forward(Xd)
+        dY = (2.0 / (b * out_f)) * (Y - T)
+        g.values.sub_(0.01 * g.backward_weight(Xd, dY))
+        if (step + 1) % 10 == 0:
+            gradient_restructure_and_compare(torch, g, out_f, in_f, 0.3, X, host(dY))
+    g.close()
+
+
+def test_full_size_gradient_restructure(torch):
+    """10000 x 10000 at 90%, zeta = 0.3, batch 4: 3,000,000 entries pruned and
+    grown at the largest gradients among 93,000,000 candidates.  Too large to
+    sort on the host, so the grown set is checked through its threshold theta
+    (the largest grown key): every kept entry survives with its value, k new
+    zero-valued positions were grown, and exactly k - 1 candidates have a key
+    below theta (the oracle's plain count over all positions).  Keys are
+    unique, so this pins the set exactly."""
+    out_f = in_f = 10_000
+    lay = synth.make_layer(out_f, in_f, 90, 0.01, 31, 32)
+    X = synth.normal((4, in_f), 1.0, 33)
+    dY = synth.normal((4, out_f), 1.0, 34)
+    g = make_gpu_layer(torch, lay)
+    v0, r0, c0 = host(g.values), host(g.rows), host(g.cols)
+    g.prune_regrow_gradient(0.3, dev(X, torch), dev(dY, torch))
+    removed, k = oracle.prune(out_f, in_f, v0, r0, c0, 0.3)
+    keep = removed == 0
+    kr, kc, kv = r0[keep], c0[keep], v0[keep]
+    lin0 = kr.astype(np.int64) * in_f + kc
+    r1, c1, v1 = host(g.rows), host(g.cols), host(g.values)
+    lin1 = r1.astype(np.int64) * in_f + c1
+    assert len(lin1) == len(v0) and np.all(np.diff(lin1) > 0)
+    held = np.isin(lin1, lin0)
+    assert int(held.sum()) == len(lin0)
+    np.testing.assert_array_equal(v1[held].view(np.uint32), kv.view(np.uint32))
+    grown = lin1[~held]
+    assert len(grown) == k and np.all(v1[~held].view(np.uint32) == 0)
+    theta = int(oracle.grad_keys(out_f, in_f, X, dY, grown).max())
+    assert oracle.grad_count_below(out_f, in_f, kr, kc, X, dY, theta) == k - 1
+    g.close()

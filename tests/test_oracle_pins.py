@@ -406,3 +406,137 @@ def test_prune_regrow_zero_fraction_is_identity():
     v, r, c = oracle.prune_regrow(10, 10, can["values"], can["rows"], can["cols"], 0.0, 5)
     np.testing.assert_array_equal(v, can["values"])
     np.testing.assert_array_equal(r, can["rows"])
+
+
+# ---------------------------------------------------------------- gradient grow (RigL)
+# [PCSR] sec. 4.3: a DST update drops a fraction of the live entries and grows
+# as many "at high-gradient locations".  The gradient at (r, c) is
+# sum_beta dY[beta, r] X[beta, c] ([PCSR] sec. 7.1 evaluated off the support).
+
+def _numpy_topk(keys_by_pos, k):
+    """Positions sorted by (larger |g| first, smaller position first)."""
+    pos = np.array(sorted(keys_by_pos, key=lambda p: (-keys_by_pos[p], p)), np.int64)
+    return np.sort(pos[:k])
+
+
+def test_grad_at_single_product_is_the_rounded_product():
+    # b = 1: fmaf(a, b, 0) is the product rounded once, which is what an fp32
+    # multiply gives
+    gen = synth.rng(91)
+    X = gen.standard_normal((1, 17)).astype(np.float32)
+    dY = gen.standard_normal((1, 11)).astype(np.float32)
+    for r in range(11):
+        for c in range(17):
+            assert np.float32(oracle.grad_at(11, 17, X, dY, r, c)) == dY[0, r] * X[0, c]
+
+
+def test_grow_gradient_batch1_matches_numpy_ranking():
+    gen = synth.rng(92)
+    out_f, in_f = 23, 31
+    X = gen.standard_normal((1, in_f)).astype(np.float32)
+    dY = gen.standard_normal((1, out_f)).astype(np.float32)
+    kept = set(gen.choice(out_f * in_f, 200, replace=False).tolist())
+    kr = np.array([p // in_f for p in sorted(kept)], np.int32)
+    kc = np.array([p % in_f for p in sorted(kept)], np.int32)
+    g = dY[0][:, None] * X[0][None, :]                      # exact fp32 products
+    mag = np.abs(g).view(np.uint32).astype(np.int64)
+    cand = {p: int(mag.flat[p]) for p in range(out_f * in_f) if p not in kept}
+    for k in (1, 10, 57, len(cand)):
+        np.testing.assert_array_equal(oracle.grow_gradient(out_f, in_f, kr, kc, X, dY, k),
+                                      _numpy_topk(cand, k))
+
+
+def test_grow_gradient_exact_integer_sums():
+    # small integers: every product and partial sum is exact in fp32, so the
+    # gradient is the integer dY^T X whatever the order
+    gen = synth.rng(93)
+    out_f, in_f, b = 13, 19, 3
+    X = gen.integers(-5, 6, (b, in_f)).astype(np.float32)
+    dY = gen.integers(-5, 6, (b, out_f)).astype(np.float32)
+    G = dY.astype(np.int64).T @ X.astype(np.int64)
+    kept = set(gen.choice(out_f * in_f, 60, replace=False).tolist())
+    kr = np.array([p // in_f for p in sorted(kept)], np.int32)
+    kc = np.array([p % in_f for p in sorted(kept)], np.int32)
+    cand = {p: abs(int(G.flat[p])) for p in range(out_f * in_f) if p not in kept}
+    for k in (5, 40, 100):
+        np.testing.assert_array_equal(oracle.grow_gradient(out_f, in_f, kr, kc, X, dY, k),
+                                      _numpy_topk(cand, k))
+
+
+def test_grow_gradient_ties_go_to_smaller_positions():
+    # every gradient has the same magnitude: the grown set is the k smallest
+    # free positions
+    out_f, in_f = 8, 9
+    X = np.ones((2, in_f), np.float32)
+    dY = np.full((2, out_f), 0.5, np.float32)
+    dY[:, ::2] *= -1
+    kr = np.array([0, 0, 3], np.int32)
+    kc = np.array([0, 5, 2], np.int32)
+    free = [p for p in range(out_f * in_f) if p not in (0, 5, 3 * in_f + 2)]
+    np.testing.assert_array_equal(oracle.grow_gradient(out_f, in_f, kr, kc, X, dY, 7), free[:7])
+
+
+def test_grow_gradient_nan_ranks_first_and_zero_last():
+    out_f, in_f = 4, 5
+    X = np.array([[1, 2, 0, 3, 1]], np.float32)
+    dY = np.array([[1, 1, 1, 1]], np.float32)
+    X[0, 4] = np.nan
+    kr = np.zeros(0, np.int32)
+    kc = np.zeros(0, np.int32)
+    # column 4 is NaN in every row (4 positions), then |g| = 3 (column 3)
+    got = oracle.grow_gradient(out_f, in_f, kr, kc, X, dY, 6)
+    np.testing.assert_array_equal(got, sorted([4, 9, 14, 19, 3, 8]))
+    # the zero column comes last of all
+    allp = oracle.grow_gradient(out_f, in_f, kr, kc, X, dY, 20)
+    np.testing.assert_array_equal(allp, np.arange(20))
+    last = oracle.grow_gradient(out_f, in_f, kr, kc, X, dY, 16)
+    assert set(range(20)) - set(last.tolist()) == {2, 7, 12, 17}
+
+
+def test_grow_gradient_count_below_is_the_rank():
+    gen = synth.rng(94)
+    out_f, in_f = 20, 24
+    X = gen.standard_normal((3, in_f)).astype(np.float32)
+    dY = gen.standard_normal((3, out_f)).astype(np.float32)
+    kept = np.sort(gen.choice(out_f * in_f, 100, replace=False))
+    kr, kc = (kept // in_f).astype(np.int32), (kept % in_f).astype(np.int32)
+    k = 50
+    grown = oracle.grow_gradient(out_f, in_f, kr, kc, X, dY, k)
+    keys = [oracle.grad_key(oracle.grad_at(out_f, in_f, X, dY, p // in_f, p % in_f), p)
+            for p in grown]
+    theta = max(keys)
+    assert oracle.grad_count_below(out_f, in_f, kr, kc, X, dY, theta) == k - 1
+    assert oracle.grad_count_below(out_f, in_f, kr, kc, X, dY, theta + 1) == k
+
+
+def test_prune_regrow_gradient_regrows_a_pruned_position():
+    # the smallest-magnitude entry sits where the gradient is largest: it is
+    # pruned and grown back at value +0.0 (the post-prune complement reading)
+    out_f, in_f = 5, 6
+    r = np.array([0, 1, 2, 3, 4], np.int32)
+    c = np.array([0, 1, 2, 3, 4], np.int32)
+    v = np.array([1e-3, 2.0, 3.0, 4.0, 5.0], np.float32)
+    X = np.zeros((1, in_f), np.float32)
+    dY = np.zeros((1, out_f), np.float32)
+    X[0, 0], dY[0, 0] = 10.0, 10.0      # |g(0, 0)| = 100, every other g is 0
+    v2, r2, c2 = oracle.prune_regrow_gradient(out_f, in_f, v, r, c, 0.2, X, dY)
+    np.testing.assert_array_equal(r2, r)
+    np.testing.assert_array_equal(c2, c)
+    assert v2[0] == 0.0 and not np.signbit(v2[0])
+    np.testing.assert_array_equal(v2[1:], v[1:])
+
+
+def test_prune_regrow_gradient_invariants():
+    lay = synth.make_layer(30, 40, 80, 1.0, 5, 6)
+    X = synth.normal((4, 40), 1.0, 7)
+    dY = synth.normal((4, 30), 1.0, 8)
+    v, r, c = oracle.prune_regrow_gradient(30, 40, lay.values, lay.rows, lay.cols, 0.3, X, dY)
+    lin = r.astype(np.int64) * 40 + c
+    assert len(v) == lay.nnz and np.all(np.diff(lin) > 0)
+    removed, k = oracle.prune(30, 40, lay.values, lay.rows, lay.cols, 0.3)
+    kept_lin = sorted(int(a) * 40 + int(b) for a, b, rm in zip(lay.rows, lay.cols, removed) if not rm)
+    kl = np.array(kept_lin, np.int64)
+    grown = oracle.grow_gradient(30, 40, (kl // 40).astype(np.int32), (kl % 40).astype(np.int32),
+                                 X, dY, k)
+    assert set(lin.tolist()) == set(kept_lin) | set(grown.tolist())
+    assert len(set(kept_lin) & set(grown.tolist())) == 0
