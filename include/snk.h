@@ -191,6 +191,73 @@ int snk_prune_regrow_gradient(snk_handle handle, float zeta, const float* X, con
                               int64_t batch, void* stream);
 
 /*
+ * Padded-CSR view ([PCSR] sec. 5), for dynamic sparse training whose per-row
+ * counts change.  A library-owned copy of the layer in the six arrays of
+ * [PCSR] sec. 5.1: slot values and column indices (column -1 marks a padding
+ * slot, value 0), row_start, row_nnz (a row's live slots come first in its
+ * region), row_capacity, and a version counter.  The view is taken from the
+ * handle's triple by snk_pcsr_build and is independent of it afterwards:
+ * mutations of the view reach a layer through snk_pcsr_export (a canonical
+ * triple for a new handle), and restructures of the handle do not reach the
+ * view.  Readings fixed by this library where the page is silent:
+ *   - padding is a whole percentage p: capacity(n) = max(1, ceil(n*(100+p)/100))
+ *     in integers ([PCSR] sec. 5.2's 0.2 is p = 20);
+ *   - an insert batch first moves every row whose live count plus inserts
+ *     exceeds its capacity, in ascending row order, to fresh slots at the end
+ *     of the used slot area with capacity(live + inserts); the old slots become
+ *     padding ([PCSR] sec. 4.3's resize); then each insert takes the next slot
+ *     of its row in batch order ([PCSR] sec. 5.3: O(1) per insert);
+ *   - a delete batch clears the slots and each touched row closes up, its
+ *     remaining live entries keeping their order;
+ *   - compact ([PCSR] sec. 8.3's compact_all) lays all rows out again from
+ *     slot 0, row by row, capacity(live) each, columns ascending.
+ *   - the version starts at 1 and goes up by one per applied insert batch,
+ *     delete batch and compact.
+ * Slot indices are int32: at most 2^31 - 1 slots.  All pointers are device
+ * pointers; calls synchronise the stream (they read counts back).
+ */
+
+/* Build (or rebuild) the view from the handle's current triple, padding p %
+ * (0 <= p <= 10000).  Errors: SNK_ERR_ARG, SNK_ERR_OOM, SNK_ERR_LIMIT, SNK_ERR_CUDA. */
+int snk_pcsr_build(snk_handle handle, int padding_pct, void* stream);
+
+/* Slots in use (the end of the last row region), live entries and version;
+ * any output may be NULL.  Errors: SNK_ERR_ARG (no view), SNK_ERR_CUDA. */
+int snk_pcsr_info(snk_handle handle, int64_t* used_slots, int64_t* n_live, int64_t* version,
+                  void* stream);
+
+/* Copy the view out: slot_values / slot_cols [used_slots], row_start, row_nnz,
+ * row_capacity [out]; any may be NULL.  Asynchronous. */
+int snk_pcsr_copy(snk_handle handle, float* slot_values, int32_t* slot_cols, int32_t* row_start,
+                  int32_t* row_nnz, int32_t* row_capacity, void* stream);
+
+/* Insert n entries (rows[i], cols[i], values[i]).  The positions must not be
+ * live (a repeat is reported by snk_pcsr_compact / snk_pcsr_export as
+ * SNK_ERR_DUP).  Errors: SNK_ERR_ARG, SNK_ERR_RANGE (an index outside the
+ * matrix; nothing changed), SNK_ERR_OOM, SNK_ERR_LIMIT, SNK_ERR_CUDA. */
+int snk_pcsr_insert(snk_handle handle, int64_t n, const int32_t* rows, const int32_t* cols,
+                    const float* values, void* stream);
+
+/* Delete the n live entries at (rows[i], cols[i]).  Errors: SNK_ERR_RANGE (an
+ * index outside the matrix), SNK_ERR_ARG (a position that is not live); on
+ * either nothing changed. */
+int snk_pcsr_delete(snk_handle handle, int64_t n, const int32_t* rows, const int32_t* cols,
+                    void* stream);
+
+/* compact_all: lay the view out again from slot 0 with fresh padding and
+ * columns ascending.  Errors: SNK_ERR_DUP (a position held twice; nothing
+ * changed), SNK_ERR_OOM, SNK_ERR_CUDA. */
+int snk_pcsr_compact(snk_handle handle, void* stream);
+
+/* Write the live entries as a canonical COO triple (row-major, columns
+ * ascending) into values / rows / cols of the given capacity; *nnz_out gets
+ * the count (also when it exceeds capacity, which returns SNK_ERR_LIMIT and
+ * writes nothing).  The triple can be bound to a new handle with snk_create.
+ * Errors: SNK_ERR_ARG, SNK_ERR_LIMIT, SNK_ERR_DUP, SNK_ERR_CUDA. */
+int snk_pcsr_export(snk_handle handle, float* values, int32_t* rows, int32_t* cols,
+                    int64_t capacity, int64_t* nnz_out, void* stream);
+
+/*
  * snk_destroy - free the library-owned workspace (never the caller's arrays).
  * NULL is accepted.  Waits for work queued on the handle's device.
  */

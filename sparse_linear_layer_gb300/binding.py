@@ -55,9 +55,19 @@ def lib():
                                     ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.snk_copy_topology.argtypes = [P, P, P, P, P, P]
         L.snk_forward_csr_noalloc.argtypes = [i64, i64, i64, P, P, P, P, i64, P, P, P]
+        L.snk_pcsr_build.argtypes = [P, I, P]
+        L.snk_pcsr_info.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                    ctypes.POINTER(i64), P]
+        L.snk_pcsr_copy.argtypes = [P, P, P, P, P, P, P]
+        L.snk_pcsr_insert.argtypes = [P, i64, P, P, P, P]
+        L.snk_pcsr_delete.argtypes = [P, i64, P, P, P]
+        L.snk_pcsr_compact.argtypes = [P, P]
+        L.snk_pcsr_export.argtypes = [P, P, P, P, i64, ctypes.POINTER(i64), P]
         for name in ("snk_create", "snk_forward", "snk_backward_input", "snk_backward_weight",
                      "snk_prune_regrow", "snk_prune_regrow_gradient", "snk_destroy",
-                     "snk_get_shape", "snk_copy_topology", "snk_forward_csr_noalloc"):
+                     "snk_get_shape", "snk_copy_topology", "snk_forward_csr_noalloc",
+                     "snk_pcsr_build", "snk_pcsr_info", "snk_pcsr_copy", "snk_pcsr_insert",
+                     "snk_pcsr_delete", "snk_pcsr_compact", "snk_pcsr_export"):
             getattr(L, name).restype = I
         _lib = L
         return L
@@ -165,6 +175,47 @@ def snk_forward_csr_noalloc(out_features: int, in_features: int, row_ptr, cols, 
                                          _stream(stream)), "snk_forward_csr_noalloc")
 
 
+def snk_pcsr_build(handle: int, padding_pct: int = 20, stream=None):
+    _check(lib().snk_pcsr_build(handle, int(padding_pct), _stream(stream)), "snk_pcsr_build")
+
+
+def snk_pcsr_info(handle: int, stream=None):
+    """(used_slots, n_live, version)"""
+    u, n, v = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().snk_pcsr_info(handle, ctypes.byref(u), ctypes.byref(n), ctypes.byref(v),
+                               _stream(stream)), "snk_pcsr_info")
+    return u.value, n.value, v.value
+
+
+def snk_pcsr_copy(handle: int, slot_values=None, slot_cols=None, row_start=None, row_nnz=None,
+                  row_capacity=None, stream=None):
+    _check(lib().snk_pcsr_copy(handle, _ptr(slot_values), _ptr(slot_cols), _ptr(row_start),
+                               _ptr(row_nnz), _ptr(row_capacity), _stream(stream)),
+           "snk_pcsr_copy")
+
+
+def snk_pcsr_insert(handle: int, rows, cols, values, stream=None):
+    _check(lib().snk_pcsr_insert(handle, rows.numel(), _ptr(rows), _ptr(cols), _ptr(values),
+                                 _stream(stream)), "snk_pcsr_insert")
+
+
+def snk_pcsr_delete(handle: int, rows, cols, stream=None):
+    _check(lib().snk_pcsr_delete(handle, rows.numel(), _ptr(rows), _ptr(cols), _stream(stream)),
+           "snk_pcsr_delete")
+
+
+def snk_pcsr_compact(handle: int, stream=None):
+    _check(lib().snk_pcsr_compact(handle, _stream(stream)), "snk_pcsr_compact")
+
+
+def snk_pcsr_export(handle: int, values, rows, cols, stream=None) -> int:
+    """Canonical live triple into the given tensors; returns nnz."""
+    n = ctypes.c_int64()
+    _check(lib().snk_pcsr_export(handle, _ptr(values), _ptr(rows), _ptr(cols), values.numel(),
+                                 ctypes.byref(n), _stream(stream)), "snk_pcsr_export")
+    return n.value
+
+
 class SparseLinear:
     """Convenience owner of one layer: keeps the caller-side tensors alive for
     the handle's lifetime and allocates outputs with torch."""
@@ -208,6 +259,22 @@ class SparseLinear:
 
     def prune_regrow_gradient(self, zeta: float, X, dY, stream=None):
         snk_prune_regrow_gradient(self.handle, zeta, X, dY, stream)
+
+    def pcsr(self):
+        """The Padded-CSR view as host-readable torch tensors (slot arrays cut
+        to the used slots)."""
+        import torch
+        dev = self.values.device
+        used, live, version = snk_pcsr_info(self.handle)
+        out = dict(slot_values=torch.empty(used, dtype=torch.float32, device=dev),
+                   slot_cols=torch.empty(used, dtype=torch.int32, device=dev),
+                   row_start=torch.empty(self.out_features, dtype=torch.int32, device=dev),
+                   row_nnz=torch.empty(self.out_features, dtype=torch.int32, device=dev),
+                   row_capacity=torch.empty(self.out_features, dtype=torch.int32, device=dev))
+        snk_pcsr_copy(self.handle, out["slot_values"], out["slot_cols"], out["row_start"],
+                      out["row_nnz"], out["row_capacity"])
+        out["n_live"], out["version"] = live, version
+        return out
 
     def topology(self):
         import torch

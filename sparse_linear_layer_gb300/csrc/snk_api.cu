@@ -9,8 +9,6 @@
 
 namespace snk {
 
-int64_t topology_hist_len(int64_t n);
-
 // Host-side fault injection for tests: SNK_FAULT=alloc makes workspace
 // allocation fail, SNK_FAULT=launch makes the product calls fail before they
 // queue work.  Nothing here touches the GPU.
@@ -24,6 +22,7 @@ static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)
 static void free_layer(Layer* L) {
     if (!L) return;
     free_restructure(L);
+    free_pcsr(L);
     void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->c16, L->rc16, L->bnd_r, L->bnd_c, L->cdesc_r, L->cdesc_c,
                     L->bdesc_r, L->bdesc_c,
                     L->part, L->cnt, L->xt, L->status, L->sort_keys, L->sort_vals,

@@ -47,6 +47,7 @@ constexpr int kStatDup = 2;
 constexpr int kStatLimit = 4;
 
 struct RestructureWs;
+struct PcsrState;
 
 // Per block: its entry range [k0, k1), and for the segment that enters the
 // block from before (head) and the one that leaves it (tail) the first and
@@ -110,7 +111,10 @@ struct Layer {
     int64_t tile_hist_len = 0;
 
     RestructureWs* rws = nullptr; // allocated on first prune_regrow
+    PcsrState* pcsr = nullptr;    // Padded-CSR view, built on request
 };
+
+void free_pcsr(Layer* L);
 
 // ---- small helpers -------------------------------------------------------
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -129,6 +133,13 @@ int build_topology(Layer* L, cudaStream_t s, bool validate);
 int exclusive_scan_i32(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp, int64_t tmp_len,
                        int32_t* total, cudaStream_t s);
 int64_t scan_tmp_len(int64_t n);
+int64_t topology_hist_len(int64_t n);
+// Stable LSD radix sort of (key, value) pairs by the low total_bits of the
+// key; the result is in the alternate buffers when *flipped.
+int sort_pairs_u64(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt, int64_t n,
+                   int total_bits, int32_t* hist, int64_t hist_len, cudaStream_t s, bool* flipped);
+int sort_pairs_u32(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt, int64_t n,
+                   int total_bits, int32_t* hist, int64_t hist_len, cudaStream_t s, bool* flipped);
 
 // ---- kernels launched by the API ----------------------------------------
 int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float* Y,

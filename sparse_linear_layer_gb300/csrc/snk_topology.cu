@@ -250,6 +250,17 @@ static int radix_sort_pairs(K* keys, uint32_t* vals, K* keys_alt, uint32_t* vals
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
+int sort_pairs_u64(uint64_t* keys, uint32_t* vals, uint64_t* keys_alt, uint32_t* vals_alt, int64_t n,
+                   int total_bits, int32_t* hist, int64_t hist_len, cudaStream_t s, bool* flipped) {
+    return radix_sort_pairs<uint64_t>(keys, vals, keys_alt, vals_alt, n, total_bits, hist,
+                                      hist_len, s, flipped);
+}
+int sort_pairs_u32(uint32_t* keys, uint32_t* vals, uint32_t* keys_alt, uint32_t* vals_alt, int64_t n,
+                   int total_bits, int32_t* hist, int64_t hist_len, cudaStream_t s, bool* flipped) {
+    return radix_sort_pairs<uint32_t>(keys, vals, keys_alt, vals_alt, n, total_bits, hist,
+                                      hist_len, s, flipped);
+}
+
 // ------------------------------------------------------------------ topology kernels
 static int bits_for(uint64_t n_values) {
     // number of bits needed to represent 0 .. n_values-1
