@@ -167,14 +167,20 @@ def test_single_dense_row_and_dense_column(torch):
         check_all_products(torch, lay, b)
 
 
-def test_global_memory_operand_path(torch):
-    """in * BP * 4 bytes exceeds shared memory: the operand is read from a
-    transposed copy in global memory."""
+def test_operand_larger_than_shared_memory(torch):
+    """in * BP * 4 bytes exceeds shared memory: every operand row is read from
+    a transposed copy in global memory (L1-cached read-only loads).
+      in = 60,000 at b = 1, 4, 8; out = 20,000 (the dX operand) at b = 16, 64;
+      in = 70,000, which has no 16-bit index copy, at b = 1, 4."""
     lay = synth.make_layer(50, 60_000, 99, 0.05, 21, 22)
     for b in (1, 4, 8):
         check_all_products(torch, lay, b)
-    lay = synth.make_layer(20_000, 64, 90, 0.05, 23, 24)  # dX path: out large
-    check_all_products(torch, lay, 16)
+    lay = synth.make_layer(20_000, 64, 90, 0.05, 23, 24)
+    for b in (16, 64):
+        check_all_products(torch, lay, b)
+    lay = synth.make_layer(40, 70_000, 99.5, 0.05, 25, 26)
+    for b in (1, 4):
+        check_all_products(torch, lay, b)
 
 
 def test_no_entries(torch):
