@@ -171,7 +171,7 @@ def test_operand_larger_than_shared_memory(torch):
     """in * BP * 4 bytes exceeds shared memory: every operand row is read from
     a transposed copy in global memory (L1-cached read-only loads).
       in = 60,000 at b = 1, 4, 8; out = 20,000 (the dX operand) at b = 16, 64;
-      in = 70,000, which has no 16-bit index copy, at b = 1, 4."""
+      in = 70,000 and out = 70,000, which have no 16-bit index copy, at b = 1, 4."""
     lay = synth.make_layer(50, 60_000, 99, 0.05, 21, 22)
     for b in (1, 4, 8):
         check_all_products(torch, lay, b)
@@ -179,6 +179,10 @@ def test_operand_larger_than_shared_memory(torch):
     for b in (16, 64):
         check_all_products(torch, lay, b)
     lay = synth.make_layer(40, 70_000, 99.5, 0.05, 25, 26)
+    for b in (1, 4):
+        check_all_products(torch, lay, b)
+    # out = 70,000: the transposed product has no 16-bit row copy either
+    lay = synth.make_layer(70_000, 40, 99.5, 0.05, 27, 28)
     for b in (1, 4):
         check_all_products(torch, lay, b)
 
