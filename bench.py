@@ -346,6 +346,32 @@ def time_ops(binding, g, X, dY, bias, Y, dX, dW, db, flush, stream, steps, warmu
     return {name: [e0.elapsed_time(e1) for e0, e1 in ev[name]] for name, _ in ops}
 
 
+def gather_reference(torch, g, flush, stream, dx_us):
+    """The transposed product reads values[perm] in random order: one 4-byte
+    value per stored entry, each from its own 32-byte sector.  That gather
+    alone, timed here as torch's index_select over the same permutation (a
+    library kernel used only as a yardstick, like the copy kernel behind the
+    HBM peak), bounds dX from below; 'frac' is gather time / dX time."""
+    perm = g.topology()["perm"].long()
+    out = torch.empty_like(g.values)
+    ts = []
+    for i in range(13):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        torch.index_select(g.values, 0, perm, out=out)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    t = statistics.mean(ts)
+    return {"bound": "random value gather (L1 sector lookups)", "kernel": "k_spmm_dx",
+            "reference": "torch.index_select(values, 0, perm), same 10M-entry permutation, "
+                         "L2 flushed, CUDA events",
+            "gather_us": t, "dx_us": dx_us, "frac": t / dx_us}
+
+
 def summarize(per_op_ms, alg, formula, peak):
     out = {}
     for n, v in per_op_ms.items():
@@ -561,6 +587,8 @@ def run_ours(args, workload, rank, world, local):
         "frac": per_op[dom]["frac"], "traffic": committed_traffic(kernel_tags[dom], workload["workload"]),
         "algorithmic_bytes_per_launch": alg[dom], "per_op": per_op,
     }
+    if not args.only and lay.nnz > 0:
+        roofline["onchip"] = gather_reference(torch, g, flush, stream, per_op["dx"]["us_mean"])
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e = None
