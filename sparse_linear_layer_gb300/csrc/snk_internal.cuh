@@ -128,6 +128,9 @@ inline int batch_tile(int64_t b) {
 // Sort + validate + write back the canonical triple + CSR + CSC + chunk tables.
 // Returns an SNK_* status; synchronises `s`.
 int build_topology(Layer* L, cudaStream_t s, bool validate);
+// The rest of the build for a triple already in canonical order whose
+// col_keys / col_vals hold (column, slot) of every entry.
+int build_views(Layer* L, cudaStream_t s);
 
 // Radix helpers reused by the restructure code.
 int exclusive_scan_i32(const int32_t* in, int32_t* out, int64_t n, int32_t* tmp, int64_t tmp_len,

@@ -40,8 +40,10 @@
 //    finds the k-th smallest key, stopping early when a digit bin holds
 //    exactly the remaining count; a last pass collects every candidate at or
 //    below it: exactly k positions, since keys are unique.
-//  * The kept and grown entries are written back into the caller's triple
-//    and the topology build re-sorts it.
+//  * Write-back: the kept entries come out of the compaction already in
+//    canonical order, so only the k grown positions are radix-sorted and the
+//    two lists are merged (merge path) straight into the caller's triple in
+//    canonical order; only the derived views are rebuilt.
 #include <algorithm>
 
 #include "snk_internal.cuh"
@@ -74,8 +76,9 @@ struct RestructureWs {
     int64_t* acc = nullptr;      // device scalar: accepted so far
     uint64_t* kept_lin = nullptr;
     uint32_t* kept_val = nullptr;
-    uint64_t* H = nullptr;
+    uint64_t* H = nullptr;       // kept-or-accepted hash set (large matrices)
     uint64_t H_mask = 0;
+    uint32_t* bits = nullptr;    // the same as a bitmap over all positions (out*in <= 2^31)
     uint64_t* R_key = nullptr;
     uint64_t* R_t = nullptr;
     uint64_t R_mask = 0;
@@ -100,7 +103,7 @@ void free_restructure(Layer* L) {
     RestructureWs* w = L->rws;
     if (!w) return;
     void* ptrs[] = {w->hist, w->sel, w->flags, w->scan_tmp, w->total, w->acc, w->kept_lin,
-                    w->kept_val, w->H, w->R_key, w->R_t, w->cand, w->new_lin, w->err,
+                    w->kept_val, w->H, w->bits, w->R_key, w->R_t, w->cand, w->new_lin, w->err,
                     w->ghist, w->gsel, w->kept_ptr};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -119,9 +122,11 @@ static int alloc_restructure(Layer* L) {
     const int64_t fl = std::max<int64_t>(n, w->cand_cap);
     w->flag_half = fl;
     w->scan_tmp_len = scan_tmp_len(fl);
-    const uint64_t hcap = next_pow2(2 * (uint64_t)n + 64);
+    const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
+    const bool use_bits = n_pos <= (1ull << 31);
+    const uint64_t hcap = use_bits ? 0 : next_pow2(2 * (uint64_t)n + 64);
     const uint64_t rcap = next_pow2(2 * (uint64_t)w->cand_cap + 64);
-    w->H_mask = hcap - 1;
+    w->H_mask = use_bits ? 0 : hcap - 1;
     w->R_mask = rcap - 1;
     bool ok = cudaMalloc(&w->hist, 256 * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&w->sel, sizeof(SelState)) == cudaSuccess &&
@@ -131,7 +136,8 @@ static int alloc_restructure(Layer* L) {
               cudaMalloc(&w->acc, sizeof(int64_t)) == cudaSuccess &&
               cudaMalloc(&w->kept_lin, n * sizeof(uint64_t)) == cudaSuccess &&
               cudaMalloc(&w->kept_val, n * sizeof(uint32_t)) == cudaSuccess &&
-              cudaMalloc(&w->H, hcap * sizeof(uint64_t)) == cudaSuccess &&
+              (use_bits ? cudaMalloc(&w->bits, (n_pos / 32 + 1) * sizeof(uint32_t))
+                        : cudaMalloc(&w->H, hcap * sizeof(uint64_t))) == cudaSuccess &&
               cudaMalloc(&w->R_key, rcap * sizeof(uint64_t)) == cudaSuccess &&
               cudaMalloc(&w->R_t, rcap * sizeof(uint64_t)) == cudaSuccess &&
               cudaMalloc(&w->cand, w->cand_cap * sizeof(uint64_t)) == cudaSuccess &&
@@ -282,22 +288,38 @@ __global__ void k_compact(const float* __restrict__ v, const int32_t* __restrict
 }
 
 // ---------------------------------------------------------------- regrow kernels
-__global__ void k_set_fill(uint64_t* H, uint64_t mask, const uint64_t* __restrict__ keys, int64_t n,
-                           int32_t* err) {
+// The set of held positions (kept, then also accepted): a bitmap over all
+// positions when there are at most 2^31 of them (it then sits in L2), else
+// an open-addressing hash set.
+struct HeldSet {
+    uint64_t* H;
+    uint64_t mask;
+    uint32_t* bits;
+    __device__ __forceinline__ bool has(uint64_t p) const {
+        if (bits) return (bits[p >> 5] >> (p & 31u)) & 1u;
+        return set_has(H, mask, p);
+    }
+    __device__ __forceinline__ void insert(uint64_t p, int32_t* err) const {
+        if (bits) atomicOr(bits + (p >> 5), 1u << (p & 31u));
+        else set_insert(H, mask, p, err);
+    }
+};
+
+__global__ void k_set_fill(HeldSet hs, const uint64_t* __restrict__ keys, int64_t n, int32_t* err) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
-        set_insert(H, mask, keys[i], err);
+        hs.insert(keys[i], err);
 }
 
-__global__ void k_draw(uint64_t seed, uint64_t t0, int64_t B, uint64_t n_pos,
-                       const uint64_t* __restrict__ H, uint64_t H_mask, uint64_t* R_key,
-                       uint64_t* R_t, uint64_t R_mask, uint64_t* __restrict__ cand, int32_t* err) {
+__global__ void k_draw(uint64_t seed, uint64_t t0, int64_t B, uint64_t n_pos, HeldSet hs,
+                       uint64_t* R_key, uint64_t* R_t, uint64_t R_mask,
+                       uint64_t* __restrict__ cand, int32_t* err) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < B;
          i += (int64_t)gridDim.x * blockDim.x) {
         const uint64_t t = t0 + (uint64_t)i;
         const uint64_t z = splitmix64_mix(seed + (t + 1ull) * kGamma);
         const uint64_t p = __umul64hi(z, n_pos);
-        if (set_has(H, H_mask, p)) {
+        if (hs.has(p)) {
             cand[i] = kEmpty;
         } else {
             cand[i] = p;
@@ -319,14 +341,14 @@ __global__ void k_first_flags(const uint64_t* __restrict__ cand, int64_t B, uint
 
 __global__ void k_take(const uint64_t* __restrict__ cand, const int32_t* __restrict__ surv,
                        const int32_t* __restrict__ pos, int64_t B, const int64_t* acc, int64_t k,
-                       uint64_t* __restrict__ new_lin, uint64_t* H, uint64_t H_mask, int32_t* err) {
+                       uint64_t* __restrict__ new_lin, HeldSet hs, int32_t* err) {
     const int64_t a = *acc;
     const int64_t need = k - a;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < B;
          i += (int64_t)gridDim.x * blockDim.x) {
         if (surv[i] && pos[i] < need) {
             new_lin[a + pos[i]] = cand[i];
-            set_insert(H, H_mask, cand[i], err);
+            hs.insert(cand[i], err);
         }
     }
 }
@@ -335,27 +357,6 @@ __global__ void k_advance(int64_t* acc, const int32_t* total, int64_t k) {
     if (threadIdx.x == 0) {
         const int64_t need = k - *acc;
         *acc += (int64_t)(*total < need ? *total : need);
-    }
-}
-
-__global__ void k_assemble(const uint64_t* __restrict__ kept_lin, const uint32_t* __restrict__ kept_val,
-                           int64_t m, const uint64_t* __restrict__ new_lin, int64_t k, int64_t in_f,
-                           float* __restrict__ v, int32_t* __restrict__ r, int32_t* __restrict__ c) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < m + k;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        uint64_t lin;
-        uint32_t val;
-        if (i < m) {
-            lin = kept_lin[i];
-            val = kept_val[i];
-        } else {
-            lin = new_lin[i - m];
-            val = 0u;
-        }
-        const uint64_t rr = lin / (uint64_t)in_f;
-        v[i] = __uint_as_float(val);
-        r[i] = (int32_t)rr;
-        c[i] = (int32_t)(lin - rr * (uint64_t)in_f);
     }
 }
 
@@ -498,6 +499,81 @@ __global__ void k_grad_pick(const int32_t* __restrict__ hist, int width, GradSel
     }
 }
 
+// Canonical triple from the kept entries (ascending positions, with values)
+// and the grown positions (ascending, value +0.0f), by merge path: output
+// tile q covers slots [q*T, (q+1)*T); the split of each tile boundary between
+// the two lists is found by a binary search on the diagonal (the lists share
+// no position), the block stages its pieces of both lists in shared memory,
+// and each thread merges kMergePer consecutive outputs from its own split.
+// Also writes the (column, slot) pairs the column view is sorted from.
+constexpr int kMergeThreads = 256;
+constexpr int kMergePer = 8;
+constexpr int kMergeTile = kMergeThreads * kMergePer;
+
+// number of kept entries among the first d outputs of the merge
+__device__ __forceinline__ int64_t merge_split(const uint64_t* __restrict__ a, int64_t m,
+                                               const uint64_t* __restrict__ b, int64_t k,
+                                               int64_t d) {
+    int64_t lo = d > k ? d - k : 0, hi = d < m ? d : m;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (a[mid] < b[d - mid - 1]) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kMergeThreads) k_merge_assemble(
+    const uint64_t* __restrict__ kept_lin, const uint32_t* __restrict__ kept_val, int64_t m,
+    const uint64_t* __restrict__ new_lin, int64_t k, int64_t in_f, float* __restrict__ v,
+    int32_t* __restrict__ r, int32_t* __restrict__ c, uint32_t* __restrict__ col_key,
+    uint32_t* __restrict__ col_val) {
+    __shared__ uint64_t sa[kMergeTile], sb[kMergeTile];
+    __shared__ uint32_t sv[kMergeTile];
+    __shared__ int64_t split[2];
+    const int64_t n = m + k;
+    for (int64_t t0 = (int64_t)blockIdx.x * kMergeTile; t0 < n; t0 += (int64_t)gridDim.x * kMergeTile) {
+        const int64_t t1 = min(n, t0 + (int64_t)kMergeTile);
+        if (threadIdx.x < 2) split[threadIdx.x] = merge_split(kept_lin, m, new_lin, k, threadIdx.x ? t1 : t0);
+        __syncthreads();
+        const int64_t i0 = split[0], i1 = split[1];
+        const int64_t j0 = t0 - i0, j1 = t1 - i1;
+        const int na = (int)(i1 - i0), nb = (int)(j1 - j0);
+        for (int x = threadIdx.x; x < na; x += kMergeThreads) {
+            sa[x] = kept_lin[i0 + x];
+            sv[x] = kept_val[i0 + x];
+        }
+        for (int x = threadIdx.x; x < nb; x += kMergeThreads) sb[x] = new_lin[j0 + x];
+        __syncthreads();
+        // this thread's outputs: [d0, d1) within the tile
+        const int d0 = min(na + nb, threadIdx.x * kMergePer);
+        const int d1 = min(na + nb, d0 + kMergePer);
+        int lo = d0 > nb ? d0 - nb : 0, hi = d0 < na ? d0 : na;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sa[mid] < sb[d0 - mid - 1]) lo = mid + 1;
+            else hi = mid;
+        }
+        int ia = lo, ib = d0 - lo;
+        for (int d = d0; d < d1; ++d) {
+            const bool take_a = ib >= nb || (ia < na && sa[ia] < sb[ib]);
+            const uint64_t lin = take_a ? sa[ia] : sb[ib];
+            const uint32_t val = take_a ? sv[ia] : 0u;
+            if (take_a) ++ia;
+            else ++ib;
+            const int64_t pos = t0 + d;
+            const uint64_t rr = lin / (uint64_t)in_f;
+            const int32_t cc = (int32_t)(lin - rr * (uint64_t)in_f);
+            v[pos] = __uint_as_float(val);
+            r[pos] = (int32_t)rr;
+            c[pos] = cc;
+            col_key[pos] = (uint32_t)cc;
+            col_val[pos] = (uint32_t)pos;
+        }
+        __syncthreads();  // before the next tile reuses the shared arrays
+    }
+}
+
 static int bits_for(uint64_t n_values) {
     int b = 0;
     while (b < 64 && (n_values - 1) >> b) ++b;
@@ -541,8 +617,10 @@ static int grow_uniform(Layer* L, int64_t k, uint64_t seed, cudaStream_t s) {
     RestructureWs* w = L->rws;
     const int64_t m = L->nnz - k;
     const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
-    cudaMemsetAsync(w->H, 0xFF, (w->H_mask + 1) * sizeof(uint64_t), s);
-    k_set_fill<<<grid_of(m, L->num_sms), 256, 0, s>>>(w->H, w->H_mask, w->kept_lin, m, w->err);
+    const HeldSet hs{w->H, w->H_mask, w->bits};
+    if (w->bits) cudaMemsetAsync(w->bits, 0, (n_pos / 32 + 1) * sizeof(uint32_t), s);
+    else cudaMemsetAsync(w->H, 0xFF, (w->H_mask + 1) * sizeof(uint64_t), s);
+    k_set_fill<<<grid_of(m, L->num_sms), 256, 0, s>>>(hs, w->kept_lin, m, w->err);
     cudaMemsetAsync(w->acc, 0, sizeof(int64_t), s);
     const uint64_t t_max = 64ull * (uint64_t)k + 1024ull;
     uint64_t t0 = 0;
@@ -553,16 +631,16 @@ static int grow_uniform(Layer* L, int64_t k, uint64_t seed, cudaStream_t s) {
         B = (int64_t)std::min<uint64_t>((uint64_t)B, t_max - t0);
         int32_t* surv = w->flags;
         int32_t* rank = w->flags + w->flag_half;
-        cudaMemsetAsync(w->R_key, 0xFF, (w->R_mask + 1) * sizeof(uint64_t), s);
-        cudaMemsetAsync(w->R_t, 0xFF, (w->R_mask + 1) * sizeof(uint64_t), s);
+        // the round-local table is sized for this round's draws
+        const uint64_t rm = std::min<uint64_t>(w->R_mask, next_pow2(2 * (uint64_t)B + 64) - 1);
+        cudaMemsetAsync(w->R_key, 0xFF, (rm + 1) * sizeof(uint64_t), s);
+        cudaMemsetAsync(w->R_t, 0xFF, (rm + 1) * sizeof(uint64_t), s);
         const unsigned GB = grid_of(B, L->num_sms);
-        k_draw<<<GB, 256, 0, s>>>(seed, t0, B, n_pos, w->H, w->H_mask, w->R_key, w->R_t, w->R_mask,
-                                  w->cand, w->err);
-        k_first_flags<<<GB, 256, 0, s>>>(w->cand, B, t0, w->R_key, w->R_t, w->R_mask, surv);
+        k_draw<<<GB, 256, 0, s>>>(seed, t0, B, n_pos, hs, w->R_key, w->R_t, rm, w->cand, w->err);
+        k_first_flags<<<GB, 256, 0, s>>>(w->cand, B, t0, w->R_key, w->R_t, rm, surv);
         int st = exclusive_scan_i32(surv, rank, B, w->scan_tmp, w->scan_tmp_len, w->total, s);
         if (st != SNK_OK) return st;
-        k_take<<<GB, 256, 0, s>>>(w->cand, surv, rank, B, w->acc, k, w->new_lin, w->H, w->H_mask,
-                                  w->err);
+        k_take<<<GB, 256, 0, s>>>(w->cand, surv, rank, B, w->acc, k, w->new_lin, hs, w->err);
         k_advance<<<1, 32, 0, s>>>(w->acc, w->total, k);
         if (cudaMemcpyAsync(&accepted, w->acc, sizeof(int64_t), cudaMemcpyDeviceToHost, s) !=
                 cudaSuccess ||
@@ -631,14 +709,25 @@ static int grow_gradient(Layer* L, int64_t k, const float* X, const float* dY, i
     return SNK_OK;
 }
 
+// Write the new triple in canonical order: the kept entries are already in
+// order, so only the k grown positions are sorted and the two lists merged;
+// then the views are rebuilt.
 static int assemble(Layer* L, int64_t k, cudaStream_t s) {
     RestructureWs* w = L->rws;
     const int64_t m = L->nnz - k;
-    k_assemble<<<grid_of(L->nnz, L->num_sms), 256, 0, s>>>(w->kept_lin, w->kept_val, m,
-                                                           w->new_lin, k, L->in_f, L->v, L->r,
-                                                           L->c);
+    bool flipped = false;
+    int st = sort_pairs_u64(w->new_lin, reinterpret_cast<uint32_t*>(w->flags), w->cand,
+                            reinterpret_cast<uint32_t*>(w->flags + w->flag_half), k,
+                            bits_for((uint64_t)L->out_f * (uint64_t)L->in_f), L->tile_hist,
+                            L->tile_hist_len, s, &flipped);
+    if (st != SNK_OK) return st;
+    const uint64_t* grown = flipped ? w->cand : w->new_lin;
+    const unsigned gm = (unsigned)std::max<int64_t>(
+        1, std::min<int64_t>(ceil_div(L->nnz, kMergeTile), (int64_t)L->num_sms * 8));
+    k_merge_assemble<<<gm, kMergeThreads, 0, s>>>(w->kept_lin, w->kept_val, m, grown, k, L->in_f,
+                                                  L->v, L->r, L->c, L->col_keys, L->col_vals);
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
-    return build_topology(L, s, false);
+    return build_views(L, s);
 }
 
 int run_prune_regrow(Layer* L, float zeta, uint64_t seed, cudaStream_t s) {

@@ -459,7 +459,6 @@ int build_topology(Layer* L, cudaStream_t s, bool validate) {
     const int64_t n = L->nnz;
     const int T = 256;
     const int64_t bits_lin = bits_for((uint64_t)L->out_f * (uint64_t)L->in_f);
-    const int bits_col = bits_for((uint64_t)L->in_f);
     cudaMemsetAsync(L->status, 0, sizeof(int32_t), s);
 
     if (n > 0) {
@@ -505,6 +504,15 @@ int build_topology(Layer* L, cudaStream_t s, bool validate) {
                 ks, vs, n, L->in_f, L->v, L->r, L->c, L->col_keys, L->col_vals);
         }
     }
+    return build_views(L, s);
+}
+
+// The derived views of a triple that is already in canonical order, with
+// col_keys / col_vals holding (column, canonical slot) of every entry.
+int build_views(Layer* L, cudaStream_t s) {
+    const int64_t n = L->nnz;
+    const int T = 256;
+    const int bits_col = bits_for((uint64_t)L->in_f);
     // CSR row pointer from the canonical rows
     k_fill_ptr<<<grid_for(n + 1, T, L->num_sms), T, 0, s>>>(L->r, n, L->out_f, L->row_ptr);
 
