@@ -56,6 +56,7 @@ constexpr int kGradTile = 1024;            // columns per bitmap tile
 constexpr int kGradDigit = 12;             // digit width of the select passes
 constexpr int kGradBins = 1 << kGradDigit;
 constexpr int kGradWarps = 8;              // warps per block of the gradient passes
+constexpr int kGradDyMax = 64;             // batch sizes whose dY row is kept in shared memory
 
 struct SelState {
     uint32_t mag;
@@ -73,7 +74,7 @@ struct RestructureWs {
     int32_t* scan_tmp = nullptr;
     int64_t scan_tmp_len = 0;
     int32_t* total = nullptr;    // device scalar
-    int64_t* acc = nullptr;      // device scalar: accepted so far
+    int64_t* acc = nullptr;      // device scalars: accepted so far, boundary keys
     uint64_t* kept_lin = nullptr;
     uint32_t* kept_val = nullptr;
     uint64_t* H = nullptr;       // kept-or-accepted hash set (large matrices)
@@ -133,7 +134,7 @@ static int alloc_restructure(Layer* L) {
               cudaMalloc(&w->flags, 2 * fl * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&w->scan_tmp, w->scan_tmp_len * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&w->total, sizeof(int32_t)) == cudaSuccess &&
-              cudaMalloc(&w->acc, sizeof(int64_t)) == cudaSuccess &&
+              cudaMalloc(&w->acc, 2 * sizeof(int64_t)) == cudaSuccess &&
               cudaMalloc(&w->kept_lin, n * sizeof(uint64_t)) == cudaSuccess &&
               cudaMalloc(&w->kept_val, n * sizeof(uint32_t)) == cudaSuccess &&
               (use_bits ? cudaMalloc(&w->bits, (n_pos / 32 + 1) * sizeof(uint32_t))
@@ -362,10 +363,11 @@ __global__ void k_advance(int64_t* acc, const int32_t* total, int64_t k) {
 
 // ---------------------------------------------------------------- gradient grow kernels
 struct GradSel {
-    uint64_t prefix;  // the selected high bits of the k-th smallest key
-    int32_t level;    // how many high key bits are fixed
-    int32_t exact;    // 1 when the selected bin holds exactly the remaining rank
-    int64_t krem;     // rank still to find among keys with that prefix
+    uint64_t prefix;    // the selected high bits of the k-th smallest key
+    int32_t level;      // how many high key bits are fixed
+    int32_t exact;      // 1 when the selected bin holds exactly the remaining rank
+    int64_t krem;       // rank still to find among keys with that prefix
+    int64_t bin_count;  // keys in the selected bin
 };
 
 __global__ void k_grad_init(GradSel* sel, int64_t k) {
@@ -389,12 +391,14 @@ __global__ void k_kept_row_ptr(const uint64_t* __restrict__ kept, int64_t m, int
 // The gradient of position (r, c): the fused multiply-add chain over the
 // batch in order, g = fma(dY[b-1,r], X[b-1,c], ... fma(dY[0,r], X[0,c], 0)).
 // Key: complement of the bit pattern of |g| (high 32 bits), then the position.
-__device__ __forceinline__ uint64_t grad_key(const float* __restrict__ X,
-                                             const float* __restrict__ dY, int b, int64_t out_f,
-                                             int64_t in_f, int64_t r, int64_t c, uint32_t p) {
+// dy holds dY[beta, r] for the row (shared memory when b <= kGradDyMax, else
+// read from global memory with stride out_f).
+__device__ __forceinline__ uint64_t grad_key(const float* __restrict__ X, const float* dy,
+                                             int64_t dy_stride, int b, int64_t in_f, int64_t c,
+                                             uint32_t p) {
     float g = 0.f;
     for (int beta = 0; beta < b; ++beta)
-        g = __fmaf_rn(__ldg(dY + beta * out_f + r), __ldg(X + beta * in_f + c), g);
+        g = __fmaf_rn(dy[beta * dy_stride], __ldg(X + beta * in_f + c), g);
     const uint32_t a = __float_as_uint(g) & 0x7fffffffu;
     return ((uint64_t)(~a) << 32) | (uint64_t)p;
 }
@@ -406,14 +410,24 @@ __device__ __forceinline__ uint64_t grad_key(const float* __restrict__ X,
 //     whose top `level` bits equal the selected prefix.
 //   COLLECT = true: every key whose top `level` bits are <= the prefix is
 //     selected; its position is appended to out_lin (at most cap).
-template <bool COLLECT>
+//   MODE 0: histogram of the digit [shift, shift+width) of the keys whose top
+//     `level` bits equal the selected prefix;
+//   MODE 1: every key whose top bits are <= the prefix is selected (its
+//     position appended to out_lin, at most cap);
+//   MODE 2: keys whose top bits are below the prefix are selected as in
+//     MODE 1, and the full keys of the selected bin (top bits equal) are
+//     appended to bnd_keys (at most bcap) to be sorted.
+template <int MODE>
 __global__ void __launch_bounds__(kGradWarps * 32) k_grad_pass(
     const uint64_t* __restrict__ kept, const int32_t* __restrict__ kept_ptr, int64_t out_f,
     int64_t in_f, const float* __restrict__ X, const float* __restrict__ dY, int b,
     const GradSel* __restrict__ sel, int shift, int width, int32_t* __restrict__ hist,
-    uint64_t* __restrict__ out_lin, int64_t* __restrict__ n_out, int64_t cap, int32_t* err) {
+    uint64_t* __restrict__ out_lin, int64_t* __restrict__ n_out, int64_t cap,
+    uint64_t* __restrict__ bnd_keys, int64_t* __restrict__ n_bnd, int64_t bcap, int32_t* err) {
+    constexpr bool COLLECT = MODE != 0;
     __shared__ int h[COLLECT ? 1 : kGradBins];
     __shared__ uint32_t bm[kGradWarps][kGradTile / 32];
+    __shared__ float dys[kGradWarps][kGradDyMax];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     if (!COLLECT) {
         for (int i = threadIdx.x; i < (1 << width); i += blockDim.x) h[i] = 0;
@@ -427,6 +441,13 @@ __global__ void __launch_bounds__(kGradWarps * 32) k_grad_pass(
         int64_t j = kept_ptr[r];
         const int64_t j_end = kept_ptr[r + 1];
         const uint64_t row0 = (uint64_t)r * (uint64_t)in_f;
+        // the row's dY values, once per row
+        const bool dy_smem = b <= kGradDyMax;
+        if (dy_smem)
+            for (int beta = lane; beta < b; beta += 32) dys[w][beta] = __ldg(dY + beta * out_f + r);
+        __syncwarp();
+        const float* dy = dy_smem ? dys[w] : dY + r;
+        const int64_t dy_stride = dy_smem ? 1 : out_f;
         for (int64_t c0 = 0; c0 < in_f; c0 += kGradTile) {
             const int64_t c1 = min(in_f, c0 + (int64_t)kGradTile);
             bm[w][lane] = 0u;
@@ -444,18 +465,31 @@ __global__ void __launch_bounds__(kGradWarps * 32) k_grad_pass(
                 if (took != 0xffffffffu) break;
             }
             __syncwarp();
-            for (int t = 0; t < kGradTile / 32; ++t) {
+            for (int t = 0; t < kGradTile / 32 && c0 + t * 32 < c1; ++t) {  // warp-uniform
                 const int64_t c = c0 + t * 32 + lane;
-                if (c >= c1) break;
-                if ((bm[w][t] >> lane) & 1u) continue;
-                const uint64_t key = grad_key(X, dY, b, out_f, in_f, r, c, (uint32_t)(row0 + (uint64_t)c));
+                const bool cand = c < c1 && !((bm[w][t] >> lane) & 1u);
+                uint64_t key = 0;
+                if (cand) key = grad_key(X, dy, dy_stride, b, in_f, c, (uint32_t)(row0 + (uint64_t)c));
                 if (!COLLECT) {
-                    if (level == 0 || (key >> (64 - level)) == prefix)
-                        atomicAdd(&h[(uint32_t)(key >> shift) & dmask], 1);
-                } else if ((key >> (64 - level)) <= prefix) {
-                    const unsigned long long i = atomicAdd(reinterpret_cast<unsigned long long*>(n_out), 1ull);
-                    if ((int64_t)i < cap) out_lin[i] = row0 + (uint64_t)c;
-                    else atomicOr(err, kStatLimit);
+                    // lanes that hit the same bin add once, from their lowest lane
+                    int bin = -1;
+                    if (cand && (level == 0 || (key >> (64 - level)) == prefix))
+                        bin = (int)((uint32_t)(key >> shift) & dmask);
+                    const unsigned same = __match_any_sync(0xffffffffu, bin);
+                    if (bin >= 0 && (same & ((1u << lane) - 1u)) == 0) atomicAdd(&h[bin], __popc(same));
+                } else if (cand) {
+                    const uint64_t top = key >> (64 - level);
+                    if (top < prefix || (MODE == 1 && top == prefix)) {
+                        const unsigned long long i =
+                            atomicAdd(reinterpret_cast<unsigned long long*>(n_out), 1ull);
+                        if ((int64_t)i < cap) out_lin[i] = row0 + (uint64_t)c;
+                        else atomicOr(err, kStatLimit);
+                    } else if (MODE == 2 && top == prefix) {
+                        const unsigned long long i =
+                            atomicAdd(reinterpret_cast<unsigned long long*>(n_bnd), 1ull);
+                        if ((int64_t)i < bcap) bnd_keys[i] = key;
+                        else atomicOr(err, kStatLimit);
+                    }
                 }
             }
             __syncwarp();
@@ -466,6 +500,13 @@ __global__ void __launch_bounds__(kGradWarps * 32) k_grad_pass(
         for (int i = threadIdx.x; i < (1 << width); i += blockDim.x)
             if (h[i]) atomicAdd(&hist[i], h[i]);
     }
+}
+
+// out[i] = position (low 32 bits) of the i-th smallest boundary key, i < n
+__global__ void k_take_keys(const uint64_t* __restrict__ keys, int64_t n, uint64_t* __restrict__ out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = keys[i] & 0xffffffffull;
 }
 
 // Pick the digit bin holding the krem-th smallest key; one warp.
@@ -492,6 +533,7 @@ __global__ void k_grad_pick(const int32_t* __restrict__ hist, int width, GradSel
                 sel->level += width;
                 sel->krem = left;
                 sel->exact = (hist[d] == left) ? 1 : 0;
+                sel->bin_count = hist[d];
                 return;
             }
             cum += hist[d];
@@ -678,14 +720,19 @@ static int grow_gradient(Layer* L, int64_t k, const float* X, const float* dY, i
     k_grad_init<<<1, 1, 0, s>>>(sel, k);
     const unsigned G = (unsigned)std::max<int64_t>(
         1, std::min<int64_t>(ceil_div(L->out_f, kGradWarps), (int64_t)L->num_sms * 4));
+    // boundary bins up to this size are sorted instead of refined by more passes
+    // (the radix sort's scratch is sized for nnz keys)
+    const int64_t bcap = std::min<int64_t>(L->nnz, int64_t(1) << 21);
     GradSel h{};
+    bool boundary = false;
     for (int level = 0; level < 64;) {
         const int width = std::min(kGradDigit, 64 - level);
         const int shift = 64 - level - width;
         cudaMemsetAsync(w->ghist, 0, (size_t)(1 << width) * sizeof(int32_t), s);
-        k_grad_pass<false><<<G, kGradWarps * 32, 0, s>>>(w->kept_lin, w->kept_ptr, L->out_f,
-                                                        L->in_f, X, dY, (int)b, sel, shift, width,
-                                                        w->ghist, nullptr, nullptr, 0, w->err);
+        k_grad_pass<0><<<G, kGradWarps * 32, 0, s>>>(w->kept_lin, w->kept_ptr, L->out_f, L->in_f,
+                                                    X, dY, (int)b, sel, shift, width, w->ghist,
+                                                    nullptr, nullptr, 0, nullptr, nullptr, 0,
+                                                    w->err);
         k_grad_pick<<<1, 32, 0, s>>>(w->ghist, width, sel);
         if (cudaMemcpyAsync(&h, sel, sizeof(GradSel), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
             cudaStreamSynchronize(s) != cudaSuccess)
@@ -693,19 +740,45 @@ static int grow_gradient(Layer* L, int64_t k, const float* X, const float* dY, i
         if (h.level != level + width) return SNK_ERR_CUDA;  // rank not found: cannot happen
         level = h.level;
         if (h.exact) break;
+        if (h.bin_count <= bcap && level < 64) {
+            boundary = true;
+            break;
+        }
     }
-    cudaMemsetAsync(w->acc, 0, sizeof(int64_t), s);
-    k_grad_pass<true><<<G, kGradWarps * 32, 0, s>>>(w->kept_lin, w->kept_ptr, L->out_f, L->in_f,
-                                                   X, dY, (int)b, sel, 0, 1, nullptr, w->new_lin,
-                                                   w->acc, k, w->err);
-    int64_t got = 0;
+    int64_t* n_bnd = w->acc + 1;
+    cudaMemsetAsync(w->acc, 0, 2 * sizeof(int64_t), s);
+    if (!boundary) {
+        k_grad_pass<1><<<G, kGradWarps * 32, 0, s>>>(w->kept_lin, w->kept_ptr, L->out_f, L->in_f,
+                                                    X, dY, (int)b, sel, 0, 1, nullptr, w->new_lin,
+                                                    w->acc, k, nullptr, nullptr, 0, w->err);
+    } else {
+        // keys below the selected bin are in; the bin itself is sorted and
+        // its first krem keys are in
+        k_grad_pass<2><<<G, kGradWarps * 32, 0, s>>>(w->kept_lin, w->kept_ptr, L->out_f, L->in_f,
+                                                    X, dY, (int)b, sel, 0, 1, nullptr, w->new_lin,
+                                                    w->acc, k - h.krem, w->cand, n_bnd, bcap,
+                                                    w->err);
+        bool flipped = false;
+        int st = sort_pairs_u64(w->cand, reinterpret_cast<uint32_t*>(w->flags), w->R_key,
+                                reinterpret_cast<uint32_t*>(w->flags + w->flag_half), h.bin_count,
+                                64 - h.level, L->tile_hist, L->tile_hist_len, s, &flipped);
+        if (st != SNK_OK) return st;
+        k_take_keys<<<grid_of(h.krem, L->num_sms), 256, 0, s>>>(flipped ? w->R_key : w->cand,
+                                                                h.krem,
+                                                                w->new_lin + (k - h.krem));
+    }
+    int64_t got[2] = {0, 0};
     int32_t h_err = 0;
-    if (cudaMemcpyAsync(&got, w->acc, sizeof(int64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+    if (cudaMemcpyAsync(got, w->acc, 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
         cudaMemcpyAsync(&h_err, w->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
             cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return SNK_ERR_CUDA;
-    if (h_err || got != k) return SNK_ERR_CUDA;  // keys are unique: exactly k are selected
+    // keys are unique: exactly k are selected
+    if (h_err) return SNK_ERR_CUDA;
+    if (!boundary && got[0] != k) return SNK_ERR_CUDA;
+    if (boundary && (got[0] != k - h.krem || got[1] != h.bin_count)) return SNK_ERR_CUDA;
     return SNK_OK;
 }
 
