@@ -60,7 +60,7 @@ constexpr int kGradDyMax = 64;             // batch sizes whose dY row is kept i
 
 struct SelState {
     uint32_t mag;
-    uint32_t pad;
+    uint32_t done;   // 1 once every entry of the selected magnitude is known to go
     uint64_t lin;
     int64_t krem;
 };
@@ -211,7 +211,7 @@ __device__ __forceinline__ bool hi_match(uint64_t x, uint64_t y, int s) {
 // ---------------------------------------------------------------- prune kernels
 __global__ void k_sel_init(SelState* sel, int64_t k) {
     sel->mag = 0;
-    sel->pad = 0;
+    sel->done = 0;
     sel->lin = 0;
     sel->krem = k;
 }
@@ -223,6 +223,7 @@ __global__ void k_sel_hist(const float* __restrict__ v, const int32_t* __restric
                            const int32_t* __restrict__ c, int64_t n, int64_t in_f,
                            const SelState* __restrict__ sel, int phase, int shift,
                            int32_t* __restrict__ hist) {
+    if (phase == 1 && sel->done) return;  // no tie on the magnitude to break
     __shared__ int h[256];
     for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
     __syncthreads();
@@ -245,6 +246,7 @@ __global__ void k_sel_hist(const float* __restrict__ v, const int32_t* __restric
 
 __global__ void k_sel_pick(const int32_t* __restrict__ hist, SelState* sel, int phase, int shift) {
     if (threadIdx.x != 0) return;
+    if (phase == 1 && sel->done) return;
     int64_t cum = 0;
     const int64_t krem = sel->krem;
     for (int d = 0; d < 256; ++d) {
@@ -252,6 +254,12 @@ __global__ void k_sel_pick(const int32_t* __restrict__ hist, SelState* sel, int 
             if (phase == 0) sel->mag |= (uint32_t)d << shift;
             else sel->lin |= (uint64_t)d << shift;
             sel->krem = krem - cum;
+            // the last magnitude digit: if every entry of this magnitude goes,
+            // no position is needed to break a tie (every position passes)
+            if (phase == 0 && shift == 0 && hist[d] == krem - cum) {
+                sel->done = 1;
+                sel->lin = ~0ull;
+            }
             return;
         }
         cum += hist[d];
@@ -553,21 +561,28 @@ constexpr int kMergePer = 8;
 constexpr int kMergeTile = kMergeThreads * kMergePer;
 
 // number of kept entries among the first d outputs of the merge
+template <typename KG>
 __device__ __forceinline__ int64_t merge_split(const uint64_t* __restrict__ a, int64_t m,
-                                               const uint64_t* __restrict__ b, int64_t k,
-                                               int64_t d) {
+                                               const KG* __restrict__ b, int64_t k, int64_t d) {
     int64_t lo = d > k ? d - k : 0, hi = d < m ? d : m;
     while (lo < hi) {
         const int64_t mid = (lo + hi) >> 1;
-        if (a[mid] < b[d - mid - 1]) lo = mid + 1;
+        if (a[mid] < (uint64_t)b[d - mid - 1]) lo = mid + 1;
         else hi = mid;
     }
     return lo;
 }
 
+__global__ void k_narrow_u32(const uint64_t* __restrict__ a, int64_t n, uint32_t* __restrict__ o) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        o[i] = (uint32_t)a[i];
+}
+
+template <typename KG>
 __global__ void __launch_bounds__(kMergeThreads) k_merge_assemble(
     const uint64_t* __restrict__ kept_lin, const uint32_t* __restrict__ kept_val, int64_t m,
-    const uint64_t* __restrict__ new_lin, int64_t k, int64_t in_f, float* __restrict__ v,
+    const KG* __restrict__ new_lin, int64_t k, int64_t in_f, float* __restrict__ v,
     int32_t* __restrict__ r, int32_t* __restrict__ c, uint32_t* __restrict__ col_key,
     uint32_t* __restrict__ col_val) {
     __shared__ uint64_t sa[kMergeTile], sb[kMergeTile];
@@ -585,7 +600,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_assemble(
             sa[x] = kept_lin[i0 + x];
             sv[x] = kept_val[i0 + x];
         }
-        for (int x = threadIdx.x; x < nb; x += kMergeThreads) sb[x] = new_lin[j0 + x];
+        for (int x = threadIdx.x; x < nb; x += kMergeThreads) sb[x] = (uint64_t)new_lin[j0 + x];
         __syncthreads();
         // this thread's outputs: [d0, d1) within the tile
         const int d0 = min(na + nb, threadIdx.x * kMergePer);
@@ -597,16 +612,34 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_assemble(
             else hi = mid;
         }
         int ia = lo, ib = d0 - lo;
-        for (int d = d0; d < d1; ++d) {
-            const bool take_a = ib >= nb || (ia < na && sa[ia] < sb[ib]);
-            const uint64_t lin = take_a ? sa[ia] : sb[ib];
-            const uint32_t val = take_a ? sv[ia] : 0u;
-            if (take_a) ++ia;
-            else ++ib;
-            const int64_t pos = t0 + d;
+        uint64_t ml[kMergePer];
+        uint32_t mv[kMergePer];
+#pragma unroll
+        for (int q = 0; q < kMergePer; ++q) {
+            if (d0 + q < d1) {
+                const bool take_a = ib >= nb || (ia < na && sa[ia] < sb[ib]);
+                ml[q] = take_a ? sa[ia] : sb[ib];
+                mv[q] = take_a ? sv[ia] : 0u;
+                if (take_a) ++ia;
+                else ++ib;
+            }
+        }
+        __syncthreads();  // every thread has read its inputs: reuse sa / sv for the output
+#pragma unroll
+        for (int q = 0; q < kMergePer; ++q) {
+            if (d0 + q < d1) {
+                sa[d0 + q] = ml[q];
+                sv[d0 + q] = mv[q];
+            }
+        }
+        __syncthreads();
+        // coalesced write of the merged tile
+        for (int x = threadIdx.x; x < na + nb; x += kMergeThreads) {
+            const uint64_t lin = sa[x];
+            const int64_t pos = t0 + x;
             const uint64_t rr = lin / (uint64_t)in_f;
             const int32_t cc = (int32_t)(lin - rr * (uint64_t)in_f);
-            v[pos] = __uint_as_float(val);
+            v[pos] = __uint_as_float(sv[x]);
             r[pos] = (int32_t)rr;
             c[pos] = cc;
             col_key[pos] = (uint32_t)cc;
@@ -788,17 +821,31 @@ static int grow_gradient(Layer* L, int64_t k, const float* X, const float* dY, i
 static int assemble(Layer* L, int64_t k, cudaStream_t s) {
     RestructureWs* w = L->rws;
     const int64_t m = L->nnz - k;
-    bool flipped = false;
-    int st = sort_pairs_u64(w->new_lin, reinterpret_cast<uint32_t*>(w->flags), w->cand,
-                            reinterpret_cast<uint32_t*>(w->flags + w->flag_half), k,
-                            bits_for((uint64_t)L->out_f * (uint64_t)L->in_f), L->tile_hist,
-                            L->tile_hist_len, s, &flipped);
-    if (st != SNK_OK) return st;
-    const uint64_t* grown = flipped ? w->cand : w->new_lin;
+    const uint64_t n_pos = (uint64_t)L->out_f * (uint64_t)L->in_f;
     const unsigned gm = (unsigned)std::max<int64_t>(
         1, std::min<int64_t>(ceil_div(L->nnz, kMergeTile), (int64_t)L->num_sms * 8));
-    k_merge_assemble<<<gm, kMergeThreads, 0, s>>>(w->kept_lin, w->kept_val, m, grown, k, L->in_f,
-                                                  L->v, L->r, L->c, L->col_keys, L->col_vals);
+    bool flipped = false;
+    uint32_t* vals = reinterpret_cast<uint32_t*>(w->flags);
+    uint32_t* vals_alt = reinterpret_cast<uint32_t*>(w->flags + w->flag_half);
+    int st;
+    if (n_pos <= (1ull << 32)) {
+        // positions fit 32 bits: sort them as such (half the bytes moved)
+        uint32_t* k32 = reinterpret_cast<uint32_t*>(w->cand);  // 2 * cand_cap words
+        k_narrow_u32<<<grid_of(k, L->num_sms), 256, 0, s>>>(w->new_lin, k, k32);
+        st = sort_pairs_u32(k32, vals, k32 + w->cand_cap, vals_alt, k, bits_for(n_pos),
+                            L->tile_hist, L->tile_hist_len, s, &flipped);
+        if (st != SNK_OK) return st;
+        k_merge_assemble<uint32_t><<<gm, kMergeThreads, 0, s>>>(
+            w->kept_lin, w->kept_val, m, flipped ? k32 + w->cand_cap : k32, k, L->in_f, L->v,
+            L->r, L->c, L->col_keys, L->col_vals);
+    } else {
+        st = sort_pairs_u64(w->new_lin, vals, w->cand, vals_alt, k, bits_for(n_pos), L->tile_hist,
+                            L->tile_hist_len, s, &flipped);
+        if (st != SNK_OK) return st;
+        k_merge_assemble<uint64_t><<<gm, kMergeThreads, 0, s>>>(
+            w->kept_lin, w->kept_val, m, flipped ? w->cand : w->new_lin, k, L->in_f, L->v, L->r,
+            L->c, L->col_keys, L->col_vals);
+    }
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     return build_views(L, s);
 }
