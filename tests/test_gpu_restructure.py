@@ -53,6 +53,21 @@ def test_prune_regrow_bit_exact(torch, out_f, in_f, sp, zeta, seed):
     g.close()
 
 
+@pytest.mark.parametrize("out_f,in_f,nnz", [
+    (70_000, 70_000, 60_000),     # 4.9e9 positions: hash set for held positions, 64-bit sort
+    (40_000, 60_000, 50_000),     # 2.4e9 positions: hash set, 32-bit sort of grown positions
+])
+def test_prune_regrow_large_position_space(torch, out_f, in_f, nnz):
+    """Layers with more than 2^31 positions take the hash-set path for held
+    positions (and above 2^32 the 64-bit sort of the grown ones)."""
+    r, c = synth.uniform_support(out_f, in_f, nnz, 61)
+    lay = synth.Layer(out_f, in_f, synth.normal(nnz, 0.05, 62), r, c)
+    g = make_gpu_layer(torch, lay)
+    for i in range(2):
+        restructure_and_compare(torch, g, out_f, in_f, 0.3, 0x5E7 + i)
+    g.close()
+
+
 def test_ties_zeros_and_signed_zero(torch):
     out_f, in_f = 60, 70
     lay = synth.make_layer(out_f, in_f, 80, 1.0, 8, 9)
