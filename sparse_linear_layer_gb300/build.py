@@ -61,13 +61,24 @@ def _compile(src: str, verbose: bool, obj_dir: str, extra) -> str:
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None, out: str | None = None) -> str:
     """Compile libsnk.so.  extra_flags (e.g. ["-DSNK_PIPE_FWD=3"]) and out
-    (another library path) build a variant beside the default library."""
+    (another library path) build a variant beside the default library.
+    Processes that build at the same time (one per GPU) take turns on a lock
+    file; the later ones then find the library up to date."""
+    import fcntl
     extra = list(extra_flags or [])
     lib = out or LIB
     if not force and not extra and out is None and up_to_date():
         return LIB
     obj_dir = OBJ if out is None else out + ".objs"
     os.makedirs(obj_dir, exist_ok=True)
+    with open(os.path.join(obj_dir, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not extra and out is None and up_to_date():
+            return LIB
+        return _build_locked(verbose, extra, lib, obj_dir)
+
+
+def _build_locked(verbose: bool, extra, lib: str, obj_dir: str) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose, obj_dir, extra), srcs))
