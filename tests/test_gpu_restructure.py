@@ -220,6 +220,8 @@ def gradient_restructure_and_compare(torch, g, out_f, in_f, zeta, X, dY):
     (768, 3072, 90, 0.3, 4, 1.2),     # GPT-2 MLP shape, Zipf rows
     (3072, 768, 99, 0.5, 2, 1.2),
     (10, 10, 10, 0.9, 2, None),       # nearly full: the whole complement is grown
+    (200, 300, 90, 0.3, 70, None),    # batch above 64: dY rows read from global memory
+    (400, 250, 95, 0.4, 1, None),     # batch 1: the gradient is one rounded product
 ])
 def test_prune_regrow_gradient_bit_exact(torch, out_f, in_f, sp, zeta, b, zipf):
     lay = synth.make_layer(out_f, in_f, sp, 0.05, 5, 6, zipf_s=zipf)
