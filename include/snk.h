@@ -90,6 +90,13 @@ typedef struct snk_layer* snk_handle;
  *          step), and must not modify `rows` or `cols`.
  * stream   queue for the build.  The call synchronises the stream before it
  *          returns, so that device-detected errors can be reported.
+ * Device memory taken by the handle: about 52 bytes per stored entry (index
+ *          views, 16-bit copies, sort scratch) plus about 264 bytes per row or
+ *          column of the larger dimension (pointers, arrival counters, and the
+ *          transposed operand copy of the global-memory path, 64 batch columns
+ *          wide); the first snk_prune_regrow adds its own workspace (about 100
+ *          bytes per entry, plus a bitmap of out * in bits when that is at
+ *          most 2^31 bits).
  * Errors:  SNK_ERR_ARG, SNK_ERR_RANGE (an index outside the matrix),
  *          SNK_ERR_DUP (a repeated position), SNK_ERR_OOM, SNK_ERR_CUDA.  On
  *          SNK_ERR_RANGE / SNK_ERR_DUP the caller's arrays are left as given.
