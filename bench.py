@@ -445,8 +445,9 @@ def run_latency(args, dev):
     """Forward latency at batch 1: one call after an L2 flush (cold,
     event-timed); back-to-back direct calls and back-to-back replays of a CUDA
     graph holding one forward call (warm: the layer stays in L2, as in
-    repeated inference; device time per call); and one call at a time, issue
-    to completion on the host clock, direct and as a graph replay."""
+    repeated inference; device time per call); one call at a time, issue
+    to completion on the host clock, direct and as a graph replay; and one
+    cold training step (forward, dX, dW + db), event-timed."""
     import torch
 
     from sparse_linear_layer_gb300 import binding, synth
@@ -504,6 +505,24 @@ def run_latency(args, dev):
             e1.record(torch.cuda.current_stream(dev))
             e1.synchronize()
             replay = e0.elapsed_time(e1) * 1e3 / n
+            # one training step (forward, dX, dW + db) after an L2 flush, for
+            # the pages whose time may cover more than the forward
+            dY = torch.randn(1, out_f, device=dev)
+            dX = torch.empty(1, in_f, device=dev)
+            dW = torch.empty(lay.nnz, device=dev)
+            db = torch.empty(out_f, device=dev)
+            step_cold = []
+            for _ in range(n):
+                if flush is not None:
+                    flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fwd()
+                binding.snk_backward_input(g.handle, dY, dX, stream.cuda_stream)
+                binding.snk_backward_weight(g.handle, X, dY, dW, db, stream.cuda_stream)
+                e1.record(stream)
+                e1.synchronize()
+                step_cold.append(e0.elapsed_time(e1) * 1e3)
             # one call at a time, host wall clock from issue to completion
             sync = {}
             for name, call in (("direct", fwd), ("graph", graph.replay)):
@@ -520,6 +539,7 @@ def run_latency(args, dev):
                    "us_warm_direct": warm, "us_warm_graph_replay": replay,
                    "us_wall_sync_direct_median": sync["direct"],
                    "us_wall_sync_graph_median": sync["graph"],
+                   "us_step_fwd_dx_dw_cold_mean": statistics.mean(step_cold),
                    "pages": pages}
             fo.write(json.dumps(row) + "\n")
             fo.flush()

@@ -48,6 +48,7 @@ constexpr int kStatLimit = 4;
 
 struct RestructureWs;
 struct PcsrState;
+struct TcState;
 
 // Per block: its entry range [k0, k1), and for the segment that enters the
 // block from before (head) and the one that leaves it (tail) the first and
@@ -112,9 +113,20 @@ struct Layer {
 
     RestructureWs* rws = nullptr; // allocated on first prune_regrow
     PcsrState* pcsr = nullptr;    // Padded-CSR view, built on request
+    TcState* tc = nullptr;        // tile-ordered views of the large-batch path, built on first use
 };
 
 void free_pcsr(Layer* L);
+
+// ---- large-batch path on the tensor cores (snk_tc.cu) ---------------------
+bool tc_eligible(const Layer* L, int64_t b);
+// Y[b, n_seg] = D[b, K] times the rows (columns = false) or the columns of W,
+// + bias.  Allocates and builds the tile-ordered view on first use.
+int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias, float* Y,
+           cudaStream_t s);
+int refresh_tc_views(Layer* L, cudaStream_t s);
+void mark_tc_views(Layer* L);
+void free_tc(Layer* L);
 
 // ---- small helpers -------------------------------------------------------
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -528,6 +528,7 @@ static SpmmArgs layer_args(Layer* L, bool columns) {
 
 int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float* Y,
                    cudaStream_t s) {
+    if (tc_eligible(L, b)) return run_tc(L, false, X, b, bias, Y, s);
     SpmmArgs a = layer_args(L, false);
     a.X = X;
     a.bias = bias;
@@ -536,6 +537,7 @@ int launch_forward(Layer* L, const float* X, int64_t b, const float* bias, float
 }
 
 int launch_backward_input(Layer* L, const float* dY, int64_t b, float* dX, cudaStream_t s) {
+    if (tc_eligible(L, b)) return run_tc(L, true, dY, b, nullptr, dX, s);
     SpmmArgs a = layer_args(L, true);
     a.X = dY;
     a.bias = nullptr;

@@ -1,0 +1,808 @@
+// Large-batch products on the tensor cores (tcgen05): Y = X W^T + b and
+// dX = dY W for batches of hundreds of rows and more.
+//
+// "Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks on
+// GPU", appendix Table 13 (GAMLP training at batch 4096): at that batch the
+// per-entry SpMM does b multiply-adds per stored weight and its operand
+// traffic, not the weight stream, sets the time.  Here each 192-row x 64-column
+// tile of the sparse operand is densified in shared memory from its own
+// entries (W never exists densely in device memory) and multiplied on the
+// tensor cores with a 128-row tile of the dense operand.
+//
+// Precision.  fp32 results within 1e-5 * sum|w||x| come from an fp16 split:
+// every operand value x is scaled by a power of two per row (so the row's
+// largest magnitude lands in [2^13, 2^14)), then written as hi = fp16(x) and
+// lo = fp16(x - hi); the products hi*hi + hi*lo + lo*hi carry about 22 bits.
+// The tensor core's fp32 accumulation truncates, so one accumulator is never
+// chained over the whole reduction: two TMEM accumulators take turns, each
+// over kTcPeriod windows, and every finished one is added into fp32 registers
+// (round to nearest) while the other fills.
+//
+// Per call: the dense operand is scaled and split once into fp16 hi/lo
+// arrays (k_tc_split), the values are gathered into tile order (k_tc_gather)
+// and the segment scales found (k_tc_seg_exp).  Then one CTA per 128 x 192
+// output tile, 10 warps:
+//   warps 0-7  build the sparse tile of each window in one of two stages
+//              (clear the positions written two windows ago, then write this
+//              window's entries), drain the accumulators and store the output;
+//   warp 8     loads the dense hi/lo tiles with TMA into one of two stages;
+//   warp 9     issues the MMAs (one thread) and owns the TMEM allocation;
+//   warp 10    stages each window's sparse entries (tile offsets and fp16
+//              pieces, contiguous in tile order) into one of four shared-memory
+//              slots with bulk copies, so the builders never wait on device
+//              memory and only store.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "snk_internal.cuh"
+
+namespace snk {
+
+struct TcView {
+    int32_t* perm_t = nullptr;    // [nnz] canonical slot of the j-th entry in tile order
+    uint16_t* off = nullptr;      // [nnz + pad] byte offset of the entry in its swizzled fp16 tile
+    int32_t* tile_ptr = nullptr;  // [n_tiles + 1] first entry of each (segment tile, window)
+    int64_t n_tiles = 0;
+    int n_win = 0;                // windows along the reduction dimension
+    int n_nt = 0;                 // segment tiles
+    int64_t version = -1;         // topology version the view was built for
+};
+
+struct TcState {
+    TcView view[2];               // [0]: rows of W (forward), [1]: columns of W (dX)
+    uint32_t* hl = nullptr;       // [nnz + pad] scaled values in tile order as fp16 hi | lo << 16 (per call)
+    int32_t* seg_exp = nullptr;   // [max(out, in)] scale exponent per segment
+    int32_t* row_exp = nullptr;   // [kTcChunk] scale exponent per dense row
+    __half* dh = nullptr;         // [kTcChunk * k_stride] dense operand, scaled, high part
+    __half* dl = nullptr;         // the low part
+    int64_t k_stride = 0;         // row stride of dh / dl: max(out, in) rounded up to 8
+};
+
+namespace {
+
+constexpr int kTcM = 128;          // dense rows per tile (TMEM lanes)
+constexpr int kTcN = 192;          // segments per tile (accumulator columns)
+constexpr int kTcK = 64;           // reduction window (128 bytes of fp16)
+constexpr int kTcBuilders = 256;   // warps 0-7
+constexpr int kTcThreads = kTcBuilders + 96;
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kRecWarp = 10;
+constexpr int kStagesA = 2, kStagesB = 2;
+constexpr int kRecSlots = 4;       // windows of sparse entries staged in shared memory
+constexpr int kRecCap = 1536;      // entries staged per window (the rest are read from memory)
+constexpr int kTcPeriod = 8;       // windows per accumulator turn
+constexpr int kTcGroupM = 8;       // dense-row tiles per raster group
+constexpr int kTcChunk = 4096;     // dense rows per launch
+constexpr int kPieceA = kTcM * kTcK * 2;          // 16 KB
+constexpr int kPieceB = kTcN * kTcK * 2;          // 24 KB
+constexpr int kStageA = 2 * kPieceA, kStageB = 2 * kPieceB;
+constexpr int kRecSlotBytes = kRecCap * 2 + kRecCap * 4;          // offsets, then fp16 pieces
+constexpr int kTcSmem = kStagesA * kStageA + kStagesB * kStageB + kRecSlots * kRecSlotBytes + 1024;
+constexpr uint32_t kAccStride = 256;              // TMEM columns between the two accumulators
+constexpr uint32_t kTmemCols = 512;
+constexpr int kColsPerThread = kTcN / 2;          // accumulator columns each builder drains
+constexpr long long kTcWaitCycles = 4000000000LL; // about two seconds
+// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major,
+// N = kTcN, M = kTcM.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+
+static_assert(kTcSmem <= 227 * 1024 - 4096, "pipeline stages exceed shared memory");
+static_assert(kTcN % 64 == 0 && kTcN <= 256, "two builder halves of whole 32-column loads");
+static_assert(kRecCap % 8 == 0, "staged ranges are whole 16-byte units");
+constexpr int kTcPad = 16;         // entries readable past nnz in the tile-order arrays
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Byte offset of fp16 element (row i, column k < 64) in a K-major tile with
+// the 128-byte swizzle: 8-row atoms of 1024 bytes, 16-byte chunks XORed with
+// the row within the atom (the layout a 128-byte-swizzled TMA load writes).
+__device__ __forceinline__ uint32_t sw128(int i, int k) {
+    return (uint32_t)((i >> 3) * 1024 + (i & 7) * 128 + (((k >> 3) ^ (i & 7)) << 4) + (k & 7) * 2);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+                 : "memory");
+}
+// Bounded wait on a phase; false after about two seconds.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+    long long t0 = 0;
+    for (int spin = 0;; ++spin) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(smem_u32(b)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (spin == 0)
+            t0 = clock64();
+        else if (clock64() - t0 > kTcWaitCycles)
+            return false;
+    }
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// OR of a flag over the 256 builder threads (named barrier 1).
+__device__ __forceinline__ bool builders_any(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.cta.red.or.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "n"(kTcBuilders)
+        : "memory");
+    return r != 0;
+}
+
+// Power-of-two exponent that brings the largest magnitude m into [2^13, 2^14).
+__device__ __forceinline__ int tc_exponent(float m) {
+    if (!(m > 0.f) || !isfinite(m)) return 0;
+    int E;
+    frexpf(m, &E);
+    return min(120, max(-120, 14 - E));
+}
+
+// fp16 pieces of one scaled value: hi + lo carries about 22 bits.
+__device__ __forceinline__ void split16(float x, __half& hi, __half& lo) {
+    hi = __float2half_rn(x);
+    lo = __float2half_rn(x - __half2float(hi));
+}
+
+struct TcArgs {
+    int b;                    // dense rows in this launch
+    int64_t K_len;            // reduction length
+    const int32_t* row_exp;   // [b]
+    const uint16_t* off;      // sparse entries in tile order: tile offsets
+    const uint32_t* hl;       // and fp16 pieces
+    const int32_t* tile_ptr;  // [n_nt * n_win + 1]
+    const int32_t* seg_exp;   // [n_seg]
+    int64_t n_seg;
+    int n_win, n_mt, n_nt;
+    const float* bias;        // [n_seg] or null
+    float* Y;                 // [b, n_seg]
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_tc_spmm(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_l,
+              const TcArgs a) {
+    extern __shared__ __align__(1024) unsigned char tc_raw[];
+    unsigned char* sa = tc_raw + ((1024 - (smem_u32(tc_raw) & 1023)) & 1023);  // A stages
+    unsigned char* sb = sa + kStagesA * kStageA;                                // B stages
+    unsigned char* sr = sb + kStagesB * kStageB;                                // staged entries
+    __shared__ uint64_t full_a[kStagesA], empty_a[kStagesA], full_b[kStagesB], empty_b[kStagesB];
+    __shared__ uint64_t rec_full[kRecSlots], rec_empty[kRecSlots];
+    __shared__ uint64_t accf[2], acce[2], fin;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    __shared__ float pw_seg[kTcN];   // 2^e of each segment of the tile
+    // per staging slot: the window's entries [j0, j1), offsets staged from
+    // index ca up to ce, fp16 pieces from va up to ve
+    __shared__ int rec_info[kRecSlots][6];
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    // raster: groups of kTcGroupM dense-row tiles sweep all segment tiles
+    const int id = blockIdx.x;
+    const int gsz = kTcGroupM * a.n_nt;
+    const int first_m = (id / gsz) * kTcGroupM;
+    const int gm = min(a.n_mt - first_m, kTcGroupM);
+    const int mt = first_m + (id % gsz) % gm;
+    const int nt = (id % gsz) / gm;
+    const int64_t r0 = (int64_t)mt * kTcM;    // first dense row
+    const int64_t s0 = (int64_t)nt * kTcN;    // first segment
+    const int n_win = a.n_win;
+    const int32_t* tp = a.tile_ptr + (int64_t)nt * n_win;
+
+    if (t == 0) {
+        for (int i = 0; i < kStagesA; ++i) {
+            mbar_init(&full_a[i], 1);
+            mbar_init(&empty_a[i], 1);
+        }
+        for (int i = 0; i < kStagesB; ++i) {
+            mbar_init(&full_b[i], kTcBuilders);
+            mbar_init(&empty_b[i], 1);
+        }
+        for (int i = 0; i < kRecSlots; ++i) {
+            mbar_init(&rec_full[i], 1);
+            mbar_init(&rec_empty[i], kTcBuilders);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&accf[i], 1);
+            mbar_init(&acce[i], kTcBuilders);
+        }
+        mbar_init(&fin, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (t < kTcN) {
+        const int64_t sg = s0 + t;
+        pw_seg[t] = ldexpf(1.f, sg < a.n_seg ? a.seg_exp[sg] : 0);
+    }
+    // the sparse stages start zeroed; afterwards only written positions are cleared
+    if (t < kTcBuilders) {
+        uint4* pb = reinterpret_cast<uint4*>(sb);
+        for (int i = t; i < kStagesB * kStageB / 16; i += kTcBuilders) pb[i] = make_uint4(0, 0, 0, 0);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    bool ok = true;   // this thread saw no wait run out
+
+    if (warp == kTmaWarp) {
+        // ---------------------------------------------------------------- dense tiles (TMA)
+        if (lane == 0) {
+            for (int w = 0; w < n_win; ++w) {
+                const int s = w % kStagesA;
+                if (w >= kStagesA && !mbar_wait(&empty_a[s], ((w / kStagesA) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* st = sa + s * kStageA;
+                mbar_expect_tx(&full_a[s], kStageA);
+                tma_load_2d(st, &map_h, w * kTcK, (int)r0, &full_a[s]);
+                tma_load_2d(st + kPieceA, &map_l, w * kTcK, (int)r0, &full_a[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kRecWarp) {
+        // ---------------------------------------------------------------- sparse entries (bulk copies)
+        if (lane == 0) {
+            for (int w = 0; w < n_win; ++w) {
+                const int r = w % kRecSlots;
+                if (w >= kRecSlots && !mbar_wait(&rec_empty[r], ((w / kRecSlots) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int j0 = tp[w], j1 = tp[w + 1];
+                const int ca = j0 & ~7, ce = j1 > j0 ? min((j1 + 7) & ~7, ca + kRecCap) : ca;
+                const int va = j0 & ~3, ve = j1 > j0 ? min((j1 + 3) & ~3, va + kRecCap) : va;
+                int* info = rec_info[r];
+                info[0] = j0;
+                info[1] = j1;
+                info[2] = ca;
+                info[3] = ce;
+                info[4] = va;
+                info[5] = ve;
+                const uint32_t bc = (uint32_t)(ce - ca) * 2, bv = (uint32_t)(ve - va) * 4;
+                unsigned char* slot = sr + r * kRecSlotBytes;
+                mbar_expect_tx(&rec_full[r], bc + bv);
+                if (bc) bulk_load(slot, a.off + ca, bc, &rec_full[r]);
+                if (bv) bulk_load(slot + kRecCap * 2, a.hl + va, bv, &rec_full[r]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            for (int w = 0; w < n_win; ++w) {
+                const int s_a = w % kStagesA, s_b = w % kStagesB;
+                const int q = w / kTcPeriod, ab = q & 1;
+                const bool first = (w % kTcPeriod) == 0;
+                if (!mbar_wait(&full_a[s_a], (w / kStagesA) & 1) ||
+                    !mbar_wait(&full_b[s_b], (w / kStagesB) & 1) ||
+                    (first && q >= 2 && !mbar_wait(&acce[ab], ((q >> 1) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ah = smem_u32(sa + s_a * kStageA), al = ah + kPieceA;
+                const uint32_t bh = smem_u32(sb + s_b * kStageB), bl = bh + kPieceB;
+                const uint32_t d = tmem + ab * kAccStride;
+#pragma unroll
+                for (int kk = 0; kk < kTcK / 16; ++kk) {
+                    const uint32_t o = 32 * kk;
+                    mma_f16(d, desc_sw128(ah + o), desc_sw128(bh + o), (first && kk == 0) ? 0u : 1u);
+                    mma_f16(d, desc_sw128(ah + o), desc_sw128(bl + o), 1u);
+                    mma_f16(d, desc_sw128(al + o), desc_sw128(bh + o), 1u);
+                }
+                if (w + kStagesA < n_win) mma_commit(&empty_a[s_a]);
+                if (w + kStagesB < n_win) mma_commit(&empty_b[s_b]);
+                if ((w % kTcPeriod) == kTcPeriod - 1 || w == n_win - 1) mma_commit(&accf[ab]);
+            }
+            // every MMA issued has completed once fin completes
+            mma_commit(&fin);
+            if (!mbar_wait(&fin, 0)) ok = false;
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- builders
+        const int lq = warp & 3;         // TMEM lane quarter this warp may read
+        const int half = warp >> 2;      // accumulator columns [half * kColsPerThread, ...)
+        float acc[kColsPerThread];
+#pragma unroll
+        for (int j = 0; j < kColsPerThread; ++j) acc[j] = 0.f;
+        const int n_per = (n_win + kTcPeriod - 1) / kTcPeriod;
+        int drained = 0;
+        // add accumulator turn q into the registers and hand the accumulator back;
+        // the whole warp reads TMEM or none of it does
+        auto drain = [&](int q) {
+            const int ab = q & 1;
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&accf[ab], (q >> 1) & 1));
+            if (!got) return false;
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + ab * kAccStride + kColsPerThread * half;
+#pragma unroll
+            for (int c = 0; c < kColsPerThread / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(ta + 32 * c, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[32 * c + i] += __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(&acce[ab]);
+            return true;
+        };
+        for (int w = 0; w < n_win; ++w) {
+            const int s = w % kStagesB, r = w % kRecSlots;
+            if (w >= kStagesB && !mbar_wait(&empty_b[s], ((w / kStagesB) - 1) & 1)) ok = false;
+            // turn q is complete once window (q+1)P - 1 has left its stage
+            if (drained < n_per && w == (drained + 1) * kTcPeriod + kStagesB - 1) {
+                if (!drain(drained)) ok = false;
+                ++drained;
+            }
+            if (!mbar_wait(&rec_full[r], (w / kRecSlots) & 1)) ok = false;
+            unsigned char* Bh = sb + s * kStageB;
+            unsigned char* Bl = Bh + kPieceB;
+            if (w >= kStagesB && ok) {
+                // clear what window w - kStagesB wrote into this stage, then
+                // release its staging slot
+                const int ro = (w - kStagesB) % kRecSlots;
+                const int* info = rec_info[ro];
+                const uint16_t* sc = reinterpret_cast<const uint16_t*>(sr + ro * kRecSlotBytes);
+                const int j1 = info[1], ca = info[2], ce = info[3];
+                for (int j = info[0] + t; j < j1; j += kTcBuilders) {
+                    const uint32_t off = j < ce ? sc[j - ca] : a.off[j];
+                    *reinterpret_cast<uint16_t*>(Bh + off) = 0;
+                    *reinterpret_cast<uint16_t*>(Bl + off) = 0;
+                }
+                mbar_arrive(&rec_empty[ro]);
+            }
+            // every clear lands before this window's writes; a wait that ran
+            // out anywhere stops all builders here
+            if (builders_any(!ok)) {
+                ok = false;
+                break;
+            }
+            {
+                const int* info = rec_info[r];
+                const unsigned char* slot = sr + r * kRecSlotBytes;
+                const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot);
+                const uint32_t* sv = reinterpret_cast<const uint32_t*>(slot + kRecCap * 2);
+                const int j1 = info[1], ca = info[2], ce = info[3], va = info[4], ve = info[5];
+                for (int j = info[0] + t; j < j1; j += kTcBuilders) {
+                    const uint32_t off = j < ce ? sc[j - ca] : a.off[j];
+                    const uint32_t v = j < ve ? sv[j - va] : a.hl[j];
+                    *reinterpret_cast<uint16_t*>(Bh + off) = (uint16_t)(v & 0xFFFFu);
+                    *reinterpret_cast<uint16_t*>(Bl + off) = (uint16_t)(v >> 16);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&full_b[s]);
+        }
+        while (ok && drained < n_per) {
+            ok = drain(drained);
+            ++drained;
+        }
+        // ---------------------------------------------------------------- epilogue
+        const int row = 32 * lq + lane;
+        const int64_t rr = r0 + row;
+        if (rr < a.b) {
+            // undo the two power-of-two scalings (each factor a normal float)
+            const float ir = ok ? ldexpf(1.f, -a.row_exp[rr]) : __int_as_float(0x7fc00000);
+            float* yrow = a.Y + rr * a.n_seg;
+            const int c0 = kColsPerThread * half;
+#pragma unroll
+            for (int j = 0; j < kColsPerThread; ++j) {
+                const int64_t sg = s0 + c0 + j;
+                if (sg < a.n_seg) {
+                    float y = (acc[j] * ir) * __frcp_rn(pw_seg[c0 + j]);
+                    if (a.bias) y += a.bias[sg];
+                    yrow[sg] = y;
+                }
+            }
+        }
+    }
+    if (!ok) atomicExch(&abort_flag, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag && t == 0) atomicOr(a.status, kStatLimit);
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// Dense operand, once per call: per row the scale exponent, and the scaled
+// values split into fp16 hi / lo at row stride ks (one block per row).
+template <bool VEC>
+__global__ void k_tc_split(const float* __restrict__ D, int64_t len, int64_t ks, int32_t* __restrict__ e_out,
+                           __half* __restrict__ dh, __half* __restrict__ dl) {
+    __shared__ float red[32];
+    const int64_t r = blockIdx.x;
+    const float* p = D + r * len;
+    float m = 0.f;
+    if (VEC) {
+        for (int64_t k = 4 * threadIdx.x; k < len; k += 4 * blockDim.x) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p + k));
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+    } else {
+        for (int64_t k = threadIdx.x; k < len; k += blockDim.x) m = fmaxf(m, fabsf(p[k]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (threadIdx.x == 0) red[0] = m;
+    }
+    __syncthreads();
+    const int e = tc_exponent(red[0]);
+    if (threadIdx.x == 0) e_out[r] = e;
+    const float pw = ldexpf(1.f, e);
+    __half* oh = dh + r * ks;
+    __half* ol = dl + r * ks;
+    if (VEC) {
+        for (int64_t k = 4 * threadIdx.x; k < len; k += 4 * blockDim.x) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p + k));
+            __half h0, h1, h2, h3, l0, l1, l2, l3;
+            split16(v.x * pw, h0, l0);
+            split16(v.y * pw, h1, l1);
+            split16(v.z * pw, h2, l2);
+            split16(v.w * pw, h3, l3);
+            uint2 hh, ll;
+            hh.x = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+            hh.y = (uint32_t)__half_as_ushort(h2) | ((uint32_t)__half_as_ushort(h3) << 16);
+            ll.x = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+            ll.y = (uint32_t)__half_as_ushort(l2) | ((uint32_t)__half_as_ushort(l3) << 16);
+            *reinterpret_cast<uint2*>(oh + k) = hh;
+            *reinterpret_cast<uint2*>(ol + k) = ll;
+        }
+    } else {
+        for (int64_t k = threadIdx.x; k < len; k += blockDim.x) {
+            __half h, l;
+            split16(p[k] * pw, h, l);
+            oh[k] = h;
+            ol[k] = l;
+        }
+    }
+}
+
+// ------------------------------------------------------------ per-call passes
+// Scale exponent of each segment (row of W, or column through perm).
+__global__ void k_tc_seg_exp(const int32_t* __restrict__ ptr, const float* __restrict__ v,
+                             const int32_t* __restrict__ perm, int64_t n_seg, int32_t* __restrict__ e) {
+    const int lane = threadIdx.x & 31;
+    for (int64_t sg = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; sg < n_seg;
+         sg += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        float m = 0.f;
+        for (int k = ptr[sg] + lane; k < ptr[sg + 1]; k += 32)
+            m = fmaxf(m, fabsf(perm ? v[perm[k]] : v[k]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) e[sg] = tc_exponent(m);
+    }
+}
+
+// The values in tile order, scaled by their segment's power of two and
+// split into fp16 hi | lo << 16 (seg_of: rows for W's rows, cols for its
+// columns).
+__global__ void k_tc_values(const float* __restrict__ v, const int32_t* __restrict__ perm_t,
+                            const int32_t* __restrict__ seg_of, const int32_t* __restrict__ seg_exp, int64_t n,
+                            uint32_t* __restrict__ hl) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t k = perm_t[j];
+        __half h, l;
+        split16(v[k] * ldexpf(1.f, seg_exp[seg_of[k]]), h, l);
+        hl[j] = (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(l) << 16);
+    }
+}
+
+// ------------------------------------------------------------ view build
+__global__ void k_tc_keys(const int32_t* __restrict__ r, const int32_t* __restrict__ c, int64_t n,
+                          bool columns, int n_win, uint32_t* __restrict__ keys,
+                          uint32_t* __restrict__ vals) {
+    for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n;
+         k += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t sg = columns ? c[k] : r[k];
+        const int32_t kk = columns ? r[k] : c[k];
+        keys[k] = (uint32_t)(sg / kTcN) * (uint32_t)n_win + (uint32_t)(kk / kTcK);
+        vals[k] = (uint32_t)k;
+    }
+}
+
+// From the entries sorted by tile: their canonical slots, their byte offsets
+// in the swizzled fp16 tile, and the first entry of every tile (empty tiles
+// included).
+__global__ void k_tc_finish(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals,
+                            int64_t n, int64_t n_tiles, const int32_t* __restrict__ r,
+                            const int32_t* __restrict__ c, bool columns, int32_t* __restrict__ perm_t,
+                            uint16_t* __restrict__ off, int32_t* __restrict__ tile_ptr) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j <= n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        if (j < n) {
+            const uint32_t k = vals[j];
+            perm_t[j] = (int32_t)k;
+            const int32_t sg = columns ? c[k] : r[k];
+            const int32_t kk = columns ? r[k] : c[k];
+            off[j] = (uint16_t)sw128(sg % kTcN, kk % kTcK);
+        }
+        const int64_t lo = j == 0 ? 0 : (int64_t)keys[j - 1] + 1;
+        const int64_t hi = j == n ? n_tiles : (int64_t)keys[j];
+        for (int64_t tt = lo; tt <= hi; ++tt) tile_ptr[tt] = (int32_t)j;
+    }
+}
+
+int grid_for(int64_t n, int threads, int num_sms) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(n, threads), (int64_t)num_sms * 8));
+}
+
+int bits_of(uint64_t n_values) {
+    int b = 0;
+    while (b < 64 && (n_values - 1) >> b) ++b;
+    return b;
+}
+
+template <typename T>
+bool tc_alloc(T** p, int64_t count) {
+    if (cudaMalloc((void**)p, (size_t)std::max<int64_t>(count, 1) * sizeof(T)) != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return false;
+    }
+    return true;
+}
+
+void tc_shape(const Layer* L, bool columns, int64_t* n_seg, int64_t* k_len) {
+    *n_seg = columns ? L->in_f : L->out_f;
+    *k_len = columns ? L->out_f : L->in_f;
+}
+
+int build_view(Layer* L, bool columns, cudaStream_t s) {
+    TcView& V = L->tc->view[columns ? 1 : 0];
+    int64_t n_seg, k_len;
+    tc_shape(L, columns, &n_seg, &k_len);
+    const int64_t n = L->nnz;
+    if (!V.perm_t) {
+        V.n_win = (int)ceil_div(k_len, kTcK);
+        V.n_nt = (int)ceil_div(n_seg, kTcN);
+        V.n_tiles = (int64_t)V.n_win * V.n_nt;
+        if (!tc_alloc(&V.perm_t, n) || !tc_alloc(&V.off, n + kTcPad) || !tc_alloc(&V.tile_ptr, V.n_tiles + 1))
+            return SNK_ERR_OOM;
+    }
+    const int T = 256;
+    uint32_t* ck = L->col_keys;
+    uint32_t* cv = L->col_vals;
+    k_tc_keys<<<grid_for(n, T, L->num_sms), T, 0, s>>>(L->r, L->c, n, columns, V.n_win, ck, cv);
+    bool flipped = false;
+    int st = sort_pairs_u32(ck, cv, ck + n, cv + n, n, bits_of((uint64_t)V.n_tiles), L->tile_hist,
+                            L->tile_hist_len, s, &flipped);
+    if (st != SNK_OK) return st;
+    k_tc_finish<<<grid_for(n + 1, T, L->num_sms), T, 0, s>>>(flipped ? ck + n : ck, flipped ? cv + n : cv, n,
+                                                             V.n_tiles, L->r, L->c, columns, V.perm_t,
+                                                             V.off, V.tile_ptr);
+    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+}
+
+// Which path: SNK_LARGE_BATCH=on|off forces it (tests); otherwise batches of
+// kTcMinBatch rows and more at density 1 / kTcDensityDiv and above.
+constexpr int64_t kTcMinBatch = 256;
+constexpr int64_t kTcDensityDiv = 100;
+
+}  // namespace
+
+bool tc_eligible(const Layer* L, int64_t b) {
+    if (L->nnz == 0) return false;
+    const int64_t n_tiles =
+        ceil_div(L->out_f, kTcN) * ceil_div(L->in_f, kTcK) + ceil_div(L->in_f, kTcN) * ceil_div(L->out_f, kTcK);
+    if (n_tiles > INT32_MAX / 2) return false;
+    const char* f = getenv("SNK_LARGE_BATCH");
+    if (f && strcmp(f, "off") == 0) return false;
+    if (f && strcmp(f, "on") == 0) return true;
+    return b >= kTcMinBatch && L->nnz * kTcDensityDiv >= L->out_f * L->in_f;
+}
+
+void free_tc(Layer* L) {
+    if (!L->tc) return;
+    TcState* T = L->tc;
+    void* ptrs[] = {T->view[0].perm_t, T->view[0].off, T->view[0].tile_ptr, T->view[1].perm_t,
+                    T->view[1].off, T->view[1].tile_ptr, T->hl, T->seg_exp, T->row_exp, T->dh, T->dl};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+    delete T;
+    L->tc = nullptr;
+}
+
+// Rebuild the views that exist, from a new canonical triple; the caller
+// marks them current once it has advanced the topology version.
+int refresh_tc_views(Layer* L, cudaStream_t s) {
+    if (!L->tc) return SNK_OK;
+    for (int d = 0; d < 2; ++d)
+        if (L->tc->view[d].perm_t) {
+            int st = build_view(L, d == 1, s);
+            if (st != SNK_OK) return st;
+        }
+    return SNK_OK;
+}
+
+void mark_tc_views(Layer* L) {
+    if (!L->tc) return;
+    for (int d = 0; d < 2; ++d)
+        if (L->tc->view[d].perm_t) L->tc->view[d].version = L->topology_version;
+}
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, resolved once through the runtime.
+EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        cudaGetLastError();
+    }
+    return fn;
+}
+
+// fp16 [rows][len] at row stride ks, loaded in 64 x 128 boxes with the
+// 128-byte swizzle; reads past len or rows come back as zeros.
+bool encode_map(CUtensorMap* map, __half* base, int64_t len, int64_t rows, int64_t ks) {
+    EncodeTiledFn fn = encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)len, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ks * sizeof(__half)};
+    cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcM};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias, float* Y,
+           cudaStream_t s) {
+    if (!L->tc) {
+        TcState* T = new TcState();
+        L->tc = T;
+        T->k_stride = ceil_div(std::max(L->out_f, L->in_f), 8) * 8;
+        if (!tc_alloc(&T->hl, L->nnz + kTcPad) || !tc_alloc(&T->seg_exp, std::max(L->out_f, L->in_f)) ||
+            !tc_alloc(&T->row_exp, kTcChunk) || !tc_alloc(&T->dh, kTcChunk * T->k_stride) ||
+            !tc_alloc(&T->dl, kTcChunk * T->k_stride)) {
+            free_tc(L);
+            return SNK_ERR_OOM;
+        }
+    }
+    TcState* T = L->tc;
+    TcView& V = T->view[columns ? 1 : 0];
+    if (V.version != L->topology_version) {
+        int st = build_view(L, columns, s);
+        if (st != SNK_OK) return st;
+        V.version = L->topology_version;
+    }
+    int64_t n_seg, k_len;
+    tc_shape(L, columns, &n_seg, &k_len);
+    const int TH = 256;
+    k_tc_seg_exp<<<grid_for(n_seg * 32, TH, L->num_sms), TH, 0, s>>>(
+        columns ? L->col_ptr : L->row_ptr, L->v, columns ? L->perm : nullptr, n_seg, T->seg_exp);
+    k_tc_values<<<grid_for(L->nnz, TH, L->num_sms), TH, 0, s>>>(L->v, V.perm_t, columns ? L->c : L->r,
+                                                                T->seg_exp, L->nnz, T->hl);
+    if (cudaFuncSetAttribute(k_tc_spmm, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
+        return SNK_ERR_CUDA;
+    const bool vec = (k_len % 4) == 0 && ((uintptr_t)D & 15) == 0;
+    for (int64_t c0 = 0; c0 < b; c0 += kTcChunk) {
+        const int bc = (int)std::min<int64_t>(kTcChunk, b - c0);
+        const float* Dc = D + c0 * k_len;
+        if (vec)
+            k_tc_split<true><<<bc, TH, 0, s>>>(Dc, k_len, T->k_stride, T->row_exp, T->dh, T->dl);
+        else
+            k_tc_split<false><<<bc, TH, 0, s>>>(Dc, k_len, T->k_stride, T->row_exp, T->dh, T->dl);
+        CUtensorMap mh, ml;
+        if (!encode_map(&mh, T->dh, k_len, bc, T->k_stride) || !encode_map(&ml, T->dl, k_len, bc, T->k_stride))
+            return SNK_ERR_CUDA;
+        TcArgs a;
+        a.b = bc;
+        a.K_len = k_len;
+        a.row_exp = T->row_exp;
+        a.off = V.off;
+        a.hl = T->hl;
+        a.tile_ptr = V.tile_ptr;
+        a.seg_exp = T->seg_exp;
+        a.n_seg = n_seg;
+        a.n_win = V.n_win;
+        a.n_nt = V.n_nt;
+        a.n_mt = (int)ceil_div(bc, kTcM);
+        a.bias = bias;
+        a.Y = Y + c0 * n_seg;
+        a.status = L->status;
+        k_tc_spmm<<<a.n_mt * a.n_nt, kTcThreads, kTcSmem, s>>>(mh, ml, a);
+    }
+    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+}
+
+}  // namespace snk

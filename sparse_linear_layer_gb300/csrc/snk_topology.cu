@@ -548,9 +548,11 @@ int build_views(Layer* L, cudaStream_t s) {
         build_partition(L->col_ptr, L->in_f, n, L->n_blocks, kWarpsPerBlockDx, L->bnd_c, L->cdesc_c,
                         L->bdesc_c, s) != SNK_OK)
         return SNK_ERR_CUDA;
+    if (refresh_tc_views(L, s) != SNK_OK) return SNK_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SNK_ERR_CUDA;
     L->topology_version += 1;
+    mark_tc_views(L);
     return SNK_OK;
 }
 

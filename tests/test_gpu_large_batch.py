@@ -1,0 +1,154 @@
+"""Large-batch products on the tensor cores (forward and dX) against the oracle.
+
+"Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks on GPU",
+appendix Table 13, trains the layer at batch 4096.  The library runs such
+batches by densifying tiles of W in shared memory and multiplying them on the
+tensor cores with an fp16 hi/lo split of both operands.  The cases here:
+- force that path (SNK_LARGE_BATCH=on) on small shapes that span several tiles
+  and leave ragged tails in every dimension, including reduction lengths that
+  are not a multiple of 4 (scalar operand loads) and a batch of one row;
+- take it by default (batch >= 256) on the 10000 x 10000 layer of the
+  benchmark, checking rows at the edges of the 128-row batch tiles;
+- use inputs that are all positive, where a long chain in the tensor core's
+  truncating fp32 accumulator would drift outside the tolerance;
+- rebuild the tile-ordered views after a restructure, and replay a CUDA graph.
+Every element is compared with |gpu - oracle| <= 1e-5 * A + 1e-6.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from sparse_linear_layer_gb300 import synth
+from tests.gpu_util import assert_within, dev, host, make_gpu_layer, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return need_gpu()
+
+
+def _check(torch, lay, X, dY, bias, rows=None):
+    """forward (with bias) and dX through the library vs the oracle; rows
+    limits the comparison to those batch rows."""
+    g = make_gpu_layer(torch, lay)
+    can = oracle.canonicalize(lay.out_f, lay.in_f, lay.values, lay.rows, lay.cols)
+    v, r, c = can["values"], can["rows"], can["cols"]
+    Y = g.forward(dev(X, torch), None if bias is None else dev(bias, torch))
+    dX = g.backward_input(dev(dY, torch))
+    torch.cuda.synchronize()
+    sel = slice(None) if rows is None else rows
+    Yr, Ay = oracle.forward(lay.out_f, lay.in_f, v, r, c, X[sel], bias)
+    dXr, Ax = oracle.backward_input(lay.out_f, lay.in_f, v, r, c, dY[sel])
+    assert_within(host(Y)[sel], Yr, Ay, "forward")
+    assert_within(host(dX)[sel], dXr, Ax, "backward_input")
+    g.close()
+
+
+@pytest.mark.parametrize("out_f,in_f,sp,b", [
+    (300, 200, 90, 130),      # 2 x 2 batch tiles, ragged segment and window tails
+    (1000, 700, 95, 257),     # 3 batch tiles, last one a single row
+    (513, 1030, 50, 1),       # one batch row
+    (260, 203, 80, 129),      # forward reduction length 203: scalar operand loads
+    (203, 260, 80, 129),      # the same for dX
+    (64, 64, 0, 200),         # fully dense W
+])
+def test_forced_small_shapes(torch, monkeypatch, out_f, in_f, sp, b):
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    lay = synth.make_layer(out_f, in_f, sp, 0.05, 81, 82)
+    X = synth.normal((b, in_f), 1.0, 83)
+    dY = synth.normal((b, out_f), 1.0, 84)
+    bias = synth.normal(out_f, 0.1, 85)
+    _check(torch, lay, X, dY, bias)
+
+
+def test_default_dispatch_full_size(torch, monkeypatch):
+    """10000 x 10000 at 90%, batch 512: the path the library picks by itself."""
+    monkeypatch.delenv("SNK_LARGE_BATCH", raising=False)
+    lay = synth.make_layer(10_000, 10_000, 90, 0.01, 21, 22)
+    b = 512
+    X = synth.normal((b, 10_000), 1.0, 86)
+    dY = synth.normal((b, 10_000), 1.0, 87)
+    rows = np.array([0, 1, 127, 128, 255, 256, 383, 384, 510, 511])
+    _check(torch, lay, X, dY, None, rows)
+
+
+@pytest.mark.parametrize("out_f,in_f", [(300, 10_000), (10_000, 300)])
+def test_all_positive_long_reduction(torch, monkeypatch, out_f, in_f):
+    """Sign-coherent sums over 10000 terms: every rounding error of a
+    truncating accumulator has the same sign, so only short accumulation
+    chains stay within 1e-5 * A."""
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    lay = synth.make_layer(out_f, in_f, 50, 1.0, 88, 89)
+    lay.values = np.abs(lay.values).astype(np.float32) + np.float32(0.01)
+    b = 130
+    X = np.abs(synth.normal((b, in_f), 1.0, 90)).astype(np.float32)
+    dY = np.abs(synth.normal((b, out_f), 1.0, 91)).astype(np.float32)
+    _check(torch, lay, X, dY, None)
+
+
+def test_views_follow_restructure(torch, monkeypatch):
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    lay = synth.make_layer(700, 900, 90, 0.05, 92, 93)
+    g = make_gpu_layer(torch, lay)
+    b = 140
+    X = synth.normal((b, 900), 1.0, 94)
+    dY = synth.normal((b, 700), 1.0, 95)
+    Xd, dYd = dev(X, torch), dev(dY, torch)
+    for step in range(3):
+        if step:
+            g.prune_regrow(0.3, 0x5E7 + step)
+            g.values.copy_(dev(synth.normal(g.nnz, 0.05, 96 + step), torch))
+        Y = g.forward(Xd)
+        dX = g.backward_input(dYd)
+        torch.cuda.synchronize()
+        v, r, c = host(g.values), host(g.rows), host(g.cols)
+        Yr, Ay = oracle.forward(700, 900, v, r, c, X, None)
+        dXr, Ax = oracle.backward_input(700, 900, v, r, c, dY)
+        assert_within(host(Y), Yr, Ay, f"forward after {step} restructures")
+        assert_within(host(dX), dXr, Ax, f"backward_input after {step} restructures")
+    g.close()
+
+
+def test_graph_replay_matches_direct(torch, monkeypatch):
+    """After a first call has built the views, forward and dX only enqueue
+    kernels: a captured pair replays to the direct result bit for bit, also
+    after a restructure rebuilt the views in place."""
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    from sparse_linear_layer_gb300 import binding
+    lay = synth.make_layer(600, 500, 90, 0.05, 97, 98)
+    g = make_gpu_layer(torch, lay)
+    b = 300
+    X = dev(synth.normal((b, 500), 1.0, 99), torch)
+    dY = dev(synth.normal((b, 600), 1.0, 100), torch)
+    Y = torch.empty((b, 600), device="cuda")
+    dX = torch.empty((b, 500), device="cuda")
+
+    def step():
+        binding.snk_forward(g.handle, X, None, Y)
+        binding.snk_backward_input(g.handle, dY, dX)
+
+    step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for phase in range(2):
+        if phase:
+            g.prune_regrow(0.3, 0x5E7)
+            g.values.add_(0.01)
+            torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        got = (Y.clone(), dX.clone())
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], Y) and torch.equal(got[1], dX), f"phase {phase}"
+    g.close()
