@@ -124,6 +124,9 @@ bool tc_eligible(const Layer* L, int64_t b);
 // + bias.  Allocates and builds the tile-ordered view on first use.
 int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias, float* Y,
            cudaStream_t s);
+// dW on the entries of W (and db = column sums of dY) for a large batch.
+int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW, float* db,
+                 cudaStream_t s);
 int refresh_tc_views(Layer* L, cudaStream_t s);
 void mark_tc_views(Layer* L);
 void free_tc(Layer* L);

@@ -238,6 +238,7 @@ int launch_backward_weight(Layer* L, const float* X, const float* dY, int64_t b,
         }
         return SNK_OK;
     }
+    if (tc_eligible(L, b)) return run_tc_sddmm(L, X, dY, b, dW, db, s);
     SddmmArgs a{};
     a.col = L->c;
     a.col16 = L->c16;

@@ -53,9 +53,12 @@ struct TcView {
 };
 
 struct TcState {
-    TcView view[2];               // [0]: rows of W (forward), [1]: columns of W (dX)
+    // [0]: rows of W in 192 x 64 tiles (forward), [1]: its columns (dX),
+    // [2]: 128-row x 192-column blocks of W (weight gradient)
+    TcView view[3];
     uint32_t* hl = nullptr;       // [nnz + pad] scaled values in tile order as fp16 hi | lo << 16 (per call)
     int32_t* seg_exp = nullptr;   // [max(out, in)] scale exponent per segment
+    int32_t* col_exp = nullptr;   // [in] weight gradient: scale exponent per column of X
     int32_t* row_exp = nullptr;   // [kTcChunk] scale exponent per dense row
     __half* dh = nullptr;         // [kTcChunk * k_stride] dense operand, scaled, high part
     __half* dl = nullptr;         // the low part
@@ -93,6 +96,7 @@ static_assert(kTcSmem <= 227 * 1024 - 4096, "pipeline stages exceed shared memor
 static_assert(kTcN % 64 == 0 && kTcN <= 256, "two builder halves of whole 32-column loads");
 static_assert(kRecCap % 8 == 0, "staged ranges are whole 16-byte units");
 constexpr int kTcPad = 16;         // entries readable past nnz in the tile-order arrays
+constexpr int kWStride = kTcN + 1; // row stride (floats) of the weight-gradient sums tile: no bank conflicts
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -542,6 +546,246 @@ __global__ void k_tc_split(const float* __restrict__ D, int64_t len, int64_t ks,
     }
 }
 
+// ------------------------------------------------------------ weight gradient
+// dW_k = sum_b dY[b, r_k] X[b, c_k] on the tensor cores: the dense product
+// dY^T X over one batch chunk for a 128-row x 192-column block of W, kept
+// only at the block's entries.  A = dY^T (rows of W, batch contiguous) and
+// B = X^T (columns of W), both scaled per row and split into fp16 hi / lo by
+// k_tc_tsplit, arrive by TMA; the accumulators take turns and are drained
+// into registers as in k_tc_spmm; the block's sums then go through shared
+// memory to the entries listed by the weight-gradient view.
+struct TcwArgs {
+    int n_win;                // batch windows in this chunk
+    int n_ot, n_it;           // row blocks (of kTcM) and column blocks (of kTcN) of W
+    int64_t out_f, in_f;
+    const int32_t* e_row;     // [out] scale exponents of dY^T rows
+    const int32_t* e_col;     // [in] scale exponents of X^T rows
+    const int32_t* perm;      // weight-gradient view: canonical slot per entry
+    const uint16_t* off;      // offset in the block's fp32 tile
+    const int32_t* tile_ptr;  // [n_ot * n_it + 1]
+    float* dW;
+    int accumulate;           // add to dW (later batch chunks) instead of writing it
+    int32_t* status;
+};
+
+constexpr int kWThreads = kTcBuilders + 64;       // 8 drain warps, a TMA warp, an MMA warp
+constexpr int kWStage = kStageA + kStageB;        // one batch window of A and B
+constexpr int kWSmem = 2 * kWStage + 1024;
+static_assert(kTcM * kWStride * 4 <= 2 * kWStage, "the sums tile reuses the pipeline stages");
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    k_tc_sddmm(const __grid_constant__ CUtensorMap map_ah, const __grid_constant__ CUtensorMap map_al,
+               const __grid_constant__ CUtensorMap map_bh, const __grid_constant__ CUtensorMap map_bl,
+               const TcwArgs a) {
+    extern __shared__ __align__(1024) unsigned char tc_raw[];
+    unsigned char* sm = tc_raw + ((1024 - (smem_u32(tc_raw) & 1023)) & 1023);
+    __shared__ uint64_t full[2], empty[2], accf[2], acce[2], fin;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    __shared__ float ipw_row[kTcM], ipw_col[kTcN];
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int id = blockIdx.x;
+    const int gsz = kTcGroupM * a.n_it;
+    const int first_m = (id / gsz) * kTcGroupM;
+    const int gm = min(a.n_ot - first_m, kTcGroupM);
+    const int ot = first_m + (id % gsz) % gm;
+    const int it = (id % gsz) / gm;
+    const int64_t o0 = (int64_t)ot * kTcM, i0 = (int64_t)it * kTcN;
+    const int n_win = a.n_win;
+
+    if (t == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+            mbar_init(&accf[i], 1);
+            mbar_init(&acce[i], kTcBuilders);
+        }
+        mbar_init(&fin, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (t < kTcM) ipw_row[t] = ldexpf(1.f, o0 + t < a.out_f ? -a.e_row[o0 + t] : 0);
+    if (t < kTcN) ipw_col[t] = ldexpf(1.f, i0 + t < a.in_f ? -a.e_col[i0 + t] : 0);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    bool ok = true;
+    const int n_per = (n_win + kTcPeriod - 1) / kTcPeriod;
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            for (int w = 0; w < n_win; ++w) {
+                const int s = w & 1;
+                if (w >= 2 && !mbar_wait(&empty[s], ((w >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* st = sm + s * kWStage;
+                mbar_expect_tx(&full[s], kWStage);
+                tma_load_2d(st, &map_ah, w * kTcK, (int)o0, &full[s]);
+                tma_load_2d(st + kPieceA, &map_al, w * kTcK, (int)o0, &full[s]);
+                tma_load_2d(st + kStageA, &map_bh, w * kTcK, (int)i0, &full[s]);
+                tma_load_2d(st + kStageA + kPieceB, &map_bl, w * kTcK, (int)i0, &full[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            for (int w = 0; w < n_win; ++w) {
+                const int s = w & 1;
+                const int q = w / kTcPeriod, ab = q & 1;
+                const bool first = (w % kTcPeriod) == 0;
+                if (!mbar_wait(&full[s], (w >> 1) & 1) ||
+                    (first && q >= 2 && !mbar_wait(&acce[ab], ((q >> 1) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ah = smem_u32(sm + s * kWStage), al = ah + kPieceA;
+                const uint32_t bh = ah + kStageA, bl = bh + kPieceB;
+                const uint32_t d = tmem + ab * kAccStride;
+#pragma unroll
+                for (int kk = 0; kk < kTcK / 16; ++kk) {
+                    const uint32_t o = 32 * kk;
+                    mma_f16(d, desc_sw128(ah + o), desc_sw128(bh + o), (first && kk == 0) ? 0u : 1u);
+                    mma_f16(d, desc_sw128(ah + o), desc_sw128(bl + o), 1u);
+                    mma_f16(d, desc_sw128(al + o), desc_sw128(bh + o), 1u);
+                }
+                if (w + 2 < n_win) mma_commit(&empty[s]);
+                if ((w % kTcPeriod) == kTcPeriod - 1 || w == n_win - 1) mma_commit(&accf[ab]);
+            }
+            mma_commit(&fin);
+            if (!mbar_wait(&fin, 0)) ok = false;
+        }
+        __syncwarp();
+    } else {
+        const int lq = warp & 3, half = warp >> 2;
+        float acc[kColsPerThread];
+#pragma unroll
+        for (int j = 0; j < kColsPerThread; ++j) acc[j] = 0.f;
+        for (int q = 0; q < n_per && ok; ++q) {
+            const int ab = q & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&accf[ab], (q >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + ab * kAccStride + kColsPerThread * half;
+#pragma unroll
+            for (int c = 0; c < kColsPerThread / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(ta + 32 * c, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[32 * c + i] += __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(&acce[ab]);
+        }
+        // every MMA has completed (all turns drained): the stages hold the sums tile
+        if (!builders_any(!ok)) {
+            float* tile = reinterpret_cast<float*>(sm);
+            const int row = 32 * lq + lane;
+            const float ir = ipw_row[row];
+#pragma unroll
+            for (int j = 0; j < kColsPerThread; ++j) {
+                const int col = kColsPerThread * half + j;
+                tile[row * kWStride + col] = (acc[j] * ir) * ipw_col[col];
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kTcBuilders) : "memory");
+            const int32_t* tp = a.tile_ptr + (int64_t)ot * a.n_it + it;
+            const int j1 = tp[1];
+            for (int j = tp[0] + t; j < j1; j += kTcBuilders) {
+                const float v = tile[a.off[j]];
+                float* dst = a.dW + a.perm[j];
+                *dst = a.accumulate ? *dst + v : v;
+            }
+        } else {
+            ok = false;
+        }
+    }
+    if (!ok) atomicExch(&abort_flag, 1);
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag && t == 0) atomicOr(a.status, kStatLimit);
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// Per column of D [rows, n]: the scale exponent of its largest magnitude and,
+// if sum is given, its sum (written, or added when accumulate), summed in
+// runs of 32 rows and then pairwise so no fp32 chain exceeds ~45 terms.
+template <bool SUM>
+__global__ void __launch_bounds__(256) k_tc_colstats(const float* __restrict__ D, int64_t rows, int64_t n,
+                                                     int32_t* __restrict__ e_out, float* __restrict__ sum,
+                                                     int accumulate) {
+    __shared__ float sm_max[8][32], sm_sum[8][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t col = (int64_t)blockIdx.x * 32 + lane;
+    float m = 0.f, tot = 0.f;
+    if (col < n) {
+        for (int64_t g = w; g * 32 < rows; g += 8) {
+            float part = 0.f;
+            const int64_t r1 = min(rows, g * 32 + 32);
+            for (int64_t r = g * 32; r < r1; ++r) {
+                const float x = D[r * n + col];
+                m = fmaxf(m, fabsf(x));
+                if (SUM) part += x;
+            }
+            if (SUM) tot += part;
+        }
+    }
+    sm_max[w][lane] = m;
+    sm_sum[w][lane] = tot;
+    __syncthreads();
+    if (w == 0 && col < n) {
+        for (int i = 1; i < 8; ++i) m = fmaxf(m, sm_max[i][lane]);
+        if (SUM) {
+            const float s01 = sm_sum[0][lane] + sm_sum[1][lane], s23 = sm_sum[2][lane] + sm_sum[3][lane];
+            const float s45 = sm_sum[4][lane] + sm_sum[5][lane], s67 = sm_sum[6][lane] + sm_sum[7][lane];
+            const float s = (s01 + s23) + (s45 + s67);
+            sum[col] = accumulate ? sum[col] + s : s;
+        }
+        e_out[col] = tc_exponent(m);
+    }
+}
+
+// out[c][r] = split(D[r][c] * 2^e[c]) for r < rows, c < n: the transposed,
+// scaled fp16 pieces (row stride bs) the weight-gradient product loads.
+__global__ void k_tc_tsplit(const float* __restrict__ D, int64_t rows, int64_t n, const int32_t* __restrict__ e,
+                            int64_t bs, __half* __restrict__ oh, __half* __restrict__ ol) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+    const int64_t c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t r = r0 + ty + 8 * i, c = c0 + tx;
+        tile[ty + 8 * i][tx] = (r < rows && c < n) ? D[r * n + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t c = c0 + ty + 8 * i, r = r0 + tx;
+        if (c < n && r < rows) {
+            __half h, l;
+            split16(tile[tx][ty + 8 * i] * ldexpf(1.f, e[c]), h, l);
+            oh[c * bs + r] = h;
+            ol[c * bs + r] = l;
+        }
+    }
+}
+
 // ------------------------------------------------------------ per-call passes
 // Scale exponent of each segment (row of W, or column through perm).
 __global__ void k_tc_seg_exp(const int32_t* __restrict__ ptr, const float* __restrict__ v,
@@ -574,14 +818,29 @@ __global__ void k_tc_values(const float* __restrict__ v, const int32_t* __restri
 }
 
 // ------------------------------------------------------------ view build
+// Tile shapes of the three views: mode 0 tiles W's rows (kTcN segments x
+// kTcK reduction indices, offsets in the swizzled fp16 tile), mode 1 its
+// columns the same way, mode 2 blocks of kTcM rows x kTcN columns (offsets
+// in the fp32 accumulator tile, row stride kWStride).
+struct TileOf {
+    int mode, n_inner;   // tiles along the second coordinate
+    __device__ __forceinline__ uint32_t key(int32_t r, int32_t c) const {
+        if (mode == 2) return (uint32_t)(r / kTcM) * (uint32_t)n_inner + (uint32_t)(c / kTcN);
+        const int32_t sg = mode ? c : r, kk = mode ? r : c;
+        return (uint32_t)(sg / kTcN) * (uint32_t)n_inner + (uint32_t)(kk / kTcK);
+    }
+    __device__ __forceinline__ uint16_t off(int32_t r, int32_t c) const {
+        if (mode == 2) return (uint16_t)((r % kTcM) * kWStride + c % kTcN);
+        const int32_t sg = mode ? c : r, kk = mode ? r : c;
+        return (uint16_t)sw128(sg % kTcN, kk % kTcK);
+    }
+};
+
 __global__ void k_tc_keys(const int32_t* __restrict__ r, const int32_t* __restrict__ c, int64_t n,
-                          bool columns, int n_win, uint32_t* __restrict__ keys,
-                          uint32_t* __restrict__ vals) {
+                          TileOf tile, uint32_t* __restrict__ keys, uint32_t* __restrict__ vals) {
     for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n;
          k += (int64_t)gridDim.x * blockDim.x) {
-        const int32_t sg = columns ? c[k] : r[k];
-        const int32_t kk = columns ? r[k] : c[k];
-        keys[k] = (uint32_t)(sg / kTcN) * (uint32_t)n_win + (uint32_t)(kk / kTcK);
+        keys[k] = tile.key(r[k], c[k]);
         vals[k] = (uint32_t)k;
     }
 }
@@ -591,16 +850,14 @@ __global__ void k_tc_keys(const int32_t* __restrict__ r, const int32_t* __restri
 // included).
 __global__ void k_tc_finish(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals,
                             int64_t n, int64_t n_tiles, const int32_t* __restrict__ r,
-                            const int32_t* __restrict__ c, bool columns, int32_t* __restrict__ perm_t,
+                            const int32_t* __restrict__ c, TileOf tile, int32_t* __restrict__ perm_t,
                             uint16_t* __restrict__ off, int32_t* __restrict__ tile_ptr) {
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j <= n;
          j += (int64_t)gridDim.x * blockDim.x) {
         if (j < n) {
             const uint32_t k = vals[j];
             perm_t[j] = (int32_t)k;
-            const int32_t sg = columns ? c[k] : r[k];
-            const int32_t kk = columns ? r[k] : c[k];
-            off[j] = (uint16_t)sw128(sg % kTcN, kk % kTcK);
+            off[j] = tile.off(r[k], c[k]);
         }
         const int64_t lo = j == 0 ? 0 : (int64_t)keys[j - 1] + 1;
         const int64_t hi = j == n ? n_tiles : (int64_t)keys[j];
@@ -633,28 +890,34 @@ void tc_shape(const Layer* L, bool columns, int64_t* n_seg, int64_t* k_len) {
     *k_len = columns ? L->out_f : L->in_f;
 }
 
-int build_view(Layer* L, bool columns, cudaStream_t s) {
-    TcView& V = L->tc->view[columns ? 1 : 0];
-    int64_t n_seg, k_len;
-    tc_shape(L, columns, &n_seg, &k_len);
+int build_view(Layer* L, int mode, cudaStream_t s) {
+    TcView& V = L->tc->view[mode];
     const int64_t n = L->nnz;
     if (!V.perm_t) {
-        V.n_win = (int)ceil_div(k_len, kTcK);
-        V.n_nt = (int)ceil_div(n_seg, kTcN);
+        if (mode == 2) {
+            V.n_win = (int)ceil_div(L->in_f, kTcN);    // column blocks
+            V.n_nt = (int)ceil_div(L->out_f, kTcM);    // row blocks
+        } else {
+            int64_t n_seg, k_len;
+            tc_shape(L, mode == 1, &n_seg, &k_len);
+            V.n_win = (int)ceil_div(k_len, kTcK);
+            V.n_nt = (int)ceil_div(n_seg, kTcN);
+        }
         V.n_tiles = (int64_t)V.n_win * V.n_nt;
         if (!tc_alloc(&V.perm_t, n) || !tc_alloc(&V.off, n + kTcPad) || !tc_alloc(&V.tile_ptr, V.n_tiles + 1))
             return SNK_ERR_OOM;
     }
+    const TileOf tile{mode, V.n_win};
     const int T = 256;
     uint32_t* ck = L->col_keys;
     uint32_t* cv = L->col_vals;
-    k_tc_keys<<<grid_for(n, T, L->num_sms), T, 0, s>>>(L->r, L->c, n, columns, V.n_win, ck, cv);
+    k_tc_keys<<<grid_for(n, T, L->num_sms), T, 0, s>>>(L->r, L->c, n, tile, ck, cv);
     bool flipped = false;
     int st = sort_pairs_u32(ck, cv, ck + n, cv + n, n, bits_of((uint64_t)V.n_tiles), L->tile_hist,
                             L->tile_hist_len, s, &flipped);
     if (st != SNK_OK) return st;
     k_tc_finish<<<grid_for(n + 1, T, L->num_sms), T, 0, s>>>(flipped ? ck + n : ck, flipped ? cv + n : cv, n,
-                                                             V.n_tiles, L->r, L->c, columns, V.perm_t,
+                                                             V.n_tiles, L->r, L->c, tile, V.perm_t,
                                                              V.off, V.tile_ptr);
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
@@ -668,8 +931,9 @@ constexpr int64_t kTcDensityDiv = 100;
 
 bool tc_eligible(const Layer* L, int64_t b) {
     if (L->nnz == 0) return false;
-    const int64_t n_tiles =
-        ceil_div(L->out_f, kTcN) * ceil_div(L->in_f, kTcK) + ceil_div(L->in_f, kTcN) * ceil_div(L->out_f, kTcK);
+    const int64_t n_tiles = ceil_div(L->out_f, kTcN) * ceil_div(L->in_f, kTcK) +
+                            ceil_div(L->in_f, kTcN) * ceil_div(L->out_f, kTcK) +
+                            ceil_div(L->out_f, kTcM) * ceil_div(L->in_f, kTcN);
     if (n_tiles > INT32_MAX / 2) return false;
     const char* f = getenv("SNK_LARGE_BATCH");
     if (f && strcmp(f, "off") == 0) return false;
@@ -681,7 +945,8 @@ void free_tc(Layer* L) {
     if (!L->tc) return;
     TcState* T = L->tc;
     void* ptrs[] = {T->view[0].perm_t, T->view[0].off, T->view[0].tile_ptr, T->view[1].perm_t,
-                    T->view[1].off, T->view[1].tile_ptr, T->hl, T->seg_exp, T->row_exp, T->dh, T->dl};
+                    T->view[1].off, T->view[1].tile_ptr, T->view[2].perm_t, T->view[2].off,
+                    T->view[2].tile_ptr, T->hl, T->seg_exp, T->col_exp, T->row_exp, T->dh, T->dl};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete T;
@@ -692,9 +957,9 @@ void free_tc(Layer* L) {
 // marks them current once it has advanced the topology version.
 int refresh_tc_views(Layer* L, cudaStream_t s) {
     if (!L->tc) return SNK_OK;
-    for (int d = 0; d < 2; ++d)
+    for (int d = 0; d < 3; ++d)
         if (L->tc->view[d].perm_t) {
-            int st = build_view(L, d == 1, s);
+            int st = build_view(L, d, s);
             if (st != SNK_OK) return st;
         }
     return SNK_OK;
@@ -702,7 +967,7 @@ int refresh_tc_views(Layer* L, cudaStream_t s) {
 
 void mark_tc_views(Layer* L) {
     if (!L->tc) return;
-    for (int d = 0; d < 2; ++d)
+    for (int d = 0; d < 3; ++d)
         if (L->tc->view[d].perm_t) L->tc->view[d].version = L->topology_version;
 }
 
@@ -731,37 +996,43 @@ EncodeTiledFn encoder() {
 
 // fp16 [rows][len] at row stride ks, loaded in 64 x 128 boxes with the
 // 128-byte swizzle; reads past len or rows come back as zeros.
-bool encode_map(CUtensorMap* map, __half* base, int64_t len, int64_t rows, int64_t ks) {
+bool encode_map(CUtensorMap* map, __half* base, int64_t len, int64_t rows, int64_t ks, int box_rows = kTcM) {
     EncodeTiledFn fn = encoder();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)len, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ks * sizeof(__half)};
-    cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcM};
+    cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The large-batch workspace, allocated on first use.
+int ensure_tc(Layer* L) {
+    if (L->tc) return SNK_OK;
+    TcState* T = new TcState();
+    L->tc = T;
+    T->k_stride = ceil_div(std::max(L->out_f, L->in_f), 8) * 8;
+    if (!tc_alloc(&T->hl, L->nnz + kTcPad) || !tc_alloc(&T->seg_exp, std::max(L->out_f, L->in_f)) ||
+        !tc_alloc(&T->col_exp, L->in_f) || !tc_alloc(&T->row_exp, kTcChunk) ||
+        !tc_alloc(&T->dh, kTcChunk * T->k_stride) || !tc_alloc(&T->dl, kTcChunk * T->k_stride)) {
+        free_tc(L);
+        return SNK_ERR_OOM;
+    }
+    return SNK_OK;
+}
+
 }  // namespace
 
 int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias, float* Y,
            cudaStream_t s) {
-    if (!L->tc) {
-        TcState* T = new TcState();
-        L->tc = T;
-        T->k_stride = ceil_div(std::max(L->out_f, L->in_f), 8) * 8;
-        if (!tc_alloc(&T->hl, L->nnz + kTcPad) || !tc_alloc(&T->seg_exp, std::max(L->out_f, L->in_f)) ||
-            !tc_alloc(&T->row_exp, kTcChunk) || !tc_alloc(&T->dh, kTcChunk * T->k_stride) ||
-            !tc_alloc(&T->dl, kTcChunk * T->k_stride)) {
-            free_tc(L);
-            return SNK_ERR_OOM;
-        }
-    }
+    int st0 = ensure_tc(L);
+    if (st0 != SNK_OK) return st0;
     TcState* T = L->tc;
     TcView& V = T->view[columns ? 1 : 0];
     if (V.version != L->topology_version) {
-        int st = build_view(L, columns, s);
+        int st = build_view(L, columns ? 1 : 0, s);
         if (st != SNK_OK) return st;
         V.version = L->topology_version;
     }
@@ -801,6 +1072,66 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
         a.Y = Y + c0 * n_seg;
         a.status = L->status;
         k_tc_spmm<<<a.n_mt * a.n_nt, kTcThreads, kTcSmem, s>>>(mh, ml, a);
+    }
+    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+}
+
+int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW, float* db,
+                 cudaStream_t s) {
+    int st = ensure_tc(L);
+    if (st != SNK_OK) return st;
+    TcState* T = L->tc;
+    TcView& V = T->view[2];
+    if (V.version != L->topology_version) {
+        st = build_view(L, 2, s);
+        if (st != SNK_OK) return st;
+        V.version = L->topology_version;
+    }
+    if (cudaFuncSetAttribute(k_tc_sddmm, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem) != cudaSuccess)
+        return SNK_ERR_CUDA;
+    const int64_t out_f = L->out_f, in_f = L->in_f;
+    // batch rows per chunk: the transposed pieces of dY and X share the workspace
+    const int64_t cap = (kTcChunk * T->k_stride) / (out_f + in_f);
+    const int64_t chunk = std::max<int64_t>(kTcK, cap / kTcK * kTcK);
+    for (int64_t c0 = 0; c0 < b; c0 += chunk) {
+        const int64_t bc = std::min<int64_t>(chunk, b - c0);
+        const int64_t bs = ceil_div(bc, 8) * 8;
+        const float* dYc = dY + c0 * out_f;
+        const float* Xc = X + c0 * in_f;
+        const int acc = c0 > 0;
+        if (db)
+            k_tc_colstats<true><<<(unsigned)ceil_div(out_f, 32), 256, 0, s>>>(dYc, bc, out_f, T->seg_exp, db, acc);
+        else
+            k_tc_colstats<false><<<(unsigned)ceil_div(out_f, 32), 256, 0, s>>>(dYc, bc, out_f, T->seg_exp, nullptr, 0);
+        k_tc_colstats<false><<<(unsigned)ceil_div(in_f, 32), 256, 0, s>>>(Xc, bc, in_f, T->col_exp, nullptr, 0);
+        __half* ah = T->dh;
+        __half* al = T->dl;
+        __half* bh = T->dh + out_f * bs;
+        __half* bl = T->dl + out_f * bs;
+        const dim3 tb(32, 8);
+        k_tc_tsplit<<<dim3((unsigned)ceil_div(out_f, 32), (unsigned)ceil_div(bc, 32)), tb, 0, s>>>(
+            dYc, bc, out_f, T->seg_exp, bs, ah, al);
+        k_tc_tsplit<<<dim3((unsigned)ceil_div(in_f, 32), (unsigned)ceil_div(bc, 32)), tb, 0, s>>>(
+            Xc, bc, in_f, T->col_exp, bs, bh, bl);
+        CUtensorMap mah, mal, mbh, mbl;
+        if (!encode_map(&mah, ah, bc, out_f, bs, kTcM) || !encode_map(&mal, al, bc, out_f, bs, kTcM) ||
+            !encode_map(&mbh, bh, bc, in_f, bs, kTcN) || !encode_map(&mbl, bl, bc, in_f, bs, kTcN))
+            return SNK_ERR_CUDA;
+        TcwArgs a;
+        a.n_win = (int)ceil_div(bc, kTcK);
+        a.n_ot = V.n_nt;
+        a.n_it = V.n_win;
+        a.out_f = out_f;
+        a.in_f = in_f;
+        a.e_row = T->seg_exp;
+        a.e_col = T->col_exp;
+        a.perm = V.perm_t;
+        a.off = V.off;
+        a.tile_ptr = V.tile_ptr;
+        a.dW = dW;
+        a.accumulate = acc;
+        a.status = L->status;
+        k_tc_sddmm<<<a.n_ot * a.n_it, kWThreads, kWSmem, s>>>(mah, mal, mbh, mbl, a);
     }
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }

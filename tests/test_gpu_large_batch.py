@@ -1,4 +1,5 @@
-"""Large-batch products on the tensor cores (forward and dX) against the oracle.
+"""Large-batch products on the tensor cores (forward, dX and dW / db) against
+the oracle.
 
 "Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks on GPU",
 appendix Table 13, trains the layer at batch 4096.  The library runs such
@@ -29,20 +30,28 @@ def torch():
     return need_gpu()
 
 
-def _check(torch, lay, X, dY, bias, rows=None):
-    """forward (with bias) and dX through the library vs the oracle; rows
-    limits the comparison to those batch rows."""
+def _check(torch, lay, X, dY, bias, rows=None, weight=True):
+    """forward (with bias), dX and dW / db through the library vs the
+    oracle; rows limits the forward and dX comparison to those batch rows
+    (dW and db always reduce over the whole batch)."""
     g = make_gpu_layer(torch, lay)
     can = oracle.canonicalize(lay.out_f, lay.in_f, lay.values, lay.rows, lay.cols)
     v, r, c = can["values"], can["rows"], can["cols"]
-    Y = g.forward(dev(X, torch), None if bias is None else dev(bias, torch))
-    dX = g.backward_input(dev(dY, torch))
+    Xd, dYd = dev(X, torch), dev(dY, torch)
+    Y = g.forward(Xd, None if bias is None else dev(bias, torch))
+    dX = g.backward_input(dYd)
+    if weight:
+        dW, db = g.backward_weight(Xd, dYd, with_bias=True)
     torch.cuda.synchronize()
     sel = slice(None) if rows is None else rows
     Yr, Ay = oracle.forward(lay.out_f, lay.in_f, v, r, c, X[sel], bias)
     dXr, Ax = oracle.backward_input(lay.out_f, lay.in_f, v, r, c, dY[sel])
     assert_within(host(Y)[sel], Yr, Ay, "forward")
     assert_within(host(dX)[sel], dXr, Ax, "backward_input")
+    if weight:
+        dWr, Aw, dbr, Ab = oracle.backward_weight(lay.out_f, lay.in_f, r, c, X, dY)
+        assert_within(host(dW), dWr, Aw, "backward_weight")
+        assert_within(host(db), dbr, Ab, "bias grad")
     g.close()
 
 
@@ -53,6 +62,7 @@ def _check(torch, lay, X, dY, bias, rows=None):
     (260, 203, 80, 129),      # forward reduction length 203: scalar operand loads
     (203, 260, 80, 129),      # the same for dX
     (64, 64, 0, 200),         # fully dense W
+    (450, 390, 90, 2200),     # weight gradient over two batch chunks
 ])
 def test_forced_small_shapes(torch, monkeypatch, out_f, in_f, sp, b):
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
@@ -71,7 +81,24 @@ def test_default_dispatch_full_size(torch, monkeypatch):
     X = synth.normal((b, 10_000), 1.0, 86)
     dY = synth.normal((b, 10_000), 1.0, 87)
     rows = np.array([0, 1, 127, 128, 255, 256, 383, 384, 510, 511])
-    _check(torch, lay, X, dY, None, rows)
+    _check(torch, lay, X, dY, None, rows, weight=False)
+
+
+def test_default_dispatch_weight_gradient(torch, monkeypatch):
+    """dW and db at 5000 x 5000, 90%, batch 1024 (every entry of W)."""
+    monkeypatch.delenv("SNK_LARGE_BATCH", raising=False)
+    lay = synth.make_layer(5000, 5000, 90, 0.01, 11, 12)
+    b = 1024
+    X = synth.normal((b, 5000), 1.0, 101)
+    dY = synth.normal((b, 5000), 1.0, 102)
+    g = make_gpu_layer(torch, lay)
+    can = oracle.canonicalize(lay.out_f, lay.in_f, lay.values, lay.rows, lay.cols)
+    dW, db = g.backward_weight(dev(X, torch), dev(dY, torch), with_bias=True)
+    torch.cuda.synchronize()
+    dWr, Aw, dbr, Ab = oracle.backward_weight(5000, 5000, can["rows"], can["cols"], X, dY)
+    assert_within(host(dW), dWr, Aw, "backward_weight")
+    assert_within(host(db), dbr, Ab, "bias grad")
+    g.close()
 
 
 @pytest.mark.parametrize("out_f,in_f", [(300, 10_000), (10_000, 300)])
@@ -102,19 +129,22 @@ def test_views_follow_restructure(torch, monkeypatch):
             g.values.copy_(dev(synth.normal(g.nnz, 0.05, 96 + step), torch))
         Y = g.forward(Xd)
         dX = g.backward_input(dYd)
+        dW = g.backward_weight(Xd, dYd)
         torch.cuda.synchronize()
         v, r, c = host(g.values), host(g.rows), host(g.cols)
         Yr, Ay = oracle.forward(700, 900, v, r, c, X, None)
         dXr, Ax = oracle.backward_input(700, 900, v, r, c, dY)
+        dWr, Aw, _, _ = oracle.backward_weight(700, 900, r, c, X, dY)
         assert_within(host(Y), Yr, Ay, f"forward after {step} restructures")
         assert_within(host(dX), dXr, Ax, f"backward_input after {step} restructures")
+        assert_within(host(dW), dWr, Aw, f"backward_weight after {step} restructures")
     g.close()
 
 
 def test_graph_replay_matches_direct(torch, monkeypatch):
-    """After a first call has built the views, forward and dX only enqueue
-    kernels: a captured pair replays to the direct result bit for bit, also
-    after a restructure rebuilt the views in place."""
+    """After a first call has built the views, forward, dX and dW only
+    enqueue kernels: a captured step replays to the direct result bit for
+    bit, also after a restructure rebuilt the views in place."""
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
     from sparse_linear_layer_gb300 import binding
     lay = synth.make_layer(600, 500, 90, 0.05, 97, 98)
@@ -124,10 +154,13 @@ def test_graph_replay_matches_direct(torch, monkeypatch):
     dY = dev(synth.normal((b, 600), 1.0, 100), torch)
     Y = torch.empty((b, 600), device="cuda")
     dX = torch.empty((b, 500), device="cuda")
+    dW = torch.empty(g.nnz, device="cuda")
+    db = torch.empty(600, device="cuda")
 
     def step():
         binding.snk_forward(g.handle, X, None, Y)
         binding.snk_backward_input(g.handle, dY, dX)
+        binding.snk_backward_weight(g.handle, X, dY, dW, db)
 
     step()
     torch.cuda.synchronize()
@@ -147,8 +180,9 @@ def test_graph_replay_matches_direct(torch, monkeypatch):
             torch.cuda.synchronize()
         graph.replay()
         torch.cuda.synchronize()
-        got = (Y.clone(), dX.clone())
+        got = [t_.clone() for t_ in (Y, dX, dW, db)]
         step()
         torch.cuda.synchronize()
-        assert torch.equal(got[0], Y) and torch.equal(got[1], dX), f"phase {phase}"
+        for name, a_, b_ in zip(("Y", "dX", "dW", "db"), got, (Y, dX, dW, db)):
+            assert torch.equal(a_, b_), f"phase {phase}: replayed {name} differs"
     g.close()
