@@ -70,6 +70,12 @@ def parse():
                    help="instead of the single line, write one JSON object per layer of the "
                         "batch-1 inference-latency set (forward only; cold, warm and "
                         "CUDA-graph replay) to FILE")
+    p.add_argument("--large-batch", default=None, metavar="FILE",
+                   help="instead of the single line, write one JSON object per (layer, batch) "
+                        "of the large-batch set (tensor-core path against 64-row batch "
+                        "tiling) to FILE")
+    p.add_argument("--no-large-batch", action="store_true",
+                   help="leave the large-batch measurement out of the single line")
     return p.parse_args()
 
 
@@ -273,6 +279,27 @@ def run_reference(args, workload, rank, world):
 
 
 # --------------------------------------------------------------------------- our arm
+# The library's dispatch rule for the tensor-core path (batches of 256 rows
+# and more at density 1% and above) and the launches that path makes per
+# call: per-call passes plus one product kernel per batch chunk.
+TC_MIN_BATCH, TC_DENSITY_DIV, TC_CHUNK = 256, 100, 4096
+
+
+def tc_path(out_f, in_f, nnz, b):
+    mode = os.environ.get("SNK_LARGE_BATCH")
+    if nnz == 0 or mode == "off":
+        return False
+    return mode == "on" or (b >= TC_MIN_BATCH and nnz * TC_DENSITY_DIV >= out_f * in_f)
+
+
+def tc_launches(op, out_f, in_f, b):
+    if op == "dw":
+        k_stride = (max(out_f, in_f) + 7) // 8 * 8
+        chunk = max(64, (TC_CHUNK * k_stride) // (out_f + in_f) // 64 * 64)
+        return 5 * ((b + chunk - 1) // chunk)
+    return 2 + 2 * ((b + TC_CHUNK - 1) // TC_CHUNK)
+
+
 def launches_per_op(n_src, b, max_smem):
     launches = 0
     for t0 in range(0, b, 64):
@@ -547,6 +574,103 @@ def run_latency(args, dev):
             g.close()
 
 
+# Large-batch set: the GAMLP-scale batches of [SNACK] appendix Table 13
+# (batch 4096) on the benchmark's 10000 x 10000 layers and the 5000 x 5000
+# GAMLP-shaped one, batches 256 .. 4096.
+LARGE_BATCH_SET = [(10000, 10000, 90), (10000, 10000, 99), (5000, 5000, 90)]
+LARGE_BATCHES = [256, 1024, 4096]
+
+
+def measure_large_batch(torch, binding, g, lay, b, dev, flush, reps, tiled_reps):
+    """Device µs of forward, dX and dW at batch b on the tensor-core path (the
+    library's own dispatch) and on 64-row batch tiling (SNK_LARGE_BATCH=off),
+    L2 flushed before every call.  The tensor roofline counts what the path
+    executes: three fp16 products (hi*hi, hi*lo, lo*hi) of the densified
+    tiles, 6 * b * out * in flops per call, against the measured bf16 dense
+    peak (kind::f16 runs at the bf16 rate)."""
+    out_f, in_f = lay.out_f, lay.in_f
+    X = torch.randn(b, in_f, device=dev)
+    dY = torch.randn(b, out_f, device=dev)
+    Y = torch.empty(b, out_f, device=dev)
+    dX = torch.empty(b, in_f, device=dev)
+    dW = torch.empty(lay.nnz, device=dev)
+    db = torch.empty(out_f, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    ops = {"fwd": lambda: binding.snk_forward(g.handle, X, None, Y, sh),
+           "dx": lambda: binding.snk_backward_input(g.handle, dY, dX, sh),
+           "dw": lambda: binding.snk_backward_weight(g.handle, X, dY, dW, db, sh)}
+
+    def timed(f, n):
+        f()   # builds the tile-ordered views on first use
+        ts = []
+        for _ in range(n):
+            if flush is not None:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.mean(ts)
+
+    saved = os.environ.pop("SNK_LARGE_BATCH", None)
+    try:
+        tc = {n: timed(f, reps) for n, f in ops.items()}
+        tiled = {}
+        if tiled_reps:
+            os.environ["SNK_LARGE_BATCH"] = "off"
+            tiled = {n: timed(f, tiled_reps) for n, f in ops.items()}
+    finally:
+        os.environ.pop("SNK_LARGE_BATCH", None)
+        if saved is not None:
+            os.environ["SNK_LARGE_BATCH"] = saved
+    peak = measured_peak_tflops()
+    dense = 6.0 * b * out_f * in_f
+    useful = 2.0 * b * lay.nnz
+    res = {"out": out_f, "in": in_f, "nnz": lay.nnz, "batch": b, "us_tensor_path": tc,
+           "us_batch_tiled": tiled or None,
+           "speedup_vs_batch_tiled": {n: tiled[n] / tc[n] for n in tiled} if tiled else None,
+           "dense_equiv_tflops": {n: dense / tc[n] / 1e6 for n in tc},
+           "useful_tflops": {n: useful / tc[n] / 1e6 for n in tc}}
+    dom = max(tc, key=lambda n: tc[n])
+    res["roofline"] = {"bound": "tensor", "op": dom,
+                       "kernel": "k_tc_sddmm" if dom == "dw" else "k_tc_spmm",
+                       "achieved": dense / tc[dom] / 1e6, "peak": peak[0], "unit": "TFLOP/s",
+                       "frac": dense / tc[dom] / 1e6 / peak[0], "peak_kind": peak[1],
+                       "flops_per_launch": dense,
+                       "note": "whole call (per-call passes included) / mean event time"}
+    del X, dY, Y, dX, dW, db
+    return res
+
+
+def measured_peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "bf16_tflops, of measured (MEASURED_PEAKS.json, burst)"
+    except Exception:
+        return 1900.0, "bf16 dense, of fallback"
+
+
+def run_large_batch(args, dev):
+    import torch
+
+    from sparse_linear_layer_gb300 import binding, synth
+    flush = L2Flush(torch, dev, args.flush_mb) if args.flush_mb else None
+    with open(args.large_batch, "w") as fo:
+        for out_f, in_f, sp in LARGE_BATCH_SET:
+            lay, g, _, _, _, _, _ = make_device_layer(torch, binding, synth, dev, out_f, in_f, sp, 1)
+            for b in LARGE_BATCHES:
+                row = measure_large_batch(torch, binding, g, lay, b, dev, flush, reps=5,
+                                          tiled_reps=1 if b >= 1024 else 3)
+                row["sparsity_pct"] = sp
+                fo.write(json.dumps(row) + "\n")
+                fo.flush()
+            g.close()
+
+
 def run_ours(args, workload, rank, world, local):
     import numpy as np
     import torch
@@ -560,6 +684,9 @@ def run_ours(args, workload, rank, world, local):
         return
     if args.latency:
         run_latency(args, dev)
+        return
+    if args.large_batch:
+        run_large_batch(args, dev)
         return
     if world > 1:
         import torch.distributed as dist
@@ -685,9 +812,17 @@ def run_ours(args, workload, rank, world, local):
                                "the gradient variant ranks all out*in - kept candidates by the "
                                "batch's |dY^T X|"}
 
-    per_op_launch = {"fwd": launches_per_op(in_f, b, max_smem),
-                     "dx": launches_per_op(out_f, b, max_smem),
-                     "dw": launches_per_op(in_f, b, max_smem)}
+    large = None
+    if rank == 0 and world == 1 and not args.no_large_batch and args.only is None and nnz > 0:
+        large = measure_large_batch(torch, binding, g, lay, 4096, dev, flush, reps=5, tiled_reps=1)
+        large["workload"] = f"{out_f}x{in_f}, {args.sparsity:g}% sparse, batch 4096 ([SNACK] Table 13 batch)"
+
+    if tc_path(out_f, in_f, nnz, b):
+        per_op_launch = {n: tc_launches(n, out_f, in_f, b) for n in ("fwd", "dx", "dw")}
+    else:
+        per_op_launch = {"fwd": launches_per_op(in_f, b, max_smem),
+                         "dx": launches_per_op(out_f, b, max_smem),
+                         "dw": launches_per_op(in_f, b, max_smem)}
     launches = args.steps * sum(per_op_launch[n] for n in per_op_ms)
 
     cpu = None
@@ -706,6 +841,7 @@ def run_ours(args, workload, rank, world, local):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload,
             "us_per_call": us, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk.summary(), "restructure": restructure,
+            "large_batch": large,
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line), flush=True)

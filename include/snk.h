@@ -41,7 +41,9 @@
  *     captured into a CUDA graph (the inference-latency mode); a replay gives
  *     the same bits as a direct call.  A graph stays valid across
  *     snk_prune_regrow (nnz and the workspace addresses do not change) and
- *     becomes invalid at snk_destroy.
+ *     becomes invalid at snk_destroy.  The one exception is the first call
+ *     of each product on the large-batch path (below): it allocates that
+ *     path's workspace and builds its view, so capture after one such call.
  *   - Nothing crosses the ABI as an exception; every entry point returns a
  *     status code (snk_status_string gives its text).
  *   - Limits: 1 <= out, in <= 2^31 - 1; 0 <= nnz <= min(out*in, 2^31 - 1);
@@ -49,6 +51,29 @@
  *   - Numerics: fp32 products accumulated in fp32 with at least 32 partial
  *     sums per output reduced by a tree, so that each output y satisfies
  *     |y - exact| <= 1e-5 * A + 1e-6 with A the sum of |terms| (+|bias|).
+ *
+ * Large batches ([SNACK] appendix Table 13 trains at batch 4096)
+ *   - From batch 256 on, when at least 1% of W is stored, the three product
+ *     calls run on the tensor cores instead of 64-row batch tiling.  W is
+ *     densified tile by tile in shared memory (never in device memory) and
+ *     multiplied with the dense operand.  The environment variable
+ *     SNK_LARGE_BATCH=on|off forces the choice for every batch size.
+ *   - Numerics: every operand row is scaled by a power of two and split
+ *     into two fp16 pieces.  The three products hi*hi, hi*lo and lo*hi carry
+ *     about 22 bits.  The tensor core's fp32 accumulation truncates, so it
+ *     is never chained over more than 8 windows of 64 terms (96 MMA steps).
+ *     The partial results are then added in fp32 with round-to-nearest.
+ *     The error stays inside the bound above even when every term has the
+ *     same sign (about 4e-6 * A then).
+ *   - Non-finite inputs: a densified tile also multiplies the stored zeros,
+ *     so an inf or NaN in a row of X (dY) makes that whole output row NaN,
+ *     and one in W makes its whole output column NaN.  The batch-tiled path
+ *     propagates them per entry.
+ *   - Memory, allocated on the first such call and kept until snk_destroy:
+ *     about 22 bytes per stored entry (three tile-ordered views of 6 bytes
+ *     and a 4-byte fp16 value pair), plus 16 KB per row or column of the
+ *     larger dimension (fp16 pieces of 4096 dense rows; larger batches run
+ *     in chunks of that size).  An allocation failure returns SNK_ERR_OOM.
  */
 #ifndef SNK_H
 #define SNK_H

@@ -186,3 +186,22 @@ def test_graph_replay_matches_direct(torch, monkeypatch):
         for name, a_, b_ in zip(("Y", "dX", "dW", "db"), got, (Y, dX, dW, db)):
             assert torch.equal(a_, b_), f"phase {phase}: replayed {name} differs"
     g.close()
+
+
+def test_non_finite_input_row(torch, monkeypatch):
+    """A NaN in one row of X makes that whole row of Y NaN on this path (the
+    densified tiles multiply it by the stored zeros too); every other row
+    still matches the oracle."""
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    lay = synth.make_layer(300, 200, 90, 0.05, 103, 104)
+    b = 130
+    X = synth.normal((b, 200), 1.0, 105)
+    X[7, 11] = np.nan
+    g = make_gpu_layer(torch, lay)
+    can = oracle.canonicalize(300, 200, lay.values, lay.rows, lay.cols)
+    Y = host(g.forward(dev(X, torch)))
+    assert np.isnan(Y[7]).all()
+    keep = np.arange(b) != 7
+    Yr, Ay = oracle.forward(300, 200, can["values"], can["rows"], can["cols"], X[keep], None)
+    assert_within(Y[keep], Yr, Ay, "rows without the NaN")
+    g.close()
