@@ -59,6 +59,7 @@ struct TcState {
     uint32_t* hl = nullptr;       // [nnz + pad] scaled values in tile order as fp16 hi | lo << 16 (per call)
     int32_t* seg_exp = nullptr;   // [max(out, in)] scale exponent per segment
     int32_t* col_exp = nullptr;   // [in] weight gradient: scale exponent per column of X
+    int32_t* run_start = nullptr; // view build: first position of each (tile, bank) run
     int32_t* row_exp = nullptr;   // [kTcChunk] scale exponent per dense row
     __half* dh = nullptr;         // [kTcChunk * k_stride] dense operand, scaled, high part
     __half* dl = nullptr;         // the low part
@@ -97,6 +98,10 @@ static_assert(kTcN % 64 == 0 && kTcN <= 256, "two builder halves of whole 32-col
 static_assert(kRecCap % 8 == 0, "staged ranges are whole 16-byte units");
 constexpr int kTcPad = 16;         // entries readable past nnz in the tile-order arrays
 constexpr int kWStride = kTcN + 1; // row stride (floats) of the weight-gradient sums tile: no bank conflicts
+// An fp16 piece of a sparse tile holds kTcN * kTcK / 64 = 192 words per bank,
+// so fewer than kRankSpan entries of one window share a bank.
+constexpr uint32_t kRankSpan = 512;
+static_assert(kTcN * kTcK / 64 * 2 <= (int)kRankSpan, "rank within a bank fits its field");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -836,12 +841,34 @@ struct TileOf {
     }
 };
 
+// Sort keys of the entries: their tile, and with by_bank also the
+// shared-memory bank their 16-bit store hits (tile * 32 + bank).
 __global__ void k_tc_keys(const int32_t* __restrict__ r, const int32_t* __restrict__ c, int64_t n,
-                          TileOf tile, uint32_t* __restrict__ keys, uint32_t* __restrict__ vals) {
+                          TileOf tile, bool by_bank, uint32_t* __restrict__ keys, uint32_t* __restrict__ vals) {
     for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n;
          k += (int64_t)gridDim.x * blockDim.x) {
-        keys[k] = tile.key(r[k], c[k]);
+        const uint32_t t = tile.key(r[k], c[k]);
+        keys[k] = by_bank ? t * 32u + ((tile.off(r[k], c[k]) >> 2) & 31u) : t;
         vals[k] = (uint32_t)k;
+    }
+}
+
+// Entries sorted by (tile, bank): the first position of every (tile, bank) run.
+__global__ void k_tc_run_start(const uint32_t* __restrict__ keys, int64_t n, int32_t* __restrict__ start) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x)
+        if (j == 0 || keys[j] != keys[j - 1]) start[keys[j]] = (int32_t)j;
+}
+
+// (tile, bank) -> (tile, rank within the bank, bank): sorted by this key, each
+// aligned group of 32 entries of a window (one warp's store instruction) takes
+// one entry from each bank while the banks last, instead of up to 32 from one.
+__global__ void k_tc_rank_key(uint32_t* __restrict__ keys, int64_t n, const int32_t* __restrict__ start) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t k1 = keys[j];
+        const uint32_t rank = (uint32_t)(j - start[k1]);
+        keys[j] = ((k1 >> 5) * kRankSpan + rank) * 32u + (k1 & 31u);
     }
 }
 
@@ -849,7 +876,7 @@ __global__ void k_tc_keys(const int32_t* __restrict__ r, const int32_t* __restri
 // in the swizzled fp16 tile, and the first entry of every tile (empty tiles
 // included).
 __global__ void k_tc_finish(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals,
-                            int64_t n, int64_t n_tiles, const int32_t* __restrict__ r,
+                            int64_t n, int64_t n_tiles, int shift, const int32_t* __restrict__ r,
                             const int32_t* __restrict__ c, TileOf tile, int32_t* __restrict__ perm_t,
                             uint16_t* __restrict__ off, int32_t* __restrict__ tile_ptr) {
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j <= n;
@@ -859,8 +886,8 @@ __global__ void k_tc_finish(const uint32_t* __restrict__ keys, const uint32_t* _
             perm_t[j] = (int32_t)k;
             off[j] = tile.off(r[k], c[k]);
         }
-        const int64_t lo = j == 0 ? 0 : (int64_t)keys[j - 1] + 1;
-        const int64_t hi = j == n ? n_tiles : (int64_t)keys[j];
+        const int64_t lo = j == 0 ? 0 : (int64_t)(keys[j - 1] >> shift) + 1;
+        const int64_t hi = j == n ? n_tiles : (int64_t)(keys[j] >> shift);
         for (int64_t tt = lo; tt <= hi; ++tt) tile_ptr[tt] = (int32_t)j;
     }
 }
@@ -909,16 +936,45 @@ int build_view(Layer* L, int mode, cudaStream_t s) {
     }
     const TileOf tile{mode, V.n_win};
     const int T = 256;
+    const int G = grid_for(n, T, L->num_sms);
+    const int tile_bits = bits_of((uint64_t)V.n_tiles);
+    // the sparse-tile views also spread each window's entries over the banks
+    // when the (tile, rank, bank) key fits 32 bits
+    const bool by_bank = mode != 2 && tile_bits + 14 <= 32;
+    if (by_bank && !L->tc->run_start) {
+        int64_t most = 0;
+        for (int m = 0; m < 2; ++m) {
+            int64_t n_seg, k_len;
+            tc_shape(L, m == 1, &n_seg, &k_len);
+            most = std::max(most, ceil_div(n_seg, kTcN) * ceil_div(k_len, kTcK) * 32);
+        }
+        if (!tc_alloc(&L->tc->run_start, most)) return SNK_ERR_OOM;
+    }
     uint32_t* ck = L->col_keys;
     uint32_t* cv = L->col_vals;
-    k_tc_keys<<<grid_for(n, T, L->num_sms), T, 0, s>>>(L->r, L->c, n, tile, ck, cv);
+    k_tc_keys<<<G, T, 0, s>>>(L->r, L->c, n, tile, by_bank, ck, cv);
     bool flipped = false;
-    int st = sort_pairs_u32(ck, cv, ck + n, cv + n, n, bits_of((uint64_t)V.n_tiles), L->tile_hist,
+    int st = sort_pairs_u32(ck, cv, ck + n, cv + n, n, tile_bits + (by_bank ? 5 : 0), L->tile_hist,
                             L->tile_hist_len, s, &flipped);
     if (st != SNK_OK) return st;
-    k_tc_finish<<<grid_for(n + 1, T, L->num_sms), T, 0, s>>>(flipped ? ck + n : ck, flipped ? cv + n : cv, n,
-                                                             V.n_tiles, L->r, L->c, tile, V.perm_t,
-                                                             V.off, V.tile_ptr);
+    uint32_t* kk = flipped ? ck + n : ck;
+    uint32_t* vv = flipped ? cv + n : cv;
+    int shift = 0;
+    if (by_bank) {
+        k_tc_run_start<<<G, T, 0, s>>>(kk, n, L->tc->run_start);
+        k_tc_rank_key<<<G, T, 0, s>>>(kk, n, L->tc->run_start);
+        uint32_t* k2 = flipped ? ck : ck + n;
+        uint32_t* v2 = flipped ? cv : cv + n;
+        st = sort_pairs_u32(kk, vv, k2, v2, n, tile_bits + 14, L->tile_hist, L->tile_hist_len, s, &flipped);
+        if (st != SNK_OK) return st;
+        if (flipped) {
+            kk = k2;
+            vv = v2;
+        }
+        shift = 14;
+    }
+    k_tc_finish<<<grid_for(n + 1, T, L->num_sms), T, 0, s>>>(kk, vv, n, V.n_tiles, shift, L->r, L->c, tile,
+                                                             V.perm_t, V.off, V.tile_ptr);
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
@@ -946,7 +1002,8 @@ void free_tc(Layer* L) {
     TcState* T = L->tc;
     void* ptrs[] = {T->view[0].perm_t, T->view[0].off, T->view[0].tile_ptr, T->view[1].perm_t,
                     T->view[1].off, T->view[1].tile_ptr, T->view[2].perm_t, T->view[2].off,
-                    T->view[2].tile_ptr, T->hl, T->seg_exp, T->col_exp, T->row_exp, T->dh, T->dl};
+                    T->view[2].tile_ptr, T->hl, T->seg_exp, T->col_exp, T->run_start, T->row_exp, T->dh,
+                    T->dl};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete T;
