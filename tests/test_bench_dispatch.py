@@ -1,0 +1,56 @@
+"""bench.py's copy of the library's path choice, checked on the host.
+
+bench.py counts the kernel launches of the timed region and picks the
+roofline (HBM for the batch-tiled kernels, tensor for the large-batch path)
+from the same rule the library applies in snk_tc.cu: batches of
+kTcMinBatch rows and more at density 1 / kTcDensityDiv and above, dense
+operands in chunks of kTcChunk rows.  These tests read the constants out of
+the CUDA source, so the two cannot drift apart silently."""
+import os
+import re
+
+import pytest
+
+import bench
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "sparse_linear_layer_gb300", "csrc", "snk_tc.cu")
+
+
+def _const(name):
+    m = re.search(r"constexpr\s+\w+\s+" + name + r"\s*=\s*(?:1\s*<<\s*)?(\d+)", open(SRC).read())
+    assert m, name
+    return int(m.group(1))
+
+
+def test_constants_match_the_library():
+    assert bench.TC_MIN_BATCH == _const("kTcMinBatch")
+    assert bench.TC_DENSITY_DIV == _const("kTcDensityDiv")
+    assert bench.TC_CHUNK == _const("kTcChunk")
+
+
+def test_rule(monkeypatch):
+    monkeypatch.delenv("SNK_LARGE_BATCH", raising=False)
+    n = 10_000
+    assert not bench.tc_path(n, n, 10_000_000, 255)
+    assert bench.tc_path(n, n, 10_000_000, 256)
+    assert bench.tc_path(n, n, 1_000_000, 4096)          # exactly 1%
+    assert not bench.tc_path(n, n, 999_999, 4096)        # below 1%
+    assert not bench.tc_path(n, n, 0, 4096)
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    assert bench.tc_path(n, n, 10, 1)
+    monkeypatch.setenv("SNK_LARGE_BATCH", "off")
+    assert not bench.tc_path(n, n, 10_000_000, 4096)
+
+
+@pytest.mark.parametrize("b", [256, 4096, 4097, 10_000])
+def test_launch_counts(b):
+    # forward / dX: segment scales and tile-order values once, then a split
+    # and a product kernel per chunk of kTcChunk rows
+    chunks = -(-b // bench.TC_CHUNK)
+    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 2 + 2 * chunks
+    # dW: two column passes, two transposes and a product kernel per chunk;
+    # the chunk is what the shared fp16 workspace holds for both operands
+    k_stride = 10_000
+    chunk = (bench.TC_CHUNK * k_stride) // 20_000 // 64 * 64
+    assert bench.tc_launches("dw", 10_000, 10_000, b) == 5 * (-(-b // chunk))

@@ -21,27 +21,31 @@ def torch():
     return need_gpu()
 
 
-def test_autograd_matches_oracle(torch):
+@pytest.mark.parametrize("lead", [(2, 3), (4, 80)])
+def test_autograd_matches_oracle(torch, lead):
+    """(2, 3): 6 rows, the batch-tiled kernels; (4, 80): 320 rows, which the
+    library runs on the tensor cores."""
     from sparse_linear_layer_gb300.module import SparseLinear
     out_f, in_f = 300, 200
+    rows = lead[0] * lead[1]
     lay = synth.make_layer(out_f, in_f, 90, 0.1, 81, 82)
     m = SparseLinear.from_triple(in_f, out_f, dev(lay.values, torch), dev(lay.rows, torch),
                                  dev(lay.cols, torch), bias=True)
     with torch.no_grad():
         m.bias.copy_(dev(synth.normal(out_f, 0.1, 83), torch))
-    x = dev(synth.normal((2, 3, in_f), 1.0, 84), torch).requires_grad_(True)
-    G = dev(synth.normal((2, 3, out_f), 1.0, 85), torch)
+    x = dev(synth.normal((*lead, in_f), 1.0, 84), torch).requires_grad_(True)
+    G = dev(synth.normal((*lead, out_f), 1.0, 85), torch)
     y = m(x)
-    assert y.shape == (2, 3, out_f)
+    assert y.shape == (*lead, out_f)
     (y * G).sum().backward()
     can = oracle.canonicalize(out_f, in_f, lay.values, lay.rows, lay.cols)
     v, r, c = can["values"], can["rows"], can["cols"]
-    X2 = host(x.detach()).reshape(6, in_f)
-    G2 = host(G).reshape(6, out_f)
+    X2 = host(x.detach()).reshape(rows, in_f)
+    G2 = host(G).reshape(rows, out_f)
     yr, ay = oracle.forward(out_f, in_f, v, r, c, X2, host(m.bias.detach()))
-    assert_within(host(y.detach()).reshape(6, out_f), yr, ay, "forward")
+    assert_within(host(y.detach()).reshape(rows, out_f), yr, ay, "forward")
     dxr, ax = oracle.backward_input(out_f, in_f, v, r, c, G2)
-    assert_within(host(x.grad).reshape(6, in_f), dxr, ax, "input grad")
+    assert_within(host(x.grad).reshape(rows, in_f), dxr, ax, "input grad")
     dwr, aw, dbr, ab = oracle.backward_weight(out_f, in_f, r, c, X2, G2)
     assert_within(host(m.values.grad), dwr, aw, "values grad")
     assert_within(host(m.bias.grad), dbr, ab, "bias grad")
