@@ -205,3 +205,23 @@ def test_non_finite_input_row(torch, monkeypatch):
     Yr, Ay = oracle.forward(300, 200, can["values"], can["rows"], can["cols"], X[keep], None)
     assert_within(Y[keep], Yr, Ay, "rows without the NaN")
     g.close()
+
+
+def test_batch_chunks_and_empty_segments(torch, monkeypatch):
+    """A batch over the 4096-row chunk of the dense workspace (two launch
+    sequences for forward and dX), on a Zipf-skewed layer whose many empty
+    rows and columns leave whole tiles without entries (outputs = bias or 0)."""
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    lay = synth.make_layer(400, 300, 80, 0.05, 106, 107, zipf_s=1.2)
+    # empty every third row and every fifth column, and all of rows 192-383
+    # (one whole segment tile) and columns 64-127 (one whole window)
+    keep = ((lay.rows % 3) != 0) & ((lay.cols % 5) != 0)
+    keep &= ~((lay.rows >= 192) & (lay.rows < 384)) & ~((lay.cols >= 64) & (lay.cols < 128))
+    lay.values, lay.rows, lay.cols = lay.values[keep], lay.rows[keep], lay.cols[keep]
+    assert (np.bincount(lay.rows, minlength=400) == 0).sum() > 250
+    b = 4100
+    X = synth.normal((b, 300), 1.0, 108)
+    dY = synth.normal((b, 400), 1.0, 109)
+    bias = synth.normal(400, 0.1, 110)
+    _check(torch, lay, X, dY, bias)
+
