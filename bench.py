@@ -295,7 +295,7 @@ def run_reference(args, workload, rank, world):
 # The library's dispatch rule for the tensor-core path (batches of 256 rows
 # and more at density 1% and above) and the launches that path makes per
 # call: per-call passes plus one product kernel per batch chunk.
-TC_MIN_BATCH, TC_DENSITY_DIV, TC_CHUNK = 256, 100, 4096
+TC_MIN_BATCH, TC_DENSITY_DIV, TC_CHUNK = 256, 100, 8192
 
 
 def tc_path(out_f, in_f, nnz, b):

@@ -71,8 +71,8 @@
  *     propagates them per entry.
  *   - Memory, allocated on the first such call and kept until snk_destroy:
  *     about 22 bytes per stored entry (three tile-ordered views of 6 bytes
- *     and a 4-byte fp16 value pair), plus 16 KB per row or column of the
- *     larger dimension (fp16 pieces of 4096 dense rows; larger batches run
+ *     and a 4-byte fp16 value pair), plus 32 KB per row or column of the
+ *     larger dimension (fp16 pieces of 8192 dense rows; larger batches run
  *     in chunks of that size).  An allocation failure returns SNK_ERR_OOM.
  */
 #ifndef SNK_H

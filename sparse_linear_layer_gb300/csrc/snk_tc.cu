@@ -79,7 +79,7 @@ constexpr int kRecSlots = 4;       // windows of sparse entries staged in shared
 constexpr int kRecCap = 1536;      // entries staged per window (the rest are read from memory)
 constexpr int kTcPeriod = 8;       // windows per accumulator turn
 constexpr int kTcGroupM = 8;       // dense-row tiles per raster group
-constexpr int kTcChunk = 4096;     // dense rows per launch
+constexpr int kTcChunk = 8192;     // dense rows per launch
 constexpr int kPieceA = kTcM * kTcK * 2;          // 16 KB
 constexpr int kPieceB = kTcN * kTcK * 2;          // 24 KB
 constexpr int kStageA = 2 * kPieceA, kStageB = 2 * kPieceB;

@@ -62,7 +62,7 @@ def _check(torch, lay, X, dY, bias, rows=None, weight=True):
     (260, 203, 80, 129),      # forward reduction length 203: scalar operand loads
     (203, 260, 80, 129),      # the same for dX
     (64, 64, 0, 200),         # fully dense W
-    (450, 390, 90, 2200),     # weight gradient over two batch chunks
+    (450, 390, 90, 4500),     # weight gradient over two batch chunks (4416 + 84 rows)
 ])
 def test_forced_small_shapes(torch, monkeypatch, out_f, in_f, sp, b):
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
@@ -208,9 +208,10 @@ def test_non_finite_input_row(torch, monkeypatch):
 
 
 def test_batch_chunks_and_empty_segments(torch, monkeypatch):
-    """A batch over the 4096-row chunk of the dense workspace (two launch
-    sequences for forward and dX), on a Zipf-skewed layer whose many empty
-    rows and columns leave whole tiles without entries (outputs = bias or 0)."""
+    """A batch over the 8192-row chunk of the dense workspace (two launch
+    sequences for forward and dX; two batch chunks of 4672 rows for dW), on
+    a layer whose many empty rows and columns leave whole tiles without
+    entries (outputs = bias or 0)."""
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
     lay = synth.make_layer(400, 300, 80, 0.05, 106, 107, zipf_s=1.2)
     # empty every third row and every fifth column, and all of rows 192-383
@@ -219,7 +220,7 @@ def test_batch_chunks_and_empty_segments(torch, monkeypatch):
     keep &= ~((lay.rows >= 192) & (lay.rows < 384)) & ~((lay.cols >= 64) & (lay.cols < 128))
     lay.values, lay.rows, lay.cols = lay.values[keep], lay.rows[keep], lay.cols[keep]
     assert (np.bincount(lay.rows, minlength=400) == 0).sum() > 250
-    b = 4100
+    b = 8300
     X = synth.normal((b, 300), 1.0, 108)
     dY = synth.normal((b, 400), 1.0, 109)
     bias = synth.normal(400, 0.1, 110)
