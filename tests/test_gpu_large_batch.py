@@ -63,6 +63,7 @@ def _check(torch, lay, X, dY, bias, rows=None, weight=True):
     (203, 260, 80, 129),      # the same for dX
     (64, 64, 0, 200),         # fully dense W
     (450, 390, 90, 4500),     # weight gradient over two batch chunks (4416 + 84 rows)
+    (1000, 700, 99, 300),     # sparse windows: stages cleared entry by entry, not by bulk copy
 ])
 def test_forced_small_shapes(torch, monkeypatch, out_f, in_f, sp, b):
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
