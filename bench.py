@@ -31,6 +31,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -153,16 +154,24 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """Source text without comments and blank space, so that editing a
+    comment does not detach committed measurements from a kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest(kernel_tag=None):
-    """Digest of the sources a kernel is built from (all of csrc when the tag
-    is not listed)."""
+    """Digest of the code a kernel is built from (all of csrc when the tag
+    is not listed); comments do not count."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_linear_layer_gb300", "csrc")
     names = KERNEL_SOURCES.get(kernel_tag) or sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
     for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

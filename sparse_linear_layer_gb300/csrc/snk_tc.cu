@@ -1,5 +1,6 @@
 // Large-batch products on the tensor cores (tcgen05): Y = X W^T + b and
-// dX = dY W for batches of hundreds of rows and more.
+// dX = dY W (k_tc_spmm), and dW on the entries of W with db (k_tc_sddmm),
+// for batches of hundreds of rows and more.
 //
 // "Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks on
 // GPU", appendix Table 13 (GAMLP training at batch 4096): at that batch the
@@ -18,10 +19,10 @@
 // over kTcPeriod windows, and every finished one is added into fp32 registers
 // (round to nearest) while the other fills.
 //
-// Per call: the dense operand is scaled and split once into fp16 hi/lo
-// arrays (k_tc_split), the values are gathered into tile order (k_tc_gather)
-// and the segment scales found (k_tc_seg_exp).  Then one CTA per 128 x 192
-// output tile, 10 warps:
+// Forward and dX, per call: the dense operand is scaled and split once into
+// fp16 hi/lo arrays (k_tc_split), the values are put into tile order, scaled
+// per segment and split (k_tc_values), after the segment scales are found
+// (k_tc_seg_exp).  Then one CTA per 128 x 192 output tile, 12 warps:
 //   warps 0-7  write each window's entries into one of two sparse stages
 //              (in sparse layers first clearing the entries written there two
 //              windows ago), drain the accumulators and store the output;
@@ -34,6 +35,7 @@
 //   warp 11    in denser layers clears each sparse stage once its MMAs are
 //              done, with a bulk copy from a zero buffer, so the builders
 //              never clear.
+// The weight gradient is described at k_tc_sddmm.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdlib.h>

@@ -54,3 +54,12 @@ def test_launch_counts(b):
     k_stride = 10_000
     chunk = (bench.TC_CHUNK * k_stride) // 20_000 // 64 * 64
     assert bench.tc_launches("dw", 10_000, 10_000, b) == 5 * (-(-b // chunk))
+
+
+def test_source_digest_ignores_comments():
+    """Committed ncu traffic stays attached to a kernel while its code is
+    unchanged: comments and spacing do not enter the digest."""
+    a = "int f() { return 1; }  // one\n/* block\ncomment */ int g;"
+    b = "// lead\nint f() {\n    return 1;\n}\nint g;  /* trailing */"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only("int f() { return 2; }") != bench._code_only("int f() { return 1; }")
