@@ -22,19 +22,17 @@
 // Forward and dX, per call: the dense operand is scaled and split once into
 // fp16 hi/lo arrays (k_tc_split), the values are put into tile order, scaled
 // per segment and split (k_tc_values), after the segment scales are found
-// (k_tc_seg_exp).  Then one CTA per 128 x 192 output tile, 12 warps:
-//   warps 0-7  write each window's entries into one of two sparse stages
-//              (in sparse layers first clearing the entries written there two
-//              windows ago), drain the accumulators and store the output;
+// (k_tc_seg_exp).  Then one CTA per 128 x 192 output tile, 11 warps:
+//   warps 0-7  clear one of two sparse stages (the whole stage in denser
+//              layers, the entries written there two windows ago in sparse
+//              ones), write this window's entries, drain the accumulators and
+//              store the output;
 //   warp 8     loads the dense hi/lo tiles with TMA into one of two stages;
 //   warp 9     issues the MMAs (one thread) and owns the TMEM allocation;
 //   warp 10    stages each window's sparse entries (tile offsets and fp16
 //              pieces, contiguous in tile order) into one of four shared-memory
 //              slots with bulk copies, so the builders never wait on device
-//              memory and only store;
-//   warp 11    in denser layers clears each sparse stage once its MMAs are
-//              done, with a bulk copy from a zero buffer, so the builders
-//              never clear.
+//              memory.
 // The weight gradient is described at k_tc_sddmm.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -68,7 +66,6 @@ struct TcState {
     int32_t* row_exp = nullptr;   // [kTcChunk] scale exponent per dense row
     __half* dh = nullptr;         // [kTcChunk * k_stride] dense operand, scaled, high part
     __half* dl = nullptr;         // the low part
-    void* zeros = nullptr;        // one sparse stage of zero bytes, the source of stage clears
     int64_t k_stride = 0;         // row stride of dh / dl: max(out, in) rounded up to 8
 };
 
@@ -78,14 +75,14 @@ constexpr int kTcM = 128;          // dense rows per tile (TMEM lanes)
 constexpr int kTcN = 192;          // segments per tile (accumulator columns)
 constexpr int kTcK = 64;           // reduction window (128 bytes of fp16)
 constexpr int kTcBuilders = 256;   // warps 0-7
-constexpr int kTcThreads = kTcBuilders + 128;
-constexpr int kTmaWarp = 8, kMmaWarp = 9, kRecWarp = 10, kZeroWarp = 11;
+constexpr int kTcThreads = kTcBuilders + 96;
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kRecWarp = 10;
 constexpr int kStagesA = 2, kStagesB = 2;
 constexpr int kRecSlots = 4;       // windows of sparse entries staged in shared memory
 constexpr int kRecCap = 1536;      // entries staged per window (the rest are read from memory)
-// Mean entries per window from which a bulk zero-fill of the whole stage
-// (48 KB) is cheaper than clearing the previous window's entries one by one
-// (measured: 1200 entries per window gain 12%, 120 lose 8%).
+// Mean entries per window from which clearing the whole stage (48 KB of
+// 16-byte stores) is cheaper than clearing the previous window's entries one
+// by one (measured at 1200 entries per window: 13% faster; at 120: slower).
 constexpr int64_t kZeroFillEntries = 400;
 constexpr int kTcPeriod = 8;       // windows per accumulator turn
 constexpr int kTcGroupM = 8;       // dense-row tiles per raster group
@@ -234,8 +231,7 @@ struct TcArgs {
     const int32_t* row_exp;   // [b]
     const uint16_t* off;      // sparse entries in tile order: tile offsets
     const uint32_t* hl;       // and fp16 pieces
-    const void* zeros;        // kStageB zero bytes
-    int zero_fill;            // clear stages by bulk copy (dense windows) or entry by entry
+    int zero_fill;            // clear whole stages (dense windows) or entry by entry
     const int32_t* tile_ptr;  // [n_nt * n_win + 1]
     const int32_t* seg_exp;   // [n_seg]
     int64_t n_seg;
@@ -253,7 +249,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* sb = sa + kStagesA * kStageA;                                // B stages
     unsigned char* sr = sb + kStagesB * kStageB;                                // staged entries
     __shared__ uint64_t full_a[kStagesA], empty_a[kStagesA], full_b[kStagesB], empty_b[kStagesB];
-    __shared__ uint64_t rec_full[kRecSlots], rec_empty[kRecSlots], zeroed[kStagesB];
+    __shared__ uint64_t rec_full[kRecSlots], rec_empty[kRecSlots];
     __shared__ uint64_t accf[2], acce[2], fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -283,7 +279,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < kStagesB; ++i) {
             mbar_init(&full_b[i], kTcBuilders);
             mbar_init(&empty_b[i], 1);
-            mbar_init(&zeroed[i], 1);
         }
         for (int i = 0; i < kRecSlots; ++i) {
             mbar_init(&rec_full[i], 1);
@@ -308,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int64_t sg = s0 + t;
         pw_seg[t] = ldexpf(1.f, sg < a.n_seg ? a.seg_exp[sg] : 0);
     }
-    // the sparse stages start zeroed; afterwards only written positions are cleared
+    // the sparse stages start zeroed; later each is cleared before it is rewritten
     if (t < kTcBuilders) {
         uint4* pb = reinterpret_cast<uint4*>(sb);
         for (int i = t; i < kStagesB * kStageB / 16; i += kTcBuilders) pb[i] = make_uint4(0, 0, 0, 0);
@@ -333,22 +328,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_expect_tx(&full_a[s], kStageA);
                 tma_load_2d(st, &map_h, w * kTcK, (int)r0, &full_a[s]);
                 tma_load_2d(st + kPieceA, &map_l, w * kTcK, (int)r0, &full_a[s]);
-            }
-        }
-        __syncwarp();
-    } else if (warp == kZeroWarp) {
-        // ---------------------------------------------------------------- stage clears (bulk copy)
-        // once the MMAs of window w - kStagesB are done with a sparse stage,
-        // the copy engine writes it back to zeros for window w
-        if (lane == 0 && a.zero_fill) {
-            for (int w = kStagesB; w < n_win; ++w) {
-                const int s = w % kStagesB;
-                if (!mbar_wait(&empty_b[s], ((w / kStagesB) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                mbar_expect_tx(&zeroed[s], kStageB);
-                bulk_load(sb + s * kStageB, a.zeros, kStageB, &zeroed[s]);
             }
         }
         __syncwarp();
@@ -442,9 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         for (int w = 0; w < n_win; ++w) {
             const int s = w % kStagesB, r = w % kRecSlots;
-            if (w >= kStagesB &&
-                !mbar_wait(a.zero_fill ? &zeroed[s] : &empty_b[s], ((w / kStagesB) - 1) & 1))
-                ok = false;
+            if (w >= kStagesB && !mbar_wait(&empty_b[s], ((w / kStagesB) - 1) & 1)) ok = false;
             // turn q is complete once window (q+1)P - 1 has left its stage
             if (drained < n_per && w == (drained + 1) * kTcPeriod + kStagesB - 1) {
                 if (!drain(drained)) ok = false;
@@ -453,6 +430,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!mbar_wait(&rec_full[r], (w / kRecSlots) & 1)) ok = false;
             unsigned char* Bh = sb + s * kStageB;
             unsigned char* Bl = Bh + kPieceB;
+            if (a.zero_fill && w >= kStagesB && ok) {
+                // dense windows: 16-byte stores clear the whole stage
+                uint4* pb = reinterpret_cast<uint4*>(Bh);
+#pragma unroll 4
+                for (int i = t; i < kStageB / 16; i += kTcBuilders) pb[i] = make_uint4(0, 0, 0, 0);
+            }
             if (!a.zero_fill && w >= kStagesB && ok) {
                 // sparse windows: clear what window w - kStagesB wrote into
                 // this stage, then release its staging slot
@@ -1035,7 +1018,7 @@ void free_tc(Layer* L) {
     void* ptrs[] = {T->view[0].perm_t, T->view[0].off, T->view[0].tile_ptr, T->view[1].perm_t,
                     T->view[1].off, T->view[1].tile_ptr, T->view[2].perm_t, T->view[2].off,
                     T->view[2].tile_ptr, T->hl, T->seg_exp, T->col_exp, T->run_start, T->row_exp, T->dh,
-                    T->dl, T->zeros};
+                    T->dl};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete T;
@@ -1105,14 +1088,9 @@ int ensure_tc(Layer* L) {
     T->k_stride = ceil_div(std::max(L->out_f, L->in_f), 8) * 8;
     if (!tc_alloc(&T->hl, L->nnz + kTcPad) || !tc_alloc(&T->seg_exp, std::max(L->out_f, L->in_f)) ||
         !tc_alloc(&T->col_exp, L->in_f) || !tc_alloc(&T->row_exp, kTcChunk) ||
-        !tc_alloc(&T->dh, kTcChunk * T->k_stride) || !tc_alloc(&T->dl, kTcChunk * T->k_stride) ||
-        !tc_alloc((char**)&T->zeros, kStageB)) {
+        !tc_alloc(&T->dh, kTcChunk * T->k_stride) || !tc_alloc(&T->dl, kTcChunk * T->k_stride)) {
         free_tc(L);
         return SNK_ERR_OOM;
-    }
-    if (cudaMemset(T->zeros, 0, kStageB) != cudaSuccess) {
-        free_tc(L);
-        return SNK_ERR_CUDA;
     }
     return SNK_OK;
 }
@@ -1156,8 +1134,7 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
         a.row_exp = T->row_exp;
         a.off = V.off;
         a.hl = T->hl;
-        a.zeros = T->zeros;
-        // dense windows are cleared by the copy engine, sparse ones entry by entry
+        // dense windows are cleared whole, sparse ones entry by entry
         a.zero_fill = L->nnz >= kZeroFillEntries * V.n_tiles;
         a.tile_ptr = V.tile_ptr;
         a.seg_exp = T->seg_exp;
