@@ -339,8 +339,9 @@ int snk_copy_topology(snk_handle handle, int32_t* row_ptr, int32_t* col_ptr, int
  * Scratch: a fixed array inside the library image (2,574,352 bytes per GPU,
  * held for the life of the process).  Limits: out <= 524,288, at most 512
  * SMs, and the operand, in * (batch rounded up to a power of two, at most
- * 64) * 4 bytes, must fit one block's shared memory; larger requests return
- * SNK_ERR_LIMIT before any work is queued.  Every call shares the scratch and starts by clearing
+ * 64) * 4 bytes, together with the kernel's per-warp partial sums (about
+ * 12.5 KB at a batch of 64) must fit one block's shared memory; larger
+ * requests return SNK_ERR_LIMIT before any work is queued.  Every call shares the scratch and starts by clearing
  * the part it needs; calls whose kernels overlap on the GPU (other streams or
  * threads) race on it and must be serialised by the caller.
  * The first call on a device looks the scratch address up (once per device,

@@ -13,8 +13,8 @@ import re
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-# SNK_LIB selects another build of the library (for example a tuning variant)
-LIB_PATH = os.environ.get("SNK_LIB") or os.path.join(_PKG, "libsnk.so")
+# the in-tree library that build.py writes; nothing selects another one
+LIB_PATH = os.path.join(_PKG, "libsnk.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "snk.h")
 
 SNK_OK, SNK_ERR_ARG, SNK_ERR_DUP, SNK_ERR_RANGE = 0, 1, 2, 3

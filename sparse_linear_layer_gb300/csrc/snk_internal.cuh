@@ -178,6 +178,9 @@ int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row
                        int64_t out_f, int64_t in_f, int n_blocks, const float* X, int64_t b,
                        const float* bias, float* Y, float* part, int32_t* cnt, int max_smem,
                        cudaStream_t s);
+// Shared memory one block of the forward product on a caller's CSR takes for
+// an operand of in_f columns and a batch tile of bp columns.
+size_t forward_csr_smem(int64_t in_f, int bp);
 void free_restructure(Layer* L);
 
 }  // namespace snk

@@ -95,10 +95,11 @@ extern "C" int snk_forward_csr_noalloc(int64_t out_features, int64_t in_features
         cudaGetLastError();
         return SNK_ERR_CUDA;
     }
-    // the operand must fit shared memory for the largest batch tile used
+    // the operand and the kernel's partial-sum slots must fit one block's
+    // shared memory for the largest batch tile used (the first one), checked
+    // before anything is queued
     const int64_t tile = batch < kMaxBatchTile ? batch : kMaxBatchTile;
-    if ((int64_t)in_features * batch_tile(tile) * (int64_t)sizeof(float) > max_smem)
-        return SNK_ERR_LIMIT;
+    if (forward_csr_smem(in_features, batch_tile(tile)) > (size_t)max_smem) return SNK_ERR_LIMIT;
 
     // one block per SM, one chunk per warp
     const int n_blocks = num_sms;

@@ -452,6 +452,20 @@ static int launch_csr_bp(SpmmArgs a, int max_smem, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
+size_t forward_csr_smem(int64_t in_f, int bp) {
+    size_t slots = 0;
+    switch (bp) {
+        case 1: slots = spmm_slot_bytes<1, false>(); break;
+        case 2: slots = spmm_slot_bytes<2, false>(); break;
+        case 4: slots = spmm_slot_bytes<4, false>(); break;
+        case 8: slots = spmm_slot_bytes<8, false>(); break;
+        case 16: slots = spmm_slot_bytes<16, false>(); break;
+        case 32: slots = spmm_slot_bytes<32, false>(); break;
+        default: slots = spmm_slot_bytes<64, false>(); break;
+    }
+    return operand_floats(in_f, bp) * sizeof(float) + slots;
+}
+
 int launch_forward_csr(const float* val, const int32_t* cols, const int32_t* row_ptr,
                        const int4* cdesc, const BlockDesc* bdesc, const int32_t* bnd, int64_t nnz,
                        int64_t out_f, int64_t in_f, int n_blocks, const float* X, int64_t b,

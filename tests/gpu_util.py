@@ -29,10 +29,17 @@ def host(t):
 
 
 def assert_within(gpu, ref, A, what=""):
+    """Element-wise parity: where the oracle's result is finite, the GPU's is
+    finite and within 1e-5 * A + 1e-6 of it; where it is NaN or +-inf, the
+    GPU's is NaN or the same infinity."""
     gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    fin = np.isfinite(ref)
     err = np.abs(gpu - ref)
     bound = RTOL_A * A + ATOL
-    bad = err > bound
+    ok = np.where(fin, err <= bound,
+                  np.where(np.isnan(ref), np.isnan(gpu), gpu == ref))
+    bad = ~ok
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(
