@@ -58,17 +58,23 @@
  *     densified tile by tile in shared memory (never in device memory) and
  *     multiplied with the dense operand.  The environment variable
  *     SNK_LARGE_BATCH=on|off forces the choice for every batch size.
- *   - Numerics: every operand row is scaled by a power of two and split
- *     into two fp16 pieces.  The three products hi*hi, hi*lo and lo*hi carry
- *     about 22 bits.  The tensor core's fp32 accumulation truncates, so it
- *     is never chained over more than 8 windows of 64 terms (96 MMA steps).
- *     The partial results are then added in fp32 with round-to-nearest.
- *     The error stays inside the bound above even when every term has the
- *     same sign (about 4e-6 * A then).
- *   - Non-finite inputs: a densified tile also multiplies the stored zeros,
- *     so an inf or NaN in a row of X (dY) makes that whole output row NaN,
- *     and one in W makes its whole output column NaN.  The batch-tiled path
- *     propagates them per entry.
+ *   - Numerics: the same contract as above, for every input.  Every operand
+ *     row is scaled by a power of two and split into two fp16 pieces.  The
+ *     three products hi*hi, hi*lo and lo*hi carry about 22 bits.  The tensor
+ *     core's fp32 accumulation truncates, so it is never chained over more
+ *     than 8 windows of 64 terms (96 MMA steps); the partial results are
+ *     added in fp32 with round-to-nearest.  The error stays inside the bound
+ *     above even when every term has the same sign (about 4e-6 * A then).
+ *   - Inputs the split cannot carry are found by the per-call passes and
+ *     their outputs recomputed per stored entry on the CUDA cores (fp32, 32
+ *     partial sums and a tree, as in the batch-tiled kernels): a row of X
+ *     (dY) or a row / column of W holding an inf or NaN (a densified tile
+ *     would otherwise spread NaN over a whole output row or column, where the
+ *     definition gives NaN or +-inf only at the outputs an entry reaches), and
+ *     a row or segment whose values span more than about 2^16 when the fp16
+ *     floor of its small values could reach a quarter of the 1e-6 term.
+ *     Ordinary data (values within a few orders of magnitude of each other)
+ *     triggers neither; each call then costs three more small launches.
  *   - Memory, allocated on the first such call and kept until snk_destroy:
  *     about 22 bytes per stored entry (three tile-ordered views of 6 bytes
  *     and a 4-byte fp16 value pair), plus 32 KB per row or column of the
@@ -297,6 +303,21 @@ int snk_destroy(snk_handle handle);
 
 /* Text of a status code (static storage). */
 const char* snk_status_string(int status);
+
+/*
+ * snk_check - report a stopped product kernel.  The tensor-core kernels of
+ * the large-batch path (above) bound every wait of their pipeline (about two
+ * seconds).  A wait that runs out stops that kernel: it waits for the copies
+ * and tensor-core operations it has already issued, writes NaN to every
+ * output it owns (Y or dX entries, or the dW entries of its block), and
+ * records the event in the handle's device status word.  The product calls
+ * are asynchronous and cannot return that record themselves; this call
+ * synchronises `stream`, reads the word and clears it.  No page has a
+ * counterpart; it is part of the library's failure handling.
+ * Returns SNK_ERR_LIMIT if such a stop happened since the last snk_check
+ * (or since snk_create), SNK_OK if not; SNK_ERR_ARG, SNK_ERR_CUDA.
+ */
+int snk_check(snk_handle handle, void* stream);
 
 /*
  * snk_get_shape - sizes and the topology version of a handle.  The version

@@ -54,6 +54,7 @@ def lib():
         L.snk_get_shape.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                     ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.snk_copy_topology.argtypes = [P, P, P, P, P, P]
+        L.snk_check.argtypes = [P, P]
         L.snk_forward_csr_noalloc.argtypes = [i64, i64, i64, P, P, P, P, i64, P, P, P]
         L.snk_pcsr_build.argtypes = [P, I, P]
         L.snk_pcsr_info.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(i64),
@@ -65,7 +66,7 @@ def lib():
         L.snk_pcsr_export.argtypes = [P, P, P, P, i64, ctypes.POINTER(i64), P]
         for name in ("snk_create", "snk_forward", "snk_backward_input", "snk_backward_weight",
                      "snk_prune_regrow", "snk_prune_regrow_gradient", "snk_destroy",
-                     "snk_get_shape", "snk_copy_topology", "snk_forward_csr_noalloc",
+                     "snk_get_shape", "snk_copy_topology", "snk_check", "snk_forward_csr_noalloc",
                      "snk_pcsr_build", "snk_pcsr_info", "snk_pcsr_copy", "snk_pcsr_insert",
                      "snk_pcsr_delete", "snk_pcsr_compact", "snk_pcsr_export"):
             getattr(L, name).restype = I
@@ -149,6 +150,13 @@ def snk_prune_regrow_gradient(handle: int, zeta: float, X, dY, stream=None,
 
 def snk_destroy(handle: int):
     _check(lib().snk_destroy(handle), "snk_destroy")
+
+
+def snk_check(handle: int, stream=None):
+    """Synchronise the stream and raise SnkError(SNK_ERR_LIMIT) if a
+    tensor-core kernel of this handle stopped on a wait limit since the last
+    check (its outputs were written as NaN)."""
+    _check(lib().snk_check(handle, _stream(stream)), "snk_check")
 
 
 def snk_get_shape(handle: int):

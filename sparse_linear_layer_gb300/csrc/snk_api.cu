@@ -196,6 +196,25 @@ int snk_destroy(snk_handle h) {
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
+int snk_check(snk_handle h, void* stream) {
+    Layer* L = reinterpret_cast<Layer*>(h);
+    if (!L) return SNK_ERR_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t word = 0;
+    if (cudaMemcpyAsync(&word, L->status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return SNK_ERR_CUDA;
+    }
+    if (!(word & kStatLimit)) return SNK_OK;
+    if (cudaMemsetAsync(L->status, 0, sizeof(int32_t), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return SNK_ERR_CUDA;
+    }
+    return SNK_ERR_LIMIT;
+}
+
 int snk_get_shape(snk_handle h, int64_t* out_features, int64_t* in_features, int64_t* nnz,
                   int64_t* topology_version) {
     Layer* L = reinterpret_cast<Layer*>(h);

@@ -128,6 +128,50 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
 int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW, float* db,
                  cudaStream_t s);
 int refresh_tc_views(Layer* L, cudaStream_t s);
+
+// The tensor path's fp16 split holds a value x of a row scaled by 2^e to
+// within 2^-22 |x| while |x| 2^e >= 2^-3, and to an absolute 2^-25 * 2^-e
+// below that (fp16's subnormal spacing).  Per row (or segment of W) the
+// pre-passes record a code: bit 0 = it holds an inf or NaN, the bits above =
+// how many nonzero values it holds below 2^-3 after scaling ("tiny").  The
+// tiny values can add at most 2^-25 * 2^-e times the sum of the magnitudes
+// they meet on the other side, which is at most the largest L1 norm there,
+// and at most their count times the largest magnitude there.  The outputs are
+// recomputed exactly on the CUDA cores when bit 0 is set, or when that bound
+// exceeds kTcFloorBudget (a quarter of the 1e-6 absolute term of the
+// tolerance; the other side gets another quarter).
+constexpr float kTcFloorBudget = 2.5e-7f;
+__device__ __forceinline__ bool tc_needs_exact(int code, int e, float other_l1, float other_max) {
+    if (code & 1) return true;
+    const int n = code >> 1;
+    if (n == 0) return false;
+    return ldexpf(fminf(other_l1, (float)n * other_max), -25 - e) > kTcFloorBudget;
+}
+// One side of W for the exact recomputation: segment o holds entries
+// [ptr[o], ptr[o+1]) with operand index idx[j] and value val[perm[j]] (or
+// val[j] when perm is null).
+struct TcSide {
+    const int32_t* ptr;
+    const int32_t* idx;
+    const int32_t* perm;
+    const float* val;
+};
+// snk_tc_exact.cu: Y[rows[i], o] for every segment o (rows relative to D and
+// Y), for i < *n_rows.
+int launch_exact_rows(const TcSide& sd, int64_t n_seg, const float* D, int64_t K,
+                      const float* bias, float* Y, const int32_t* rows, const uint32_t* n_rows,
+                      int num_sms, cudaStream_t s);
+// Y[beta, o] for every beta < b and every candidate segment o that
+// tc_needs_exact confirms against other[0] (largest L1 norm of the dense rows)
+// and other[1] (their largest magnitude), both fp32 bit patterns.
+int launch_exact_segs(const TcSide& sd, int64_t n_seg, const float* D, int64_t K, int64_t b,
+                      const float* bias, float* Y, const int32_t* cand, const uint32_t* n_cand,
+                      const int32_t* seg_exp, const int32_t* seg_code, const uint32_t* other,
+                      int num_sms, cudaStream_t s);
+// dW for every entry of the listed rows (values below out) and columns
+// (out + column) of W, over the whole batch.
+int launch_exact_dw(const Layer* L, const float* X, const float* dY, int64_t b, float* dW,
+                    const int32_t* list, const uint32_t* n_list, cudaStream_t s);
 void mark_tc_views(Layer* L);
 void free_tc(Layer* L);
 

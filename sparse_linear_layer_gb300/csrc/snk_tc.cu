@@ -17,7 +17,10 @@
 // The tensor core's fp32 accumulation truncates, so one accumulator is never
 // chained over the whole reduction: two TMEM accumulators take turns, each
 // over kTcPeriod windows, and every finished one is added into fp32 registers
-// (round to nearest) while the other fills.
+// (round to nearest) while the other fills.  Rows and segments the split
+// cannot carry (an inf or NaN; values spanning more than ~2^16, see
+// tc_needs_exact) are flagged by the per-call passes and their outputs
+// recomputed per stored entry by the kernels of snk_tc_exact.cu.
 //
 // Forward and dX, per call: the dense operand is scaled and split once into
 // fp16 hi/lo arrays (k_tc_split), the values are put into tile order, scaled
@@ -67,6 +70,36 @@ struct TcState {
     __half* dh = nullptr;         // [kTcChunk * k_stride] dense operand, scaled, high part
     __half* dl = nullptr;         // the low part
     int64_t k_stride = 0;         // row stride of dh / dl: max(out, in) rounded up to 8
+    // outputs recomputed exactly (see tc_needs_exact): per segment of W (or,
+    // for dW, per column of dY) and per column of X the flag bits; the
+    // candidate segments; the flagged dense rows of the current chunk; the
+    // flagged rows / columns of W for dW (list and set); and the counters and
+    // maxima below
+    int32_t* seg_code = nullptr;  // [max(out, in)]
+    int32_t* col_code = nullptr;  // [in]
+    int32_t* cand = nullptr;      // [max(out, in)]
+    int32_t* frows = nullptr;     // [kTcChunk]
+    int32_t* dw_flag = nullptr;   // [out + in]
+    int32_t* dw_list = nullptr;   // [out + in]
+    uint32_t* fix = nullptr;      // [kFixWords]
+};
+
+// Words of TcState::fix: counters, and largest L1 norms and magnitudes as
+// fp32 bit patterns (non-negative, so integer atomicMax orders them).  Each
+// (L1, max) pair is adjacent: the exact kernels take a pointer to it.
+enum {
+    kFixRows = 0,     // flagged dense rows in the current chunk
+    kFixCand = 1,     // candidate segments
+    kFixSegL1 = 2,    // largest sum |v| over the segments of W
+    kFixSegMax = 3,   // largest |v| in W
+    kFixRowL1 = 4,    // largest sum |x| over the dense rows
+    kFixRowMax = 5,   // largest |x| in the dense operand
+    kFixDwList = 6,   // flagged rows / columns of W (weight gradient)
+    kFixDyL1 = 8,     // weight gradient, per batch chunk: largest column sum of |dY|
+    kFixDyMax = 9,    // largest |dY|
+    kFixXL1 = 10,     // largest column sum of |X|
+    kFixXMax = 11,    // largest |X|
+    kFixWords = 12
 };
 
 namespace {
@@ -95,7 +128,16 @@ constexpr int kTcSmem = kStagesA * kStageA + kStagesB * kStageB + kRecSlots * kR
 constexpr uint32_t kAccStride = 256;              // TMEM columns between the two accumulators
 constexpr uint32_t kTmemCols = 512;
 constexpr int kColsPerThread = kTcN / 2;          // accumulator columns each builder drains
-constexpr long long kTcWaitCycles = 4000000000LL; // about two seconds
+// Limit of a pipeline wait (about two seconds at the boost clock); a build
+// may shorten it (SNK_TC_WAIT_CYCLES) to exercise the abort path.  A wait
+// that runs out stops the CTA's pipeline: every role then waits, with the
+// fixed drain limit, for the copies and MMAs it has issued, the outputs are
+// written as NaN and the status word records kStatLimit.
+#ifndef SNK_TC_WAIT_CYCLES
+#define SNK_TC_WAIT_CYCLES 4000000000LL
+#endif
+constexpr long long kTcWaitCycles = SNK_TC_WAIT_CYCLES;
+constexpr long long kTcDrainCycles = 4000000000LL;
 // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major,
 // N = kTcN, M = kTcM.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
@@ -138,8 +180,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
                  : "memory");
 }
-// Bounded wait on a phase; false after about two seconds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+// Bounded wait on a phase; false once `limit` cycles have passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long long limit = kTcWaitCycles) {
     long long t0 = 0;
     for (int spin = 0;; ++spin) {
         uint32_t ok;
@@ -151,9 +193,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
         if (ok) return true;
         if (spin == 0)
             t0 = clock64();
-        else if (clock64() - t0 > kTcWaitCycles)
+        else if (clock64() - t0 > limit)
             return false;
     }
+}
+// After a pipeline stopped early: wait for the last `issued` uses of a ring of
+// `slots` barriers (window w used barrier w % slots in its (w / slots)-th
+// phase), i.e. for every copy still landing in shared memory.
+__device__ __forceinline__ bool drain_ring(uint64_t* bars, int slots, int issued) {
+    bool ok = true;
+    for (int w = issued > slots ? issued - slots : 0; w < issued; ++w)
+        if (!mbar_wait(&bars[w % slots], (w / slots) & 1, kTcDrainCycles)) ok = false;
+    return ok;
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -318,7 +369,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kTmaWarp) {
         // ---------------------------------------------------------------- dense tiles (TMA)
         if (lane == 0) {
-            for (int w = 0; w < n_win; ++w) {
+            int w = 0;
+            for (; w < n_win; ++w) {
                 const int s = w % kStagesA;
                 if (w >= kStagesA && !mbar_wait(&empty_a[s], ((w / kStagesA) - 1) & 1)) {
                     ok = false;
@@ -329,12 +381,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tma_load_2d(st, &map_h, w * kTcK, (int)r0, &full_a[s]);
                 tma_load_2d(st + kPieceA, &map_l, w * kTcK, (int)r0, &full_a[s]);
             }
+            if (!ok) drain_ring(full_a, kStagesA, w);
         }
         __syncwarp();
     } else if (warp == kRecWarp) {
         // ---------------------------------------------------------------- sparse entries (bulk copies)
         if (lane == 0) {
-            for (int w = 0; w < n_win; ++w) {
+            int w = 0;
+            for (; w < n_win; ++w) {
                 const int r = w % kRecSlots;
                 if (w >= kRecSlots && !mbar_wait(&rec_empty[r], ((w / kRecSlots) - 1) & 1)) {
                     ok = false;
@@ -356,6 +410,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (bc) bulk_load(slot, a.off + ca, bc, &rec_full[r]);
                 if (bv) bulk_load(slot + kRecCap * 2, a.hl + va, bv, &rec_full[r]);
             }
+            if (!ok) drain_ring(rec_full, kRecSlots, w);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -386,9 +441,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (w + kStagesB < n_win) mma_commit(&empty_b[s_b]);
                 if ((w % kTcPeriod) == kTcPeriod - 1 || w == n_win - 1) mma_commit(&accf[ab]);
             }
-            // every MMA issued has completed once fin completes
+            // every MMA issued has completed once fin completes (also after
+            // an early stop: TMEM and the stages are released only then)
             mma_commit(&fin);
-            if (!mbar_wait(&fin, 0)) ok = false;
+            if (!mbar_wait(&fin, 0, kTcDrainCycles)) ok = false;
         }
         __syncwarp();
     } else {
@@ -507,47 +563,83 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-// Dense operand, once per call: per row the scale exponent, and the scaled
-// values split into fp16 hi / lo at row stride ks (one block per row).
+// Dense operand, once per call: per row the scale exponent of its largest
+// finite magnitude, and the scaled values split into fp16 hi / lo at row
+// stride ks (one block per row; non-finite values are split as zeros).  The
+// row's code (an inf or NaN; the count of nonzero values below 2^-3 after
+// scaling) is checked against W's largest segment sum and magnitude
+// (tc_needs_exact); a row that fails is listed in rows[] for the exact
+// recomputation.  The row's sum of finite magnitudes and its largest one go
+// into the running maxima that the segments' own check uses.
 template <bool VEC>
 __global__ void k_tc_split(const float* __restrict__ D, int64_t len, int64_t ks, int32_t* __restrict__ e_out,
-                           __half* __restrict__ dh, __half* __restrict__ dl) {
-    __shared__ float red[32];
+                           __half* __restrict__ dh, __half* __restrict__ dl, int32_t* __restrict__ rows,
+                           uint32_t* __restrict__ fix) {
+    __shared__ float red[3][32];
+    __shared__ int red_n[32];
     const int64_t r = blockIdx.x;
     const float* p = D + r * len;
-    float m = 0.f;
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5, lane = threadIdx.x & 31;
+    float m = 0.f, sum = 0.f, nf = 0.f;
+    auto take = [&](float x) {
+        x = fabsf(x);
+        if (isfinite(x)) {
+            m = fmaxf(m, x);
+            sum += x;
+        } else {
+            nf = 1.f;
+        }
+    };
     if (VEC) {
         for (int64_t k = 4 * threadIdx.x; k < len; k += 4 * blockDim.x) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(p + k));
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            take(v.x);
+            take(v.y);
+            take(v.z);
+            take(v.w);
         }
     } else {
-        for (int64_t k = threadIdx.x; k < len; k += blockDim.x) m = fmaxf(m, fabsf(p[k]));
+        for (int64_t k = threadIdx.x; k < len; k += blockDim.x) take(p[k]);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (threadIdx.x == 0) red[0] = m;
+    for (int o = 16; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        nf = fmaxf(nf, __shfl_xor_sync(0xffffffffu, nf, o));
+    }
+    if (lane == 0) {
+        red[0][w] = m;
+        red[1][w] = sum;
+        red[2][w] = nf;
     }
     __syncthreads();
-    const int e = tc_exponent(red[0]);
-    if (threadIdx.x == 0) e_out[r] = e;
+    m = 0.f;
+    sum = 0.f;
+    nf = 0.f;
+    for (int i = 0; i < nw; ++i) {   // every thread reduces the warp results in the same order
+        m = fmaxf(m, red[0][i]);
+        sum += red[1][i];
+        nf = fmaxf(nf, red[2][i]);
+    }
+    const int e = tc_exponent(m);
     const float pw = ldexpf(1.f, e);
+    const float tiny = ldexpf(0.125f, -e);
+    int n_tiny = 0;
+    auto scaled = [&](float x) {
+        const float ax = fabsf(x);
+        n_tiny += (ax > 0.f && ax < tiny) ? 1 : 0;
+        return isfinite(x) ? x * pw : 0.f;
+    };
     __half* oh = dh + r * ks;
     __half* ol = dl + r * ks;
     if (VEC) {
         for (int64_t k = 4 * threadIdx.x; k < len; k += 4 * blockDim.x) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(p + k));
             __half h0, h1, h2, h3, l0, l1, l2, l3;
-            split16(v.x * pw, h0, l0);
-            split16(v.y * pw, h1, l1);
-            split16(v.z * pw, h2, l2);
-            split16(v.w * pw, h3, l3);
+            split16(scaled(v.x), h0, l0);
+            split16(scaled(v.y), h1, l1);
+            split16(scaled(v.z), h2, l2);
+            split16(scaled(v.w), h3, l3);
             uint2 hh, ll;
             hh.x = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
             hh.y = (uint32_t)__half_as_ushort(h2) | ((uint32_t)__half_as_ushort(h3) << 16);
@@ -559,10 +651,24 @@ __global__ void k_tc_split(const float* __restrict__ D, int64_t len, int64_t ks,
     } else {
         for (int64_t k = threadIdx.x; k < len; k += blockDim.x) {
             __half h, l;
-            split16(p[k] * pw, h, l);
+            split16(scaled(p[k]), h, l);
             oh[k] = h;
             ol[k] = l;
         }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n_tiny += __shfl_xor_sync(0xffffffffu, n_tiny, o);
+    if (lane == 0) red_n[w] = n_tiny;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int i = 0; i < nw; ++i) n += red_n[i];
+        e_out[r] = e;
+        const int cd = (nf > 0.f ? 1 : 0) | (n << 1);
+        if (tc_needs_exact(cd, e, __uint_as_float(fix[kFixSegL1]), __uint_as_float(fix[kFixSegMax])))
+            rows[atomicAdd(fix + kFixRows, 1u)] = (int32_t)r;
+        atomicMax(fix + kFixRowL1, __float_as_uint(sum));
+        atomicMax(fix + kFixRowMax, __float_as_uint(m));
     }
 }
 
@@ -643,7 +749,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
     if (warp == kTmaWarp) {
         if (lane == 0) {
-            for (int w = 0; w < n_win; ++w) {
+            int w = 0;
+            for (; w < n_win; ++w) {
                 const int s = w & 1;
                 if (w >= 2 && !mbar_wait(&empty[s], ((w >> 1) - 1) & 1)) {
                     ok = false;
@@ -656,6 +763,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 tma_load_2d(st + kStageA, &map_bh, w * kTcK, (int)i0, &full[s]);
                 tma_load_2d(st + kStageA + kPieceB, &map_bl, w * kTcK, (int)i0, &full[s]);
             }
+            if (!ok) drain_ring(full, 2, w);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -684,7 +792,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 if ((w % kTcPeriod) == kTcPeriod - 1 || w == n_win - 1) mma_commit(&accf[ab]);
             }
             mma_commit(&fin);
-            if (!mbar_wait(&fin, 0)) ok = false;
+            if (!mbar_wait(&fin, 0, kTcDrainCycles)) ok = false;
         }
         __syncwarp();
     } else {
@@ -710,9 +818,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tc_fence_before();
             mbar_arrive(&acce[ab]);
         }
-        // every MMA has completed (all turns drained): the stages hold the sums tile
-        if (!builders_any(!ok)) {
-            float* tile = reinterpret_cast<float*>(sm);
+        // every MMA has completed (all turns drained): the stages hold the
+        // sums tile.  After an early stop the block's entries get NaN instead,
+        // so no stale gradient is left behind.
+        const bool stopped = builders_any(!ok);
+        float* tile = reinterpret_cast<float*>(sm);
+        if (!stopped) {
             const int row = 32 * lq + lane;
             const float ir = ipw_row[row];
 #pragma unroll
@@ -721,15 +832,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 tile[row * kWStride + col] = (acc[j] * ir) * ipw_col[col];
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kTcBuilders) : "memory");
-            const int32_t* tp = a.tile_ptr + (int64_t)ot * a.n_it + it;
-            const int j1 = tp[1];
-            for (int j = tp[0] + t; j < j1; j += kTcBuilders) {
-                const float v = tile[a.off[j]];
-                float* dst = a.dW + a.perm[j];
-                *dst = a.accumulate ? *dst + v : v;
-            }
         } else {
             ok = false;
+        }
+        const int32_t* tp = a.tile_ptr + (int64_t)ot * a.n_it + it;
+        const int j1 = tp[1];
+        for (int j = tp[0] + t; j < j1; j += kTcBuilders) {
+            float* dst = a.dW + a.perm[j];
+            if (stopped) {
+                *dst = __int_as_float(0x7fc00000);
+            } else {
+                const float v = tile[a.off[j]];
+                *dst = a.accumulate ? *dst + v : v;
+            }
         }
     }
     if (!ok) atomicExch(&abort_flag, 1);
@@ -743,24 +858,36 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
 }
 
-// Per column of D [rows, n]: the scale exponent of its largest magnitude and,
-// if sum is given, its sum (written, or added when accumulate), summed in
-// runs of 32 rows and then pairwise so no fp32 chain exceeds ~45 terms.
+// Per column of D [rows, n]: the scale exponent of its largest finite
+// magnitude, its code's inf / NaN bit (k_tc_tsplit adds the count of values
+// under the fp16 floor; see tc_needs_exact), the running maxima over columns
+// of the sum of finite magnitudes and of the largest one (l1max[0], l1max[1],
+// fp32 bit patterns) and, if sum is given, the column's plain sum (written,
+// or added when accumulate), summed in runs of 32 rows and then pairwise so
+// no fp32 chain exceeds ~45 terms; an inf or NaN propagates into that sum as
+// it does in the definition.
 template <bool SUM>
 __global__ void __launch_bounds__(256) k_tc_colstats(const float* __restrict__ D, int64_t rows, int64_t n,
-                                                     int32_t* __restrict__ e_out, float* __restrict__ sum,
+                                                     int32_t* __restrict__ e_out, int32_t* __restrict__ code,
+                                                     uint32_t* __restrict__ l1max, float* __restrict__ sum,
                                                      int accumulate) {
-    __shared__ float sm_max[8][32], sm_sum[8][32];
+    __shared__ float sm_max[8][32], sm_sum[8][32], sm_abs[8][32], sm_nf[8][32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t col = (int64_t)blockIdx.x * 32 + lane;
-    float m = 0.f, tot = 0.f;
+    float m = 0.f, tot = 0.f, ab = 0.f, nf = 0.f;
     if (col < n) {
         for (int64_t g = w; g * 32 < rows; g += 8) {
             float part = 0.f;
             const int64_t r1 = min(rows, g * 32 + 32);
             for (int64_t r = g * 32; r < r1; ++r) {
                 const float x = D[r * n + col];
-                m = fmaxf(m, fabsf(x));
+                const float ax = fabsf(x);
+                if (isfinite(ax)) {
+                    m = fmaxf(m, ax);
+                    ab += ax;
+                } else {
+                    nf = 1.f;
+                }
                 if (SUM) part += x;
             }
             if (SUM) tot += part;
@@ -768,9 +895,15 @@ __global__ void __launch_bounds__(256) k_tc_colstats(const float* __restrict__ D
     }
     sm_max[w][lane] = m;
     sm_sum[w][lane] = tot;
+    sm_abs[w][lane] = ab;
+    sm_nf[w][lane] = nf;
     __syncthreads();
     if (w == 0 && col < n) {
-        for (int i = 1; i < 8; ++i) m = fmaxf(m, sm_max[i][lane]);
+        for (int i = 1; i < 8; ++i) {
+            m = fmaxf(m, sm_max[i][lane]);
+            ab += sm_abs[i][lane];
+            nf = fmaxf(nf, sm_nf[i][lane]);
+        }
         if (SUM) {
             const float s01 = sm_sum[0][lane] + sm_sum[1][lane], s23 = sm_sum[2][lane] + sm_sum[3][lane];
             const float s45 = sm_sum[4][lane] + sm_sum[5][lane], s67 = sm_sum[6][lane] + sm_sum[7][lane];
@@ -778,13 +911,42 @@ __global__ void __launch_bounds__(256) k_tc_colstats(const float* __restrict__ D
             sum[col] = accumulate ? sum[col] + s : s;
         }
         e_out[col] = tc_exponent(m);
+        code[col] = nf > 0.f ? 1 : 0;
+        atomicMax(l1max, __float_as_uint(ab));
+        atomicMax(l1max + 1, __float_as_uint(m));
+    }
+}
+
+// Weight gradient, per batch chunk: the rows (dY columns, list value r) and
+// columns (X columns, list value out + c) of W whose entries are recomputed
+// exactly (tc_needs_exact against the other operand's maxima, scaled by the
+// number of chunks, since each chunk adds its own floor error), each listed
+// once per call however many chunks flag it.
+__global__ void k_tc_dw_decide(const int32_t* __restrict__ e_row, const int32_t* __restrict__ code_row,
+                               const int32_t* __restrict__ e_col, const int32_t* __restrict__ code_col,
+                               int64_t out_f, int64_t in_f, float n_chunks, int32_t* __restrict__ flag,
+                               int32_t* __restrict__ list, uint32_t* __restrict__ fix) {
+    const float dy_l1 = __uint_as_float(fix[kFixDyL1]) * n_chunks;
+    const float dy_mx = __uint_as_float(fix[kFixDyMax]) * n_chunks;
+    const float x_l1 = __uint_as_float(fix[kFixXL1]) * n_chunks;
+    const float x_mx = __uint_as_float(fix[kFixXMax]) * n_chunks;
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < out_f + in_f;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const bool is_row = u < out_f;
+        const int64_t i = is_row ? u : u - out_f;
+        const bool need = is_row ? tc_needs_exact(code_row[i], e_row[i], x_l1, x_mx)
+                                 : tc_needs_exact(code_col[i], e_col[i], dy_l1, dy_mx);
+        if (need && atomicOr(flag + u, 1) == 0) list[atomicAdd(fix + kFixDwList, 1u)] = (int32_t)u;
     }
 }
 
 // out[c][r] = split(D[r][c] * 2^e[c]) for r < rows, c < n: the transposed,
-// scaled fp16 pieces (row stride bs) the weight-gradient product loads.
+// scaled fp16 pieces (row stride bs) the weight-gradient product loads
+// (non-finite values are split as zeros); each column's count of nonzero
+// values below 2^-3 after scaling is added into its code (2 per value).
 __global__ void k_tc_tsplit(const float* __restrict__ D, int64_t rows, int64_t n, const int32_t* __restrict__ e,
-                            int64_t bs, __half* __restrict__ oh, __half* __restrict__ ol) {
+                            int64_t bs, __half* __restrict__ oh, __half* __restrict__ ol,
+                            int32_t* __restrict__ code) {
     __shared__ float tile[32][33];
     const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
     const int64_t c0 = (int64_t)blockIdx.x * 32, r0 = (int64_t)blockIdx.y * 32;
@@ -797,28 +959,72 @@ __global__ void k_tc_tsplit(const float* __restrict__ D, int64_t rows, int64_t n
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int64_t c = c0 + ty + 8 * i, r = r0 + tx;
+        int n_tiny = 0;
         if (c < n && r < rows) {
             __half h, l;
-            split16(tile[tx][ty + 8 * i] * ldexpf(1.f, e[c]), h, l);
+            const float x = tile[tx][ty + 8 * i];
+            const int ex = e[c];
+            const float ax = fabsf(x);
+            n_tiny = (ax > 0.f && ax < ldexpf(0.125f, -ex)) ? 1 : 0;
+            split16(isfinite(x) ? x * ldexpf(1.f, ex) : 0.f, h, l);
             oh[c * bs + r] = h;
             ol[c * bs + r] = l;
         }
+        // the 32 lanes of this warp hold the rows of one column
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n_tiny += __shfl_xor_sync(0xffffffffu, n_tiny, o);
+        if (tx == 0 && n_tiny) atomicAdd(code + c, 2 * n_tiny);
     }
 }
 
 // ------------------------------------------------------------ per-call passes
-// Scale exponent of each segment (row of W, or column through perm).
+// Per segment of W (a row, or a column through perm): the scale exponent of
+// its largest finite magnitude and its code (tc_needs_exact: an inf or NaN,
+// and the count of nonzero values below 2^-3 after scaling); segments with a
+// nonzero code become candidates for the exact recomputation.  Also the
+// largest sum of finite magnitudes over the segments and the largest
+// magnitude, which the dense rows' own check uses.
 __global__ void k_tc_seg_exp(const int32_t* __restrict__ ptr, const float* __restrict__ v,
-                             const int32_t* __restrict__ perm, int64_t n_seg, int32_t* __restrict__ e) {
+                             const int32_t* __restrict__ perm, int64_t n_seg, int32_t* __restrict__ e,
+                             int32_t* __restrict__ code, int32_t* __restrict__ cand, uint32_t* __restrict__ fix) {
     const int lane = threadIdx.x & 31;
     for (int64_t sg = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; sg < n_seg;
          sg += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-        float m = 0.f;
-        for (int k = ptr[sg] + lane; k < ptr[sg + 1]; k += 32)
-            m = fmaxf(m, fabsf(perm ? v[perm[k]] : v[k]));
+        const int k0 = ptr[sg], k1 = ptr[sg + 1];
+        float m = 0.f, sum = 0.f;
+        bool nf = false;
+        for (int k = k0 + lane; k < k1; k += 32) {
+            const float x = fabsf(perm ? v[perm[k]] : v[k]);
+            if (isfinite(x)) {
+                m = fmaxf(m, x);
+                sum += x;
+            } else {
+                nf = true;
+            }
+        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) e[sg] = tc_exponent(m);
+        for (int o = 16; o > 0; o >>= 1) {
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        }
+        nf = __any_sync(0xffffffffu, nf);
+        const int ex = tc_exponent(m);
+        const float tiny = ldexpf(0.125f, -ex);
+        int n_tiny = 0;
+        for (int k = k0 + lane; k < k1; k += 32) {
+            const float x = fabsf(perm ? v[perm[k]] : v[k]);
+            n_tiny += (x > 0.f && x < tiny) ? 1 : 0;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n_tiny += __shfl_xor_sync(0xffffffffu, n_tiny, o);
+        if (lane == 0) {
+            const int cd = (nf ? 1 : 0) | (n_tiny << 1);
+            e[sg] = ex;
+            code[sg] = cd;
+            if (cd) cand[atomicAdd(fix + kFixCand, 1u)] = (int32_t)sg;
+            atomicMax(fix + kFixSegL1, __float_as_uint(sum));
+            atomicMax(fix + kFixSegMax, __float_as_uint(m));
+        }
     }
 }
 
@@ -831,8 +1037,11 @@ __global__ void k_tc_values(const float* __restrict__ v, const int32_t* __restri
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
         const int32_t k = perm_t[j];
+        const float x = v[k];
         __half h, l;
-        split16(v[k] * ldexpf(1.f, seg_exp[seg_of[k]]), h, l);
+        // an inf or NaN flags its segment for the exact recomputation; the
+        // tile holds a zero in its place
+        split16(isfinite(x) ? x * ldexpf(1.f, seg_exp[seg_of[k]]) : 0.f, h, l);
         hl[j] = (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(l) << 16);
     }
 }
@@ -1018,7 +1227,7 @@ void free_tc(Layer* L) {
     void* ptrs[] = {T->view[0].perm_t, T->view[0].off, T->view[0].tile_ptr, T->view[1].perm_t,
                     T->view[1].off, T->view[1].tile_ptr, T->view[2].perm_t, T->view[2].off,
                     T->view[2].tile_ptr, T->hl, T->seg_exp, T->col_exp, T->run_start, T->row_exp, T->dh,
-                    T->dl};
+                    T->dl, T->seg_code, T->col_code, T->cand, T->frows, T->dw_flag, T->dw_list, T->fix};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete T;
@@ -1088,7 +1297,11 @@ int ensure_tc(Layer* L) {
     T->k_stride = ceil_div(std::max(L->out_f, L->in_f), 8) * 8;
     if (!tc_alloc(&T->hl, L->nnz + kTcPad) || !tc_alloc(&T->seg_exp, std::max(L->out_f, L->in_f)) ||
         !tc_alloc(&T->col_exp, L->in_f) || !tc_alloc(&T->row_exp, kTcChunk) ||
-        !tc_alloc(&T->dh, kTcChunk * T->k_stride) || !tc_alloc(&T->dl, kTcChunk * T->k_stride)) {
+        !tc_alloc(&T->dh, kTcChunk * T->k_stride) || !tc_alloc(&T->dl, kTcChunk * T->k_stride) ||
+        !tc_alloc(&T->seg_code, std::max(L->out_f, L->in_f)) || !tc_alloc(&T->col_code, L->in_f) ||
+        !tc_alloc(&T->cand, std::max(L->out_f, L->in_f)) || !tc_alloc(&T->frows, kTcChunk) ||
+        !tc_alloc(&T->dw_flag, L->out_f + L->in_f) || !tc_alloc(&T->dw_list, L->out_f + L->in_f) ||
+        !tc_alloc(&T->fix, kFixWords)) {
         free_tc(L);
         return SNK_ERR_OOM;
     }
@@ -1111,20 +1324,29 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
     int64_t n_seg, k_len;
     tc_shape(L, columns, &n_seg, &k_len);
     const int TH = 256;
+    if (cudaMemsetAsync(T->fix, 0, kFixWords * sizeof(uint32_t), s) != cudaSuccess) return SNK_ERR_CUDA;
     k_tc_seg_exp<<<grid_for(n_seg * 32, TH, L->num_sms), TH, 0, s>>>(
-        columns ? L->col_ptr : L->row_ptr, L->v, columns ? L->perm : nullptr, n_seg, T->seg_exp);
+        columns ? L->col_ptr : L->row_ptr, L->v, columns ? L->perm : nullptr, n_seg, T->seg_exp,
+        T->seg_code, T->cand, T->fix);
     k_tc_values<<<grid_for(L->nnz, TH, L->num_sms), TH, 0, s>>>(L->v, V.perm_t, columns ? L->c : L->r,
                                                                 T->seg_exp, L->nnz, T->hl);
     if (cudaFuncSetAttribute(k_tc_spmm, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
         return SNK_ERR_CUDA;
     const bool vec = (k_len % 4) == 0 && ((uintptr_t)D & 15) == 0;
+    // the entries of the segments, for the exact recomputation of flagged outputs
+    TcSide side{columns ? L->col_ptr : L->row_ptr, columns ? L->rows_c : L->c, columns ? L->perm : nullptr,
+                L->v};
     for (int64_t c0 = 0; c0 < b; c0 += kTcChunk) {
         const int bc = (int)std::min<int64_t>(kTcChunk, b - c0);
         const float* Dc = D + c0 * k_len;
+        if (c0 > 0 && cudaMemsetAsync(T->fix + kFixRows, 0, sizeof(uint32_t), s) != cudaSuccess)
+            return SNK_ERR_CUDA;
         if (vec)
-            k_tc_split<true><<<bc, TH, 0, s>>>(Dc, k_len, T->k_stride, T->row_exp, T->dh, T->dl);
+            k_tc_split<true><<<bc, TH, 0, s>>>(Dc, k_len, T->k_stride, T->row_exp, T->dh, T->dl, T->frows,
+                                               T->fix);
         else
-            k_tc_split<false><<<bc, TH, 0, s>>>(Dc, k_len, T->k_stride, T->row_exp, T->dh, T->dl);
+            k_tc_split<false><<<bc, TH, 0, s>>>(Dc, k_len, T->k_stride, T->row_exp, T->dh, T->dl, T->frows,
+                                                T->fix);
         CUtensorMap mh, ml;
         if (!encode_map(&mh, T->dh, k_len, bc, T->k_stride) || !encode_map(&ml, T->dl, k_len, bc, T->k_stride))
             return SNK_ERR_CUDA;
@@ -1146,8 +1368,15 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
         a.Y = Y + c0 * n_seg;
         a.status = L->status;
         k_tc_spmm<<<a.n_mt * a.n_nt, kTcThreads, kTcSmem, s>>>(mh, ml, a);
+        // dense rows of this chunk that the split cannot carry: every output
+        // of theirs again, per stored entry
+        int st = launch_exact_rows(side, n_seg, Dc, k_len, bias, Y + c0 * n_seg, T->frows,
+                                   T->fix + kFixRows, L->num_sms, s);
+        if (st != SNK_OK) return st;
     }
-    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+    // segments of W that the split cannot carry, for every dense row
+    return launch_exact_segs(side, n_seg, D, k_len, b, bias, Y, T->cand, T->fix + kFixCand, T->seg_exp,
+                             T->seg_code, T->fix + kFixRowL1, L->num_sms, s);
 }
 
 int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW, float* db,
@@ -1164,6 +1393,9 @@ int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW
     if (cudaFuncSetAttribute(k_tc_sddmm, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem) != cudaSuccess)
         return SNK_ERR_CUDA;
     const int64_t out_f = L->out_f, in_f = L->in_f;
+    if (cudaMemsetAsync(T->fix, 0, kFixWords * sizeof(uint32_t), s) != cudaSuccess ||
+        cudaMemsetAsync(T->dw_flag, 0, (out_f + in_f) * sizeof(int32_t), s) != cudaSuccess)
+        return SNK_ERR_CUDA;
     // batch rows per chunk: the transposed pieces of dY and X share the workspace
     const int64_t cap = (kTcChunk * T->k_stride) / (out_f + in_f);
     const int64_t chunk = std::max<int64_t>(kTcK, cap / kTcK * kTcK);
@@ -1173,20 +1405,28 @@ int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW
         const float* dYc = dY + c0 * out_f;
         const float* Xc = X + c0 * in_f;
         const int acc = c0 > 0;
+        if (c0 > 0 && cudaMemsetAsync(T->fix + kFixDyL1, 0, 4 * sizeof(uint32_t), s) != cudaSuccess)
+            return SNK_ERR_CUDA;
         if (db)
-            k_tc_colstats<true><<<(unsigned)ceil_div(out_f, 32), 256, 0, s>>>(dYc, bc, out_f, T->seg_exp, db, acc);
+            k_tc_colstats<true><<<(unsigned)ceil_div(out_f, 32), 256, 0, s>>>(
+                dYc, bc, out_f, T->seg_exp, T->seg_code, T->fix + kFixDyL1, db, acc);
         else
-            k_tc_colstats<false><<<(unsigned)ceil_div(out_f, 32), 256, 0, s>>>(dYc, bc, out_f, T->seg_exp, nullptr, 0);
-        k_tc_colstats<false><<<(unsigned)ceil_div(in_f, 32), 256, 0, s>>>(Xc, bc, in_f, T->col_exp, nullptr, 0);
+            k_tc_colstats<false><<<(unsigned)ceil_div(out_f, 32), 256, 0, s>>>(
+                dYc, bc, out_f, T->seg_exp, T->seg_code, T->fix + kFixDyL1, nullptr, 0);
+        k_tc_colstats<false><<<(unsigned)ceil_div(in_f, 32), 256, 0, s>>>(Xc, bc, in_f, T->col_exp, T->col_code,
+                                                                          T->fix + kFixXL1, nullptr, 0);
         __half* ah = T->dh;
         __half* al = T->dl;
         __half* bh = T->dh + out_f * bs;
         __half* bl = T->dl + out_f * bs;
         const dim3 tb(32, 8);
         k_tc_tsplit<<<dim3((unsigned)ceil_div(out_f, 32), (unsigned)ceil_div(bc, 32)), tb, 0, s>>>(
-            dYc, bc, out_f, T->seg_exp, bs, ah, al);
+            dYc, bc, out_f, T->seg_exp, bs, ah, al, T->seg_code);
         k_tc_tsplit<<<dim3((unsigned)ceil_div(in_f, 32), (unsigned)ceil_div(bc, 32)), tb, 0, s>>>(
-            Xc, bc, in_f, T->col_exp, bs, bh, bl);
+            Xc, bc, in_f, T->col_exp, bs, bh, bl, T->col_code);
+        k_tc_dw_decide<<<grid_for(out_f + in_f, 256, L->num_sms), 256, 0, s>>>(
+            T->seg_exp, T->seg_code, T->col_exp, T->col_code, out_f, in_f, (float)ceil_div(b, chunk),
+            T->dw_flag, T->dw_list, T->fix);
         CUtensorMap mah, mal, mbh, mbl;
         if (!encode_map(&mah, ah, bc, out_f, bs, kTcM) || !encode_map(&mal, al, bc, out_f, bs, kTcM) ||
             !encode_map(&mbh, bh, bc, in_f, bs, kTcN) || !encode_map(&mbl, bl, bc, in_f, bs, kTcN))
@@ -1207,7 +1447,9 @@ int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW
         a.status = L->status;
         k_tc_sddmm<<<a.n_ot * a.n_it, kWThreads, kWSmem, s>>>(mah, mal, mbh, mbl, a);
     }
-    return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
+    // rows and columns of W flagged by any chunk: their entries again, over the whole batch
+    return launch_exact_dw(L, X, dY, b, dW, T->dw_list, T->fix + kFixDwList, s);
 }
 
 }  // namespace snk

@@ -35,7 +35,8 @@ def assert_within(gpu, ref, A, what=""):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     fin = np.isfinite(ref)
-    err = np.abs(gpu - ref)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(gpu - ref)
     bound = RTOL_A * A + ATOL
     ok = np.where(fin, err <= bound,
                   np.where(np.isnan(ref), np.isnan(gpu), gpu == ref))

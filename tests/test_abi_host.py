@@ -20,7 +20,7 @@ def test_every_declared_symbol_is_exported(L):
     names = binding.declared_symbols()
     assert {"snk_create", "snk_forward", "snk_backward_input", "snk_backward_weight",
             "snk_prune_regrow", "snk_destroy", "snk_status_string", "snk_get_shape",
-            "snk_copy_topology"} <= set(names)
+            "snk_copy_topology", "snk_check", "snk_forward_csr_noalloc"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
 

@@ -12,8 +12,11 @@ tensor cores with an fp16 hi/lo split of both operands.  The cases here:
   benchmark, checking rows at the edges of the 128-row batch tiles;
 - use inputs that are all positive, where a long chain in the tensor core's
   truncating fp32 accumulator would drift outside the tolerance;
-- rebuild the tile-ordered views after a restructure, and replay a CUDA graph.
-Every element is compared with |gpu - oracle| <= 1e-5 * A + 1e-6.
+- rebuild the tile-ordered views after a restructure, and replay a CUDA graph;
+- feed inf and NaN, and rows or segments whose values span 1e8, which the
+  fp16 split cannot carry: those outputs are recomputed per stored entry.
+Every element is compared with |gpu - oracle| <= 1e-5 * A + 1e-6 (and the same
+NaN or infinity where the oracle has one).
 """
 import numpy as np
 import pytest
@@ -189,23 +192,137 @@ def test_graph_replay_matches_direct(torch, monkeypatch):
     g.close()
 
 
-def test_non_finite_input_row(torch, monkeypatch):
-    """A NaN in one row of X makes that whole row of Y NaN on this path (the
-    densified tiles multiply it by the stored zeros too); every other row
-    still matches the oracle."""
+def _split_repr(a, axis):
+    """Host emulation of the tensor path's operand split: each row (axis=1)
+    or column (axis=0) scaled by the power of two that brings its largest
+    finite magnitude into [2^13, 2^14), written as fp16 hi + fp16 lo, and
+    scaled back.  Used only to show that an input defeats the split."""
+    a = np.asarray(a, np.float32)
+    mag = np.where(np.isfinite(a), np.abs(a), 0).astype(np.float64)
+    m = mag.max(axis=axis, keepdims=True)
+    ex = np.where(m > 0, 14 - np.frexp(np.where(m > 0, m, 1.0))[1], 0)
+    s = np.ldexp(a.astype(np.float64), ex)
+    hi = s.astype(np.float16).astype(np.float64)
+    lo = (s - hi).astype(np.float16).astype(np.float64)
+    return np.ldexp(hi + lo, -ex)
+
+
+def _violates(gpu_like, ref, A):
+    err = np.abs(np.asarray(gpu_like, np.float64) - ref)
+    return bool((err > 1e-5 * A + 1e-6).any())
+
+
+def test_non_finite_inputs_follow_the_definition(torch, monkeypatch):
+    """inf and NaN in X, dY and W: the outputs match the oracle entry by
+    entry (NaN where it has NaN, the same infinity where it has one, within
+    the tolerance elsewhere), although a densified tile multiplies the stored
+    zeros too: the rows and segments holding them are recomputed per entry."""
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
-    lay = synth.make_layer(300, 200, 90, 0.05, 103, 104)
-    b = 130
-    X = synth.normal((b, 200), 1.0, 105)
+    out_f, in_f, b = 300, 200, 130
+    lay = synth.make_layer(out_f, in_f, 90, 0.05, 103, 104)
+    can = oracle.canonicalize(out_f, in_f, lay.values, lay.rows, lay.cols)
+    v, r, c = can["values"].copy(), can["rows"], can["cols"]
+    X = synth.normal((b, in_f), 1.0, 105)
+    dY = synth.normal((b, out_f), 1.0, 106)
+    # a row whose two stored columns meet +inf and -inf (NaN there), a NaN,
+    # an inf that meets a stored zero (NaN), and infinities in the tail tile
+    k0 = int(can["row_ptr"][40])
+    ca, cb = int(c[k0]), int(c[k0 + 1])
+    v[k0], v[k0 + 1] = 0.5, 0.5
+    X[3, ca], X[3, cb] = np.inf, -np.inf
     X[7, 11] = np.nan
-    g = make_gpu_layer(torch, lay)
-    can = oracle.canonicalize(300, 200, lay.values, lay.rows, lay.cols)
-    Y = host(g.forward(dev(X, torch)))
-    assert np.isnan(Y[7]).all()
-    keep = np.arange(b) != 7
-    Yr, Ay = oracle.forward(300, 200, can["values"], can["rows"], can["cols"], X[keep], None)
-    assert_within(Y[keep], Yr, Ay, "rows without the NaN")
-    g.close()
+    kz = int(can["row_ptr"][90])
+    v[kz] = 0.0
+    X[64, int(c[kz])] = np.inf
+    X[129, 0] = -np.inf
+    dY[5, 17] = np.nan
+    dY[128, 299] = np.inf
+    dY[70, r[k0]] = -np.inf
+    # non-finite values in W: each poisons one segment of either side
+    v[int(can["row_ptr"][150])] = np.inf
+    v[int(can["row_ptr"][151])] = np.nan
+    v[int(can["row_ptr"][299])] = -np.inf
+    bias = synth.normal(out_f, 0.1, 107)
+    lay2 = synth.Layer(out_f, in_f, v, r, c)
+    _check(torch, lay2, X, dY, bias)
+
+
+def test_wide_range_dense_rows(torch, monkeypatch):
+    """Rows of X and dY holding one value near 1e8 among N(0, 1) values: after
+    scaling, the small values fall under fp16's normal range.  The emulated
+    split alone misses the tolerance; the library recomputes those rows."""
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    out_f, in_f, b = 300, 200, 130
+    lay = synth.make_layer(out_f, in_f, 90, 0.05, 111, 112)
+    can = oracle.canonicalize(out_f, in_f, lay.values, lay.rows, lay.cols)
+    X = synth.normal((b, in_f), 1.0, 113)
+    dY = synth.normal((b, out_f), 1.0, 114)
+    X[5, 17] = 1.0e8
+    X[100, 3] = -3.0e7
+    dY[9, 250] = 1.0e8
+    Yr, Ay = oracle.forward(out_f, in_f, can["values"], can["rows"], can["cols"], X, None)
+    Ye, _ = oracle.forward(out_f, in_f, can["values"], can["rows"], can["cols"],
+                           _split_repr(X, 1).astype(np.float32), None)
+    assert _violates(Ye, Yr, Ay), "the case must defeat the plain split"
+    dXr, Ax = oracle.backward_input(out_f, in_f, can["values"], can["rows"], can["cols"], dY)
+    dXe, _ = oracle.backward_input(out_f, in_f, can["values"], can["rows"], can["cols"],
+                                   _split_repr(dY, 1).astype(np.float32))
+    assert _violates(dXe, dXr, Ax), "the case must defeat the plain split"
+    _check(torch, lay, X, dY, None)
+
+
+def test_wide_range_segments_of_w(torch, monkeypatch):
+    """A row and a column of W each holding one value near 1e8 among
+    N(0, 0.05^2) values, with the operand zero where that value would make
+    the tolerance loose: the emulated split of W alone misses it; the library
+    recomputes those segments for every batch row."""
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    out_f, in_f, b = 300, 200, 130
+    lay = synth.make_layer(out_f, in_f, 90, 0.05, 121, 122)
+    can = oracle.canonicalize(out_f, in_f, lay.values, lay.rows, lay.cols)
+    v, r, c = can["values"].copy(), can["rows"], can["cols"]
+    k_big = int(can["row_ptr"][33])        # forward: row 33 of W
+    v[k_big] = 1.0e8
+    c_big = int(c[k_big])
+    col_idx = np.nonzero(c == 77)[0]       # dX: column 77 of W
+    k_col = int(col_idx[0])
+    v[k_col] = -1.0e8
+    r_col = int(r[k_col])
+    X = synth.normal((b, in_f), 1.0, 123)
+    dY = synth.normal((b, out_f), 1.0, 124)
+    X[::2, c_big] = 0.0                    # half the rows do not meet the big value
+    dY[::2, r_col] = 0.0
+    Yr, Ay = oracle.forward(out_f, in_f, v, r, c, X, None)
+    We = np.empty_like(v)
+    for o in range(out_f):
+        lo_, hi_ = int(can["row_ptr"][o]), int(can["row_ptr"][o + 1])
+        if hi_ > lo_:
+            We[lo_:hi_] = _split_repr(v[lo_:hi_][None, :], 1)[0]
+    Ye, _ = oracle.forward(out_f, in_f, We.astype(np.float32), r, c, X, None)
+    assert _violates(Ye, Yr, Ay), "the case must defeat the plain split"
+    _check(torch, synth.Layer(out_f, in_f, v, r, c), X, dY, None)
+
+
+def test_wide_range_weight_gradient_columns(torch, monkeypatch):
+    """dW when a column of dY and a column of X hold one value near 1e8 among
+    N(0, 1) values (with zeros where it would make the tolerance loose): the
+    rows and columns of W they feed are recomputed over the whole batch."""
+    monkeypatch.setenv("SNK_LARGE_BATCH", "on")
+    out_f, in_f, b = 300, 200, 130
+    lay = synth.make_layer(out_f, in_f, 90, 0.05, 131, 132)
+    X = synth.normal((b, in_f), 1.0, 133)
+    dY = synth.normal((b, out_f), 1.0, 134)
+    dY[4, 21] = 1.0e8
+    X[4, :] = 0.0                          # the big dY value meets no X value
+    X[9, 150] = -1.0e8
+    dY[9, :] = 0.0
+    can = oracle.canonicalize(out_f, in_f, lay.values, lay.rows, lay.cols)
+    dWr, Aw, _, _ = oracle.backward_weight(out_f, in_f, can["rows"], can["cols"], X, dY)
+    dWe, _, _, _ = oracle.backward_weight(out_f, in_f, can["rows"], can["cols"],
+                                          _split_repr(X, 0).astype(np.float32),
+                                          _split_repr(dY, 0).astype(np.float32))
+    assert _violates(dWe, dWr, Aw), "the case must defeat the plain split"
+    _check(torch, lay, X, dY, None)
 
 
 def test_batch_chunks_and_empty_segments(torch, monkeypatch):
