@@ -10,19 +10,20 @@ weight gradient on the support (dW, with db).  The restructure
 (``restructure`` key).
 
 Metric: microseconds per call and achieved HBM GB/s for forward / dX / dW.
-``value`` = algorithmic bytes of the step's three kernels / their summed
-device time, over all ranks (GB/s).  L2 is flushed (a 512 MB write) before
-every kernel, outside the timed interval; each kernel is bracketed by CUDA
-events on the stream it is launched on.
+``value`` = the contract bytes of the step's three kernels / their summed
+device time, over all ranks (GB/s).  The contract bytes per call are the
+layer's formula: nnz*12 + b*(in+out)*4 for forward and dX, plus nnz*4 (the
+gradient written) for dW.  L2 is flushed (a 512 MB write) before every
+kernel, outside the timed interval; each kernel is bracketed by CUDA events
+on the stream it is launched on.  ``sweep`` repeats the three calls over
+b = 1..64 at 90 / 95 / 99 % sparsity.
 
-Algorithmic bytes per launch (what each kernel must move at least; i is the
-width of the index copy it reads: 2 bytes on the shared-memory operand path,
-else 4):
+The minimal bytes each kernel must move with the index width it reads (i: 2
+bytes for the 16-bit copies of the shared-memory operand path, else 4) are
+reported beside them (``frac_minimal``):
   forward  nnz*(4+i) (values, cols) + (out+1)*4 (row_ptr) + b*in*4 (X) + b*out*4 (Y) + out*4 (bias)
   dX       nnz*(i+4+4) (rows in column order, perm, values) + (in+1)*4 + b*out*4 + b*in*4
   dW       nnz*(i+4) (cols read, dW written) + (out+1)*4 + b*(in+out)*4 (X, dY) + out*4 (db)
-The contract formula bytes (nnz*12 + b*(in+out)*4, plus nnz*4 for dW) are
-reported beside them as ``formula``.
 
 --impl reference runs the CPU oracle (the plain fp64 reference) on the host
 cores instead, each step a bounded sample of the same workload.
@@ -77,6 +78,8 @@ def parse():
                         "tiling) to FILE")
     p.add_argument("--no-large-batch", action="store_true",
                    help="leave the large-batch measurement out of the single line")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="leave the b = 1..64 x 90/95/99 %% sweep out of the single line")
     return p.parse_args()
 
 
@@ -283,8 +286,8 @@ def run_reference(args, workload, rank, world):
     dt = time.perf_counter() - t0
     # bytes of the sampled work: entries scale the triple terms; the dense
     # operands are counted for the rows touched
-    alg, _ = op_bytes(args.out, args.inp, lay0.nnz, b)
-    total_bytes = sum(alg.values()) * (nnz_done / lay0.nnz if lay0.nnz else 0.0)
+    _, formula = op_bytes(args.out, args.inp, lay0.nnz, b)
+    total_bytes = sum(formula.values()) * (nnz_done / lay0.nnz if lay0.nnz else 0.0)
     value = total_bytes / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
@@ -315,11 +318,16 @@ def tc_path(out_f, in_f, nnz, b):
 
 
 def tc_launches(op, out_f, in_f, b):
+    """Kernels per call on the tensor-core path: per batch chunk the column
+    passes, the flag decision, the transposes and the product, plus the exact
+    recomputation of flagged entries (dW); the segment and value passes, per
+    chunk the split, the product and the exact recomputation of flagged rows,
+    plus that of flagged segments (forward, dX)."""
     if op == "dw":
         k_stride = (max(out_f, in_f) + 7) // 8 * 8
         chunk = max(64, (TC_CHUNK * k_stride) // (out_f + in_f) // 64 * 64)
-        return 5 * ((b + chunk - 1) // chunk)
-    return 2 + 2 * ((b + TC_CHUNK - 1) // TC_CHUNK)
+        return 6 * ((b + chunk - 1) // chunk) + 1
+    return 3 + 3 * ((b + TC_CHUNK - 1) // TC_CHUNK)
 
 
 def launches_per_op(n_src, b, max_smem):
@@ -333,7 +341,10 @@ def launches_per_op(n_src, b, max_smem):
     return launches
 
 
-def time_cpu_baseline(lay, X, dY, budget_s=12.0, max_steps=25):
+def time_cpu_baseline(lay, X, dY, budget_s=12.0, max_steps=25, omp=False):
+    """Full oracle steps (forward, dX, dW) of the layer until the budget is
+    spent; omp runs the OpenMP build of the same source on every core this
+    process may use."""
     import oracle
     oracle.build()
     can = oracle.canonicalize(lay.out_f, lay.in_f, lay.values, lay.rows, lay.cols)
@@ -341,9 +352,9 @@ def time_cpu_baseline(lay, X, dY, budget_s=12.0, max_steps=25):
     steps = 0
     t0 = time.perf_counter()
     while steps < max_steps and (time.perf_counter() - t0) < budget_s:
-        oracle.forward(lay.out_f, lay.in_f, v, r, c, X, None)
-        oracle.backward_input(lay.out_f, lay.in_f, v, r, c, dY)
-        oracle.backward_weight(lay.out_f, lay.in_f, r, c, X, dY)
+        oracle.forward(lay.out_f, lay.in_f, v, r, c, X, None, omp=omp)
+        oracle.backward_input(lay.out_f, lay.in_f, v, r, c, dY, omp=omp)
+        oracle.backward_weight(lay.out_f, lay.in_f, r, c, X, dY, omp=omp)
         steps += 1
     return steps, time.perf_counter() - t0
 
@@ -422,15 +433,18 @@ def gather_reference(torch, g, flush, stream, dx_us):
 
 
 def summarize(per_op_ms, alg, formula, peak):
+    """Per op: event-timed µs, and GB/s and fraction of the HBM peak on the
+    contract (formula) bytes, with the minimal-bytes figures beside them."""
     out = {}
     for n, v in per_op_ms.items():
         mean_us = sum(v) / len(v) * 1e3
         srt = sorted(v)
         out[n] = {"us_median": statistics.median(v) * 1e3, "us_mean": mean_us,
                   "us_p10": srt[len(v) // 10] * 1e3, "us_p90": srt[(9 * len(v)) // 10] * 1e3,
-                  "gbs": alg[n] / (mean_us * 1e-6) / 1e9,
-                  "frac": alg[n] / (mean_us * 1e-6) / 1e9 / peak,
-                  "formula_gbs": formula[n] / (mean_us * 1e-6) / 1e9}
+                  "gbs": formula[n] / (mean_us * 1e-6) / 1e9,
+                  "frac": formula[n] / (mean_us * 1e-6) / 1e9 / peak,
+                  "minimal_gbs": alg[n] / (mean_us * 1e-6) / 1e9,
+                  "frac_minimal": alg[n] / (mean_us * 1e-6) / 1e9 / peak}
     return out
 
 
@@ -443,6 +457,44 @@ def make_device_layer(torch, binding, synth, dev, out_f, in_f, sparsity, b):
     td = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     g = binding.SparseLinear(out_f, in_f, td(lay.values), td(lay.rows), td(lay.cols))
     return lay, g, X_h, dY_h, td(X_h), td(dY_h), td(bias_h)
+
+
+SWEEP_SPARSITY = (90, 95, 99)
+SWEEP_BATCHES = (1, 2, 4, 8, 16, 32, 64)
+
+
+def sweep_points(torch, binding, synth, dev, out_f, in_f, flush, stream, steps, warmup,
+                 layers=None):
+    """The metric's range: forward, dX and dW at b = 1..64 on the layer at
+    90 / 95 / 99 % sparsity, each call event-timed after an L2 flush.  Per
+    point: mean µs and the fraction of the HBM peak on the contract bytes.
+    layers maps a sparsity to an existing (synth layer, handle) to reuse."""
+    peak, _ = measured_peaks()
+    max_smem = torch.cuda.get_device_properties(dev).shared_memory_per_block_optin
+    pts = []
+    for sp in SWEEP_SPARSITY:
+        own = not (layers and sp in layers)
+        if own:
+            lay, g, _, _, _, _, _ = make_device_layer(torch, binding, synth, dev, out_f, in_f, sp, 1)
+        else:
+            lay, g = layers[sp]
+        bias = torch.zeros(out_f, device=dev)
+        for b in SWEEP_BATCHES:
+            X = torch.randn(b, in_f, device=dev)
+            dY = torch.randn(b, out_f, device=dev)
+            Y = torch.empty(b, out_f, device=dev)
+            dX = torch.empty(b, in_f, device=dev)
+            dW = torch.empty(lay.nnz, device=dev)
+            db = torch.empty(out_f, device=dev)
+            ms = time_ops(binding, g, X, dY, bias, Y, dX, dW, db, flush, stream, steps, warmup)
+            alg, formula = op_bytes(out_f, in_f, lay.nnz, b, max_smem)
+            summ = summarize(ms, alg, formula, peak)
+            pts.append({"sparsity_pct": sp, "batch": b,
+                        "us": {n: round(v["us_mean"], 2) for n, v in summ.items()},
+                        "frac": {n: round(v["frac"], 4) for n, v in summ.items()}})
+        if own:
+            g.close()
+    return pts
 
 
 def run_sweep(args, dev):
@@ -742,7 +794,7 @@ def run_ours(args, workload, rank, world, local):
     total_ms = reduce_max_ms(sum(sum(v) for v in per_op_ms.values()), dev)
     max_smem = torch.cuda.get_device_properties(dev).shared_memory_per_block_optin
     alg, formula = op_bytes(out_f, in_f, nnz, b, max_smem)
-    step_bytes = sum(alg[n] for n in per_op_ms)
+    step_bytes = sum(formula[n] for n in per_op_ms)
     value = aggregate_gbs(world, step_bytes, args.steps, total_ms)
     peak, peak_kind = measured_peaks()
     per_op = summarize(per_op_ms, alg, formula, peak)
@@ -766,8 +818,14 @@ def run_ours(args, workload, rank, world, local):
         roofline = {
             "bound": "hbm", "kernel": kernel_tags[dom], "op": dom, "achieved": per_op[dom]["gbs"],
             "peak": peak, "peak_kind": f"hbm_gbs, {peak_kind}", "unit": "GB/s",
-            "frac": per_op[dom]["frac"], "traffic": committed_traffic(kernel_tags[dom], workload["workload"]),
-            "algorithmic_bytes_per_launch": alg[dom], "per_op": per_op,
+            "frac": per_op[dom]["frac"], "frac_formula": per_op[dom]["frac"],
+            "frac_minimal": per_op[dom]["frac_minimal"],
+            "traffic": committed_traffic(kernel_tags[dom], workload["workload"]),
+            "algorithmic_bytes_per_launch": formula[dom], "minimal_bytes_per_launch": alg[dom],
+            "bytes_note": "achieved/frac use the contract bytes (nnz*12 + b*(in+out)*4, + nnz*4 "
+                          "for dW); frac_minimal uses the bytes the kernel must move with the "
+                          "index width it reads",
+            "per_op": per_op,
         }
         if not args.only and lay.nnz > 0:
             roofline["onchip"] = gather_reference(torch, g, flush, stream, per_op["dx"]["us_mean"])
@@ -824,6 +882,16 @@ def run_ours(args, workload, rank, world, local):
                        "overlaps the kernels not waiting for them; dW stays on the device for "
                        "the optimizer; L2 flushed before each step only"}
 
+    # ---- the metric's range: b = 1..64 at 90 / 95 / 99 % (the step's layer is reused)
+    sweep = None
+    if rank == 0 and world == 1 and args.only is None and (out_f, in_f) == (10000, 10000) \
+            and b <= 64 and not args.no_sweep:
+        reuse = {int(args.sparsity): (lay, g)} if float(args.sparsity).is_integer() else None
+        sweep = {"layer": f"{out_f}x{in_f}", "steps": 20, "warmup": 3,
+                 "unit": "us per call (mean) and fraction of the HBM peak on the contract bytes",
+                 "points": sweep_points(torch, binding, synth, dev, out_f, in_f, flush, stream, 20, 3,
+                                        reuse)}
+
     # ---- restructure (SET cadence work), timed separately
     restructure = None
     if rank == 0 and not args.no_restructure:
@@ -863,10 +931,25 @@ def run_ours(args, workload, rank, world, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         steps_c, dt_c = time_cpu_baseline(lay, X_h, dY_h)
-        cpu = {"value": sum(alg.values()) * steps_c / dt_c / 1e9, "unit": "GB/s", "cores": 1,
+        cpu = {"value": sum(formula.values()) * steps_c / dt_c / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle",
                "sample": f"{steps_c} full steps (forward + dX + dW, fp64 accumulation) of the same "
                          f"{out_f}x{in_f} layer, batch {b}, single-threaded"}
+        import oracle
+        if oracle.openmp_available():
+            cores = len(os.sched_getaffinity(0))
+            os.environ["OMP_NUM_THREADS"] = str(cores)
+            os.environ.setdefault("OMP_PROC_BIND", "false")
+            steps_o, dt_o = time_cpu_baseline(lay, X_h, dY_h, budget_s=8.0, omp=True)
+            cpu["openmp"] = {
+                "value": sum(formula.values()) * steps_o / dt_o / 1e9, "unit": "GB/s",
+                "cores": oracle.threads(omp=True), "affinity_cores": cores, "kind": "oracle",
+                "sample": f"{steps_o} full steps of the same layer and batch, the oracle's "
+                          f"source built with OpenMP: outputs split statically over the cores "
+                          f"(rows for the forward, columns for dX, entries for dW), the same "
+                          f"bits as the single-threaded build"}
+        else:
+            cpu["openmp"] = None
 
     if rank == 0:
         line = {
@@ -876,7 +959,9 @@ def run_ours(args, workload, rank, world, local):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload,
             "us_per_call": us, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk.summary(), "restructure": restructure,
-            "large_batch": large,
+            "large_batch": large, "sweep": sweep,
+            "library": {"path": os.path.relpath(binding.LIB_PATH, ROOT),
+                        "source_digest": kernel_source_digest()},
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line), flush=True)

@@ -20,7 +20,7 @@ __all__ = [
     "backward_weight", "prune_count", "prune", "regrow", "prune_regrow",
     "grad_at", "grad_key", "grad_keys", "grow_gradient", "grad_count_below",
     "prune_regrow_gradient",
-    "splitmix64_nth", "mulhi64", "candidate", "regrow_limit",
+    "splitmix64_nth", "mulhi64", "candidate", "regrow_limit", "openmp_available", "threads",
     "ORC_OK", "ORC_ERR_ARG", "ORC_ERR_DUP", "ORC_ERR_RANGE", "ORC_ERR_OOM",
     "ORC_ERR_NOSPACE", "ORC_ERR_LIMIT",
 ]
@@ -32,8 +32,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "snk_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libsnk_oracle.so")
+# the same source built with OpenMP: the products split their outputs among
+# the host's cores (same terms in the same order per output, same bits); used
+# for the benchmark's all-core CPU baseline
+_OMP_PATH = os.path.join(_OUT_DIR, "libsnk_oracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_omp_lib = None
 
 
 class OracleError(RuntimeError):
@@ -42,25 +47,42 @@ class OracleError(RuntimeError):
         self.status = status
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (portable C, no target-specific flags)."""
+def _compile(path: str, extra, force: bool) -> str:
     os.makedirs(_OUT_DIR, exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    stale = (not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC))
     if force or stale:
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp,
+        tmp = path + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", *extra, "-o", tmp,
                         _SRC, "-lm"], check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+        os.replace(tmp, path)
+    return path
 
 
-def _load():
-    global _lib
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (portable C, no target-specific flags),
+    single-threaded, and the same source with OpenMP when the compiler has
+    it (the all-core CPU baseline; tests use the single-threaded build)."""
+    path = _compile(_LIB_PATH, [], force)
+    try:
+        _compile(_OMP_PATH, ["-fopenmp"], force)
+    except (subprocess.CalledProcessError, OSError):
+        pass
+    return path
+
+
+def openmp_available() -> bool:
+    build()
+    return os.path.exists(_OMP_PATH)
+
+
+def _load(omp: bool = False):
+    global _lib, _omp_lib
+    if omp and not openmp_available():
+        raise OracleError(-1, "OpenMP build not available")
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
+        if (_omp_lib if omp else _lib) is not None:
+            return _omp_lib if omp else _lib
+        lib = ctypes.CDLL(_OMP_PATH if omp else build())
         i64, u64, f32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
         P = ctypes.c_void_p
         lib.orc_canonicalize.argtypes = [i64, i64, i64, P, P, P, P, P, P, P]
@@ -97,8 +119,18 @@ def _load():
         lib.orc_mulhi64.restype = u64
         lib.orc_candidate.argtypes = [u64, u64, u64]
         lib.orc_candidate.restype = u64
-        _lib = lib
+        lib.orc_threads.argtypes = []
+        lib.orc_threads.restype = ctypes.c_int
+        if omp:
+            _omp_lib = lib
+        else:
+            _lib = lib
         return lib
+
+
+def threads(omp: bool = False) -> int:
+    """Threads the products of a build use (1 without OpenMP)."""
+    return int(_load(omp).orc_threads())
 
 
 def _ptr(a):
@@ -131,9 +163,10 @@ def canonicalize(out_f: int, in_f: int, v, r, c):
                 rows_c=rows_c, perm=perm)
 
 
-def forward(out_f: int, in_f: int, v, r, c, X, bias=None):
-    """Y = X (W.M)^T + bias in fp64, and the magnitude sum A ([PCSR] sec. 6.1)."""
-    lib = _load()
+def forward(out_f: int, in_f: int, v, r, c, X, bias=None, omp: bool = False):
+    """Y = X (W.M)^T + bias in fp64, and the magnitude sum A ([PCSR] sec. 6.1).
+    omp: run the OpenMP build (same bits)."""
+    lib = _load(omp)
     v, r, c, X = _f32(v), _i32(r), _i32(c), _f32(X)
     b = X.shape[0]
     assert X.shape == (b, in_f)
@@ -145,9 +178,9 @@ def forward(out_f: int, in_f: int, v, r, c, X, bias=None):
     return Y, A
 
 
-def backward_input(out_f: int, in_f: int, v, r, c, dY):
+def backward_input(out_f: int, in_f: int, v, r, c, dY, omp: bool = False):
     """dX = dY (W.M) in fp64, and its magnitude sum ([PCSR] sec. 7.1)."""
-    lib = _load()
+    lib = _load(omp)
     v, r, c, dY = _f32(v), _i32(r), _i32(c), _f32(dY)
     b = dY.shape[0]
     assert dY.shape == (b, out_f)
@@ -158,9 +191,9 @@ def backward_input(out_f: int, in_f: int, v, r, c, dY):
     return dX, A
 
 
-def backward_weight(out_f: int, in_f: int, r, c, X, dY):
+def backward_weight(out_f: int, in_f: int, r, c, X, dY, omp: bool = False):
     """dW on the support and db, each with its magnitude sum ([PCSR] sec. 7.1)."""
-    lib = _load()
+    lib = _load(omp)
     r, c, X, dY = _i32(r), _i32(c), _f32(X), _f32(dY)
     b = X.shape[0]
     assert X.shape == (b, in_f) and dY.shape == (b, out_f)

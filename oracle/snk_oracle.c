@@ -42,6 +42,40 @@
 #include <stdlib.h>
 #include <string.h>
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Multi-core build.  Built with -fopenmp, the three products split their    */
+/* OUTPUTS among threads, in the spirit of [PCSR] sec. 6.3's static split of */
+/* rows over cores: each thread owns a contiguous block of output rows       */
+/* (forward) or columns (input gradient), walks the whole triple in the      */
+/* given order and skips entries whose output it does not own; the weight    */
+/* gradient's entries are independent and are split statically.  Every      */
+/* output therefore receives the same terms in the same order as in the      */
+/* single-threaded build, so both builds give identical bits.  Without      */
+/* OpenMP there is one block holding every output.                          */
+/* ------------------------------------------------------------------------ */
+static void orc_my_block(int64_t n, int64_t* lo, int64_t* hi) {
+#ifdef _OPENMP
+    const int64_t nt = omp_get_num_threads(), t = omp_get_thread_num();
+    *lo = n * t / nt;
+    *hi = n * (t + 1) / nt;
+#else
+    *lo = 0;
+    *hi = n;
+#endif
+}
+
+/* Threads the products use (1 in the single-threaded build). */
+int orc_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 enum {
     ORC_OK = 0,
@@ -154,12 +188,18 @@ void orc_forward(int64_t out_f, int64_t in_f, int64_t nnz,
             if (A) A[beta * out_f + o] = fabs(bo);
         }
     }
-    for (int64_t k = 0; k < nnz; ++k) {
-        double w = (double)v[k];
-        for (int64_t beta = 0; beta < b; ++beta) {
-            double x = (double)X[beta * in_f + c[k]];
-            Y[beta * out_f + r[k]] += w * x;
-            if (A) A[beta * out_f + r[k]] += fabs(w * x);
+#pragma omp parallel
+    {
+        int64_t o0, o1;
+        orc_my_block(out_f, &o0, &o1);
+        for (int64_t k = 0; k < nnz; ++k) {
+            if (r[k] < o0 || r[k] >= o1) continue;
+            double w = (double)v[k];
+            for (int64_t beta = 0; beta < b; ++beta) {
+                double x = (double)X[beta * in_f + c[k]];
+                Y[beta * out_f + r[k]] += w * x;
+                if (A) A[beta * out_f + r[k]] += fabs(w * x);
+            }
         }
     }
 }
@@ -176,12 +216,18 @@ void orc_backward_input(int64_t out_f, int64_t in_f, int64_t nnz,
         dX[q] = 0.0;
         if (A) A[q] = 0.0;
     }
-    for (int64_t k = 0; k < nnz; ++k) {
-        double w = (double)v[k];
-        for (int64_t beta = 0; beta < b; ++beta) {
-            double g = (double)dY[beta * out_f + r[k]];
-            dX[beta * in_f + c[k]] += w * g;
-            if (A) A[beta * in_f + c[k]] += fabs(w * g);
+#pragma omp parallel
+    {
+        int64_t i0, i1;
+        orc_my_block(in_f, &i0, &i1);
+        for (int64_t k = 0; k < nnz; ++k) {
+            if (c[k] < i0 || c[k] >= i1) continue;
+            double w = (double)v[k];
+            for (int64_t beta = 0; beta < b; ++beta) {
+                double g = (double)dY[beta * out_f + r[k]];
+                dX[beta * in_f + c[k]] += w * g;
+                if (A) A[beta * in_f + c[k]] += fabs(w * g);
+            }
         }
     }
 }
@@ -199,6 +245,7 @@ void orc_backward_weight(int64_t out_f, int64_t in_f, int64_t nnz,
                          const int32_t* r, const int32_t* c,
                          const float* X, const float* dY, int64_t b,
                          double* dW, double* A_dW, double* db, double* A_db) {
+#pragma omp parallel for schedule(static)
     for (int64_t k = 0; k < nnz; ++k) {
         double s = 0.0, a = 0.0;
         for (int64_t beta = 0; beta < b; ++beta) {

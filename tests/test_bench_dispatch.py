@@ -45,15 +45,17 @@ def test_rule(monkeypatch):
 
 @pytest.mark.parametrize("b", [256, 4096, 4097, 10_000])
 def test_launch_counts(b):
-    # forward / dX: segment scales and tile-order values once, then a split
-    # and a product kernel per chunk of kTcChunk rows
+    # forward / dX: segment scales and tile-order values once, then a split,
+    # a product and an exact-row kernel per chunk of kTcChunk rows, and one
+    # exact-segment kernel
     chunks = -(-b // bench.TC_CHUNK)
-    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 2 + 2 * chunks
-    # dW: two column passes, two transposes and a product kernel per chunk;
-    # the chunk is what the shared fp16 workspace holds for both operands
+    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 3 + 3 * chunks
+    # dW: two column passes, a flag decision, two transposes and a product
+    # kernel per chunk, then one exact-entry kernel; the chunk is what the
+    # shared fp16 workspace holds for both operands
     k_stride = 10_000
     chunk = (bench.TC_CHUNK * k_stride) // 20_000 // 64 * 64
-    assert bench.tc_launches("dw", 10_000, 10_000, b) == 5 * (-(-b // chunk))
+    assert bench.tc_launches("dw", 10_000, 10_000, b) == 6 * (-(-b // chunk)) + 1
 
 
 def test_source_digest_ignores_comments():

@@ -540,3 +540,27 @@ def test_prune_regrow_gradient_invariants():
                                  X, dY, k)
     assert set(lin.tolist()) == set(kept_lin) | set(grown.tolist())
     assert len(set(kept_lin) & set(grown.tolist())) == 0
+
+
+def test_openmp_build_gives_the_same_bits():
+    """The OpenMP build of the oracle (the benchmark's all-core CPU baseline)
+    splits outputs among threads but adds each output's terms in the same
+    order, so it must return exactly the single-threaded results, also on a
+    triple in random order and with empty rows."""
+    if not oracle.openmp_available():
+        pytest.skip("gcc without OpenMP")
+    lay = synth.make_layer(333, 257, 80, 0.05, 71, 72)
+    X = synth.normal((5, 257), 1.0, 73)
+    dY = synth.normal((5, 333), 1.0, 74)
+    bias = synth.normal(333, 0.1, 75)
+    v, r, c = lay.values, lay.rows, lay.cols
+    for a, b_ in zip(oracle.forward(333, 257, v, r, c, X, bias),
+                     oracle.forward(333, 257, v, r, c, X, bias, omp=True)):
+        assert np.array_equal(a, b_)
+    for a, b_ in zip(oracle.backward_input(333, 257, v, r, c, dY),
+                     oracle.backward_input(333, 257, v, r, c, dY, omp=True)):
+        assert np.array_equal(a, b_)
+    for a, b_ in zip(oracle.backward_weight(333, 257, r, c, X, dY),
+                     oracle.backward_weight(333, 257, r, c, X, dY, omp=True)):
+        assert np.array_equal(a, b_)
+    assert oracle.threads(omp=False) == 1
