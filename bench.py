@@ -305,16 +305,20 @@ def run_reference(args, workload, rank, world):
 
 # --------------------------------------------------------------------------- our arm
 # The library's dispatch rule for the tensor-core path (batches of 256 rows
-# and more at density 1% and above) and the launches that path makes per
-# call: per-call passes plus one product kernel per batch chunk.
+# and more at density 1% and above, 128 and more at 5% and above) and the
+# launches that path makes per call: per-call passes plus the product kernels
+# of each batch chunk.
 TC_MIN_BATCH, TC_DENSITY_DIV, TC_CHUNK = 256, 100, 8192
+TC_MIN_BATCH_DENSE, TC_DENSITY_DIV_DENSE = 128, 20
+TC_SMS, TC_N = 152, 192
 
 
 def tc_path(out_f, in_f, nnz, b):
     mode = os.environ.get("SNK_LARGE_BATCH")
     if nnz == 0 or mode == "off":
         return False
-    return mode == "on" or (b >= TC_MIN_BATCH and nnz * TC_DENSITY_DIV >= out_f * in_f)
+    return mode == "on" or (b >= TC_MIN_BATCH and nnz * TC_DENSITY_DIV >= out_f * in_f) or \
+        (b >= TC_MIN_BATCH_DENSE and nnz * TC_DENSITY_DIV_DENSE >= out_f * in_f)
 
 
 def tc_launches(op, out_f, in_f, b):
@@ -327,7 +331,14 @@ def tc_launches(op, out_f, in_f, b):
         k_stride = (max(out_f, in_f) + 7) // 8 * 8
         chunk = max(64, (TC_CHUNK * k_stride) // (out_f + in_f) // 64 * 64)
         return 6 * ((b + chunk - 1) // chunk) + 1
-    return 3 + 3 * ((b + TC_CHUNK - 1) // TC_CHUNK)
+    n_seg = in_f if op == "dx" else out_f
+    n_nt = (n_seg + TC_N - 1) // TC_N
+    n = 3
+    for c0 in range(0, b, TC_CHUNK):
+        n_mt = (min(TC_CHUNK, b - c0) + 127) // 128
+        split = TC_SMS // (n_mt * n_nt)
+        n += 4 if split >= 2 else 3      # split pass, product, (partial sum), exact rows
+    return n
 
 
 def launches_per_op(n_src, b, max_smem):

@@ -82,6 +82,8 @@ struct TcState {
     int32_t* dw_flag = nullptr;   // [out + in]
     int32_t* dw_list = nullptr;   // [out + in]
     uint32_t* fix = nullptr;      // [kFixWords]
+    float* part = nullptr;        // partial sums of split CTAs (small batches)
+    int64_t part_len = 0;
 };
 
 // Words of TcState::fix: counters, and largest L1 norms and magnitudes as
@@ -290,6 +292,8 @@ struct TcArgs {
     const float* bias;        // [n_seg] or null
     float* Y;                 // [b, n_seg]
     int32_t* status;
+    int split;                // CTAs sharing one output tile, each over a range of windows
+    float* part;              // [split][b][n_seg] their partial sums (split > 1)
 };
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -310,8 +314,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ int rec_info[kRecSlots][6];
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    // raster: groups of kTcGroupM dense-row tiles sweep all segment tiles
-    const int id = blockIdx.x;
+    // raster: groups of kTcGroupM dense-row tiles sweep all segment tiles;
+    // with a split, slice sk of the grid takes windows [w0, w1) of every tile
+    const int tiles = a.n_mt * a.n_nt;
+    const int sk = blockIdx.x / tiles;
+    const int id = blockIdx.x % tiles;
     const int gsz = kTcGroupM * a.n_nt;
     const int first_m = (id / gsz) * kTcGroupM;
     const int gm = min(a.n_mt - first_m, kTcGroupM);
@@ -319,8 +326,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nt = (id % gsz) / gm;
     const int64_t r0 = (int64_t)mt * kTcM;    // first dense row
     const int64_t s0 = (int64_t)nt * kTcN;    // first segment
-    const int n_win = a.n_win;
-    const int32_t* tp = a.tile_ptr + (int64_t)nt * n_win;
+    const int w0 = (int)((int64_t)a.n_win * sk / a.split);
+    const int n_win = (int)((int64_t)a.n_win * (sk + 1) / a.split) - w0;   // windows of this CTA
+    const int32_t* tp = a.tile_ptr + (int64_t)nt * a.n_win + w0;
 
     if (t == 0) {
         for (int i = 0; i < kStagesA; ++i) {
@@ -378,8 +386,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 unsigned char* st = sa + s * kStageA;
                 mbar_expect_tx(&full_a[s], kStageA);
-                tma_load_2d(st, &map_h, w * kTcK, (int)r0, &full_a[s]);
-                tma_load_2d(st + kPieceA, &map_l, w * kTcK, (int)r0, &full_a[s]);
+                tma_load_2d(st, &map_h, (w0 + w) * kTcK, (int)r0, &full_a[s]);
+                tma_load_2d(st + kPieceA, &map_l, (w0 + w) * kTcK, (int)r0, &full_a[s]);
             }
             if (!ok) drain_ring(full_a, kStagesA, w);
         }
@@ -537,16 +545,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = 32 * lq + lane;
         const int64_t rr = r0 + row;
         if (rr < a.b) {
-            // undo the two power-of-two scalings (each factor a normal float)
+            // undo the two power-of-two scalings (each factor a normal float);
+            // a split CTA leaves its partial sum for k_tc_split_sum
             const float ir = ok ? ldexpf(1.f, -a.row_exp[rr]) : __int_as_float(0x7fc00000);
-            float* yrow = a.Y + rr * a.n_seg;
+            float* yrow = a.split > 1 ? a.part + ((int64_t)sk * a.b + rr) * a.n_seg : a.Y + rr * a.n_seg;
+            const float* bias = a.split > 1 ? nullptr : a.bias;
             const int c0 = kColsPerThread * half;
 #pragma unroll
             for (int j = 0; j < kColsPerThread; ++j) {
                 const int64_t sg = s0 + c0 + j;
                 if (sg < a.n_seg) {
                     float y = (acc[j] * ir) * __frcp_rn(pw_seg[c0 + j]);
-                    if (a.bias) y += a.bias[sg];
+                    if (bias) y += bias[sg];
                     yrow[sg] = y;
                 }
             }
@@ -560,6 +570,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
+    }
+}
+
+// Y = bias + the split CTAs' partial sums, added in split order.
+__global__ void k_tc_split_sum(const float* __restrict__ part, int split, int64_t rows, int64_t n_seg,
+                               const float* __restrict__ bias, float* __restrict__ Y) {
+    const int64_t n = rows * n_seg;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float y = 0.f;
+        for (int k = 0; k < split; ++k) y += part[(int64_t)k * n + i];
+        Y[i] = bias ? y + bias[i % n_seg] : y;
     }
 }
 
@@ -1202,10 +1223,14 @@ int build_view(Layer* L, int mode, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
 
-// Which path: SNK_LARGE_BATCH=on|off forces it (tests); otherwise batches of
-// kTcMinBatch rows and more at density 1 / kTcDensityDiv and above.
+// Which path: SNK_LARGE_BATCH=on|off forces it (tests); otherwise the
+// measured crossover with 64-row batch tiling (10000^2 and 5000^2 layers):
+// from kTcMinBatch rows at density 1 / kTcDensityDiv and above, and from
+// kTcMinBatchDense rows at density 1 / kTcDensityDivDense and above.
 constexpr int64_t kTcMinBatch = 256;
 constexpr int64_t kTcDensityDiv = 100;
+constexpr int64_t kTcMinBatchDense = 128;
+constexpr int64_t kTcDensityDivDense = 20;
 
 }  // namespace
 
@@ -1218,7 +1243,8 @@ bool tc_eligible(const Layer* L, int64_t b) {
     const char* f = getenv("SNK_LARGE_BATCH");
     if (f && strcmp(f, "off") == 0) return false;
     if (f && strcmp(f, "on") == 0) return true;
-    return b >= kTcMinBatch && L->nnz * kTcDensityDiv >= L->out_f * L->in_f;
+    return (b >= kTcMinBatch && L->nnz * kTcDensityDiv >= L->out_f * L->in_f) ||
+           (b >= kTcMinBatchDense && L->nnz * kTcDensityDivDense >= L->out_f * L->in_f);
 }
 
 void free_tc(Layer* L) {
@@ -1227,7 +1253,7 @@ void free_tc(Layer* L) {
     void* ptrs[] = {T->view[0].perm_t, T->view[0].off, T->view[0].tile_ptr, T->view[1].perm_t,
                     T->view[1].off, T->view[1].tile_ptr, T->view[2].perm_t, T->view[2].off,
                     T->view[2].tile_ptr, T->hl, T->seg_exp, T->col_exp, T->run_start, T->row_exp, T->dh,
-                    T->dl, T->seg_code, T->col_code, T->cand, T->frows, T->dw_flag, T->dw_list, T->fix};
+                    T->dl, T->seg_code, T->col_code, T->cand, T->frows, T->dw_flag, T->dw_list, T->fix, T->part};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete T;
@@ -1289,6 +1315,16 @@ bool encode_map(CUtensorMap* map, __half* base, int64_t len, int64_t rows, int64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CTAs per output tile: when the output tiles fill at most half a wave,
+// each is shared by `split` CTAs over consecutive ranges of windows, as many
+// as still fit one wave (at most kTcMaxSplit).  A split that needs a second
+// wave was measured slower (10000^2, 90%, batch 256: 297 against 257 us).
+constexpr int kTcMaxSplit = 8;
+int tc_split(int tiles, int n_win, int num_sms) {
+    const int sp = std::min(std::min(kTcMaxSplit, n_win), num_sms / std::max(tiles, 1));
+    return sp >= 2 ? sp : 1;
+}
+
 // The large-batch workspace, allocated on first use.
 int ensure_tc(Layer* L) {
     if (L->tc) return SNK_OK;
@@ -1302,6 +1338,18 @@ int ensure_tc(Layer* L) {
         !tc_alloc(&T->cand, std::max(L->out_f, L->in_f)) || !tc_alloc(&T->frows, kTcChunk) ||
         !tc_alloc(&T->dw_flag, L->out_f + L->in_f) || !tc_alloc(&T->dw_list, L->out_f + L->in_f) ||
         !tc_alloc(&T->fix, kFixWords)) {
+        free_tc(L);
+        return SNK_ERR_OOM;
+    }
+    // split partials: a split only happens below one wave of tiles, i.e. for
+    // fewer than num_sms / (segment tiles) dense-row tiles
+    for (int side = 0; side < 2; ++side) {
+        const int64_t n_seg = side ? L->in_f : L->out_f;
+        const int64_t n_nt = ceil_div(n_seg, kTcN);
+        const int64_t m_tiles = std::max<int64_t>(1, (L->num_sms - 1) / n_nt);
+        T->part_len = std::max(T->part_len, (int64_t)kTcMaxSplit * kTcM * m_tiles * n_seg);
+    }
+    if (!tc_alloc(&T->part, T->part_len)) {
         free_tc(L);
         return SNK_ERR_OOM;
     }
@@ -1367,7 +1415,13 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
         a.bias = bias;
         a.Y = Y + c0 * n_seg;
         a.status = L->status;
-        k_tc_spmm<<<a.n_mt * a.n_nt, kTcThreads, kTcSmem, s>>>(mh, ml, a);
+        a.split = tc_split(a.n_mt * a.n_nt, a.n_win, L->num_sms);
+        a.part = T->part;
+        if (a.split > 1 && (int64_t)a.split * bc * n_seg > T->part_len) a.split = 1;
+        k_tc_spmm<<<a.split * a.n_mt * a.n_nt, kTcThreads, kTcSmem, s>>>(mh, ml, a);
+        if (a.split > 1)
+            k_tc_split_sum<<<grid_for((int64_t)bc * n_seg, TH, L->num_sms), TH, 0, s>>>(T->part, a.split, bc, n_seg,
+                                                                                       bias, Y + c0 * n_seg);
         // dense rows of this chunk that the split cannot carry: every output
         // of theirs again, per stored entry
         int st = launch_exact_rows(side, n_seg, Dc, k_len, bias, Y + c0 * n_seg, T->frows,

@@ -27,13 +27,18 @@ def test_constants_match_the_library():
     assert bench.TC_MIN_BATCH == _const("kTcMinBatch")
     assert bench.TC_DENSITY_DIV == _const("kTcDensityDiv")
     assert bench.TC_CHUNK == _const("kTcChunk")
+    assert bench.TC_MIN_BATCH_DENSE == _const("kTcMinBatchDense")
+    assert bench.TC_DENSITY_DIV_DENSE == _const("kTcDensityDivDense")
 
 
 def test_rule(monkeypatch):
     monkeypatch.delenv("SNK_LARGE_BATCH", raising=False)
     n = 10_000
-    assert not bench.tc_path(n, n, 10_000_000, 255)
-    assert bench.tc_path(n, n, 10_000_000, 256)
+    assert not bench.tc_path(n, n, 10_000_000, 127)
+    assert bench.tc_path(n, n, 10_000_000, 128)          # 10%: from 128 rows
+    assert bench.tc_path(n, n, 5_000_000, 128)           # exactly 5%
+    assert not bench.tc_path(n, n, 4_999_999, 255)       # below 5%: from 256 rows
+    assert bench.tc_path(n, n, 4_999_999, 256)
     assert bench.tc_path(n, n, 1_000_000, 4096)          # exactly 1%
     assert not bench.tc_path(n, n, 999_999, 4096)        # below 1%
     assert not bench.tc_path(n, n, 0, 4096)
@@ -49,7 +54,10 @@ def test_launch_counts(b):
     # a product and an exact-row kernel per chunk of kTcChunk rows, and one
     # exact-segment kernel
     chunks = -(-b // bench.TC_CHUNK)
-    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 3 + 3 * chunks
+    # one output-tile row (b <= 128) below half a wave of 53 segment tiles:
+    # a split over windows adds the partial-sum kernel
+    split = 1 if b > 128 else 2
+    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 3 + 3 * chunks + (chunks if split > 1 else 0)
     # dW: two column passes, a flag decision, two transposes and a product
     # kernel per chunk, then one exact-entry kernel; the chunk is what the
     # shared fp16 workspace holds for both operands
