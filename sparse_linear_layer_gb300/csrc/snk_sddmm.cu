@@ -45,7 +45,7 @@ __device__ __forceinline__ void load_dy_row(const SddmmArgs& a, int r, int sub,
     constexpr int VEC = Tile<BP>::VEC;
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
-        const int beta = sub * VEC + j;
+        const int beta = Tile<BP>::beta(sub, j);
         d[j] = beta < a.b ? __ldg(a.dY + (int64_t)beta * a.out_f + r) : 0.f;
     }
 }
@@ -123,9 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     float x[VEC];
-                    const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
-                    if constexpr (SMEM) VecF<VEC>::load(px, x);
-                    else VecF<VEC>::ldg(px, x);
+                    const float* px = xsrc + ib[s].get(j) * BP;
+                    if constexpr (SMEM) TL::load(px, sub, x);
+                    else TL::ldg(px, sub, x);
                     float p = 0.f;
 #pragma unroll
                     for (int t = 0; t < VEC; ++t) p = fmaf(dyr[t], x[t], p);
@@ -141,9 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
                 const uint32_t k = base + j;
                 const bool ok = k >= lo_k && k < hi_k;
                 float x[VEC];
-                const float* px = xsrc + (ok ? ib[s].get(j) : 0) * BP + sub * VEC;
-                if constexpr (SMEM) VecF<VEC>::load(px, x);
-                else VecF<VEC>::ldg(px, x);
+                const float* px = xsrc + (ok ? ib[s].get(j) : 0) * BP;
+                if constexpr (SMEM) TL::load(px, sub, x);
+                else TL::ldg(px, sub, x);
                 float p = 0.f;
 #pragma unroll
                 for (int t = 0; t < VEC; ++t) p = fmaf(dyr[t], x[t], p);

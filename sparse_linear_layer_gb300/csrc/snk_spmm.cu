@@ -103,7 +103,7 @@ __device__ __forceinline__ void finish_segment(const SpmmArgs& a, float (&acc)[T
         if (lane < LPE) {
 #pragma unroll
             for (int j = 0; j < VEC; ++j) {
-                const int beta = sub * VEC + j;
+                const int beta = TL::beta(sub, j);
                 if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = acc[j] + bo;
             }
         }
@@ -153,7 +153,7 @@ __device__ __noinline__ void cross_block(const SpmmArgs& a, int r, int slot,
         const float bo = a.bias ? __ldg(a.bias + r) : 0.f;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            const int beta = sub * VEC + j;
+            const int beta = TL::beta(sub, j);
             if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = tot[j] + bo;
         }
     }
@@ -195,7 +195,7 @@ __device__ __forceinline__ void block_combine(const SpmmArgs& a, const float* sp
                     const float bo = a.bias ? __ldg(a.bias + r) : 0.f;
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) {
-                        const int beta = sub * VEC + j;
+                        const int beta = TL::beta(sub, j);
                         if (beta < a.b) a.Y[(int64_t)beta * a.n_seg + r] = sum[j] + bo;
                     }
                 }
@@ -307,9 +307,9 @@ __global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmAr
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     float x[VEC];
-                    const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
-                    if constexpr (SMEM) VecF<VEC>::load(px, x);
-                    else VecF<VEC>::ldg(px, x);
+                    const float* px = xsrc + ib[s].get(j) * BP;
+                    if constexpr (SMEM) TL::load(px, sub, x);
+                    else TL::ldg(px, sub, x);
 #pragma unroll
                     for (int t = 0; t < VEC; ++t) acc[t] = fmaf(wb[s][j], x[t], acc[t]);
                 }
@@ -323,9 +323,9 @@ __global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmAr
                     const uint32_t k = base + j;
                     if (k >= lo_k && k < hi_k) {
                         float x[VEC];
-                        const float* px = xsrc + ib[s].get(j) * BP + sub * VEC;
-                        if constexpr (SMEM) VecF<VEC>::load(px, x);
-                        else VecF<VEC>::ldg(px, x);
+                        const float* px = xsrc + ib[s].get(j) * BP;
+                        if constexpr (SMEM) TL::load(px, sub, x);
+                        else TL::ldg(px, sub, x);
 #pragma unroll
                         for (int t = 0; t < VEC; ++t) acc[t] = fmaf(wb[s][j], x[t], acc[t]);
                     }
