@@ -151,6 +151,7 @@ def measured_peaks():
 KERNEL_SOURCES = {
     "k_spmm_fwd": ["snk_spmm.cu", "snk_device.cuh", "snk_internal.cuh"],
     "k_spmm_dx": ["snk_spmm.cu", "snk_device.cuh", "snk_internal.cuh"],
+    "k_sweep_dx": ["snk_spmm.cu", "snk_sweep.cu", "snk_device.cuh", "snk_internal.cuh"],
     "k_sddmm": ["snk_sddmm.cu", "snk_device.cuh", "snk_internal.cuh"],
     "k_tc_spmm": ["snk_tc.cu", "snk_internal.cuh"],
     "k_tc_sddmm": ["snk_tc.cu", "snk_internal.cuh"],
@@ -321,6 +322,16 @@ def tc_path(out_f, in_f, nnz, b):
         (b >= TC_MIN_BATCH_DENSE and nnz * TC_DENSITY_DIV_DENSE >= out_f * in_f)
 
 
+def dx_kernel(out_f, in_f, b, num_sms=152):
+    """The kernel the library runs for dX on the batch-tiled path: the column
+    sweep for tiles of up to 4 columns when the rows have 16-bit copies (out
+    <= 65536) and its lane tables fit the layer's scratch, else the chunk
+    walk."""
+    if b <= 4 and out_f <= 65536 and 8 * (in_f + num_sms) <= max(out_f, in_f) * 64:
+        return "k_sweep_dx"
+    return "k_spmm_dx"
+
+
 def tc_launches(op, out_f, in_f, b):
     """Kernels per call on the tensor-core path: per batch chunk the column
     passes, the flag decision, the transposes and the product, plus the exact
@@ -417,7 +428,7 @@ def time_ops(binding, g, X, dY, bias, Y, dX, dW, db, flush, stream, steps, warmu
     return {name: [e0.elapsed_time(e1) for e0, e1 in ev[name]] for name, _ in ops}
 
 
-def gather_reference(torch, g, flush, stream, dx_us):
+def gather_reference(torch, g, flush, stream, dx_us, dx_tag):
     """The transposed product reads values[perm] in random order: one 4-byte
     value per stored entry, each from its own 32-byte sector.  That gather
     alone, timed here as torch's index_select over the same permutation (a
@@ -437,7 +448,7 @@ def gather_reference(torch, g, flush, stream, dx_us):
         if i >= 3:
             ts.append(e0.elapsed_time(e1) * 1e3)
     t = statistics.mean(ts)
-    return {"bound": "random value gather (L1 sector lookups)", "kernel": "k_spmm_dx",
+    return {"bound": "random value gather (L1 sector lookups)", "kernel": dx_tag,
             "reference": "torch.index_select(values, 0, perm), same 10M-entry permutation, "
                          "L2 flushed, CUDA events",
             "gather_us": t, "dx_us": dx_us, "frac": t / dx_us}
@@ -825,7 +836,7 @@ def run_ours(args, workload, rank, world, local):
             "note": "6*b*out*in fp16 flops: three products of the densified tiles",
         }
     else:
-        kernel_tags = {"fwd": "k_spmm_fwd", "dx": "k_spmm_dx", "dw": "k_sddmm"}
+        kernel_tags = {"fwd": "k_spmm_fwd", "dx": dx_kernel(out_f, in_f, b), "dw": "k_sddmm"}
         roofline = {
             "bound": "hbm", "kernel": kernel_tags[dom], "op": dom, "achieved": per_op[dom]["gbs"],
             "peak": peak, "peak_kind": f"hbm_gbs, {peak_kind}", "unit": "GB/s",
@@ -839,7 +850,8 @@ def run_ours(args, workload, rank, world, local):
             "per_op": per_op,
         }
         if not args.only and lay.nnz > 0:
-            roofline["onchip"] = gather_reference(torch, g, flush, stream, per_op["dx"]["us_mean"])
+            roofline["onchip"] = gather_reference(torch, g, flush, stream, per_op["dx"]["us_mean"],
+                                                  dx_kernel(out_f, in_f, b))
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e = None

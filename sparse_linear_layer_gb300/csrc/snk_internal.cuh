@@ -32,6 +32,12 @@ constexpr int kWarp = 32;
 #ifndef SNK_IDX16
 #define SNK_IDX16 1        // read 16-bit index copies on the shared-memory path
 #endif
+#ifndef SNK_SWEEP_PHASE_KB
+#define SNK_SWEEP_PHASE_KB 96  // column sweep: shared memory per phase at a 4-column tile
+#endif
+#ifndef SNK_SWEEP_NS
+#define SNK_SWEEP_NS 3     // column sweep: quads in flight per lane
+#endif
 
 constexpr int kThreads = SNK_THREADS;
 constexpr int kWarpsPerBlock = kThreads / kWarp;
@@ -49,6 +55,7 @@ constexpr int kStatLimit = 4;
 struct RestructureWs;
 struct PcsrState;
 struct TcState;
+struct Sweep;
 
 // Per block: its entry range [k0, k1), and for the segment that enters the
 // block from before (head) and the one that leaves it (tail) the first and
@@ -114,9 +121,27 @@ struct Layer {
     RestructureWs* rws = nullptr; // allocated on first prune_regrow
     PcsrState* pcsr = nullptr;    // Padded-CSR view, built on request
     TcState* tc = nullptr;        // tile-ordered views of the large-batch path, built on first use
+    Sweep* sweep = nullptr;       // lane tables of the column sweep (snk_sweep.cu)
 };
 
 void free_pcsr(Layer* L);
+
+// ---- column sweep of the transposed product (snk_sweep.cu) ---------------
+// Every column of a block gets its own lanes, as many as its share of the
+// block's entries; see snk_sweep.cu for the tables' layout.
+struct SweepView {
+    const int4* blk;    // [2 n_blocks] (first col, end col, virtual lanes, first lane), (first col record, first global partial, head, tail)
+    const int2* col;    // per block and column: (first virtual lane, lanes)
+    const int4* lane;   // per virtual lane: (first quad, quad stride, first entry, end entry)
+    const int* split;   // [phases - 1][n_lane]: 2 * resume quad (+1 if that quad straddles the row)
+    int64_t n_lane;
+    int phases;         // row phases of the tables (a power of two, at most 8)
+    int rows;           // rows per phase (a multiple of 4)
+};
+int build_sweep(Layer* L, cudaStream_t s);
+void mark_sweep(Layer* L);
+void free_sweep(Layer* L);
+bool sweep_view(const Layer* L, SweepView* v);
 
 // ---- large-batch path on the tensor cores (snk_tc.cu) ---------------------
 bool tc_eligible(const Layer* L, int64_t b);

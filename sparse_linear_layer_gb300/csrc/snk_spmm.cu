@@ -58,6 +58,16 @@ struct SpmmArgs {
     float* Y;                // [b, n_seg] row-major
     float* part;             // [n_blocks][2][BP] cross-block partial sums
     int32_t* cnt;            // [n_seg] arrival counters
+    // column sweep of the transposed product (k_sweep only)
+    const int4* sw_blk;      // per block: two records
+    const int2* sw_col;      // per block and column: (first virtual lane, lanes)
+    const int4* sw_lane;     // per virtual lane: (first quad, quad stride, first entry, end entry)
+    float* sw_gpart;         // partials of virtual lanes beyond the block's threads
+    const int* sw_split;     // [boundary][lane] resume quad of each lane at each table boundary
+    int64_t sw_nlane;        // lanes per boundary in sw_split
+    int sw_rows;             // operand rows staged per phase (a multiple of 4)
+    int sw_phases;           // phases of this launch
+    int sw_stride;           // table boundaries per phase of this launch
 };
 
 // A segment cut by a chunk boundary, whose partial sum this warp stored in
@@ -372,6 +382,255 @@ __global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmAr
     block_combine<BP, W>(a, sp, srow, pend, warp, lane, sub);
 }
 
+// ---------------------------------------------------------------------------
+// Column sweep of the transposed product (batch tile BP <= 4, operand in
+// shared memory).  Every column of the block has its own lanes (snk_sweep.cu
+// builds the tables); lane j of a column with n lanes takes the column's
+// aligned quads j, j + n, j + 2n, ... and masks the entries outside the
+// column's range in this block.  Rows rise along a column, so all lanes move
+// down the rows together, and the values they gather for nearby rows share
+// sectors in L1.
+//
+// Row phases: the operand is staged a band of rows at a time, so that L1
+// keeps room for the gathered values (at batch 4 the whole operand would take
+// 160 KB of an SM's 256 KB at out = 10000).  The tables cut the rows into P
+// equal phases (P a power of two, about SNK_SWEEP_PHASE_KB of shared memory
+// each at a 4-column tile) and hold, for every lane and cut, the quad where
+// the lane crosses it; a launch with a narrower tile merges phases.  A phase
+// takes the entries whose rows it holds, up to that quad (inclusive when the
+// quad straddles the cut), and the next phase resumes there, so a lane's
+// loop bound is known before it starts.
+//
+// A lane keeps two accumulators (even and odd positions of the quad) and
+// folds them into its partial sums every 8 quads and at the end of each
+// phase, so no running sum takes more than 16 terms.  The column's result
+// adds its lanes' partials in lane order, 32 at a time; the column cut by the
+// block's first (or last) boundary goes through the same cross-block
+// protocol as the chunk walk, so results are deterministic and launches of
+// either kernel mix.
+
+// Index loads of the sweep bypass L1 allocation, leaving L1 to the values.
+__device__ __forceinline__ int4 sw_ld4(const int4* p) {
+    int4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 sw_ld2(const uint2* p) {
+    uint2 r;
+    asm volatile("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+// The walk of one virtual lane, resumable across row phases: between phases
+// it keeps only its next quad and its partial sums.
+template <int BP>
+struct SweepLane {
+    uint32_t u;          // next quad
+    uint32_t st, s, e;   // quad stride; the column's entry range in the block
+    float outer[BP];     // partial sums
+
+    __device__ __forceinline__ void init(const int4 ln) {
+        u = (uint32_t)ln.x;
+        st = (uint32_t)ln.y;
+        s = (uint32_t)ln.z;
+        e = (uint32_t)ln.w;
+#pragma unroll
+        for (int t = 0; t < BP; ++t) outer[t] = 0.f;
+    }
+
+    // Entries with rows in [r0, r1); xs holds those operand rows.  Quads
+    // stream NS - 1 ahead; their values are gathered one ahead.  Two
+    // accumulators (even and odd positions of the quad) fold into the
+    // partial sums every 8 quads and at the end of the phase, so no running
+    // sum takes more than 16 terms.
+    // Quads from u up to (not including) qend, entries with rows in [r0, r1).
+    template <bool GX = false>
+    __device__ __forceinline__ void run(const SpmmArgs& a, const float* xs, int r0, int r1, uint32_t qend) {
+        constexpr int NS = SNK_SWEEP_NS;
+        const uint32_t qe = min((e + 3) >> 2, qend);
+        float acc[2][BP];
+#pragma unroll
+        for (int t = 0; t < BP; ++t) acc[0][t] = acc[1][t] = 0.f;
+        int since_fold = 0;
+        auto fold = [&]() {
+#pragma unroll
+            for (int t = 0; t < BP; ++t) {
+                outer[t] += acc[0][t] + acc[1][t];
+                acc[0][t] = acc[1][t] = 0.f;
+            }
+        };
+        int pp[NS][4];
+        uint32_t rr[NS][2];   // rows, two 16-bit rows per word
+        float ww[NS][4];
+        auto row_of = [&](int sl, int j) -> int {
+            const uint32_t w2 = rr[sl][j >> 1];
+            return (int)((j & 1) ? (w2 >> 16) : (w2 & 0xffffu));
+        };
+        auto issue = [&](int sl, uint32_t q) {
+            const int4 p4 = sw_ld4(reinterpret_cast<const int4*>(a.perm) + q);
+            const uint2 r4 = sw_ld2(reinterpret_cast<const uint2*>(a.idx16) + q);
+            pp[sl][0] = p4.x;
+            pp[sl][1] = p4.y;
+            pp[sl][2] = p4.z;
+            pp[sl][3] = p4.w;
+            rr[sl][0] = r4.x;
+            rr[sl][1] = r4.y;
+        };
+        auto gather = [&](int sl, uint32_t q) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t k = 4 * q + j;
+                ww[sl][j] = (k >= s && k < e) ? __ldg(a.val + pp[sl][j]) : 0.f;
+            }
+        };
+        // the quad's entries with rows in [r0, r1)
+        auto consume = [&](int sl, uint32_t q) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t k = 4 * q + j;
+                const int r = row_of(sl, j);
+                if (k >= s && k < e) {
+                    if (r >= r0 && r < r1) {
+                        float x[BP];
+                        if constexpr (GX) {
+#pragma unroll
+                            for (int t = 0; t < BP; ++t) x[t] = t < a.b ? __ldg(a.X + (int64_t)t * a.n_src + r) : 0.f;
+                        } else {
+                            VecF<BP>::load(xs + (r - r0) * BP, x);
+                        }
+#pragma unroll
+                        for (int t = 0; t < BP; ++t) acc[j & 1][t] = fmaf(ww[sl][j], x[t], acc[j & 1][t]);
+                    }
+                }
+            }
+            if (++since_fold == 8) {
+                since_fold = 0;
+                fold();
+            }
+        };
+        if (u >= qe) {
+            u = qe;
+            return;
+        }
+#pragma unroll
+        for (int k = 0; k < NS - 1; ++k)
+            if (u + k * st < qe) issue(k, u + k * st);
+        gather(0, u);
+        for (uint32_t qb = u; qb < qe; qb += NS * st) {
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                const uint32_t q = qb + i * st;
+                if (q < qe) {
+                    if (q + (NS - 1) * st < qe) issue((i + NS - 1) % NS, q + (NS - 1) * st);
+                    if (q + st < qe) gather((i + 1) % NS, q + st);
+                    consume(i, q);
+                }
+            }
+        }
+        u = qe;
+        fold();
+    }
+};
+
+// Sum of the partials of virtual lanes v0 .. v0 + n - 1 (in shared memory
+// below the thread count, else in global scratch), 32 at a time.
+template <int BP>
+__device__ __forceinline__ void sweep_sum(const float* red, const float* gred, int v0, int n, float (&sum)[BP]) {
+#pragma unroll
+    for (int t = 0; t < BP; ++t) sum[t] = 0.f;
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        float u[BP];
+#pragma unroll
+        for (int t = 0; t < BP; ++t) u[t] = 0.f;
+        const int k1 = min(n, k0 + 32);
+        for (int k = k0; k < k1; ++k) {
+            const int v = v0 + k;
+            const float* p = v < kThreadsDx ? red + v * BP : gred + (int64_t)(v - kThreadsDx) * BP;
+#pragma unroll
+            for (int t = 0; t < BP; ++t) u[t] += p[t];
+        }
+#pragma unroll
+        for (int t = 0; t < BP; ++t) sum[t] += u[t];
+    }
+}
+
+// A further virtual lane of a thread (blocks with more than NT / 2 columns
+// only): walked once over all rows after the phases, its operand read
+// straight from X, its partial kept in global scratch.
+template <int BP>
+__device__ __forceinline__ void sweep_extra(const SpmmArgs& a, const int4 ln, float* g) {
+    SweepLane<BP> w2;
+    w2.init(ln);
+    w2.template run<true>(a, nullptr, 0, (int)a.n_src, 0xffffffffu);
+#pragma unroll
+    for (int t = 0; t < BP; ++t) g[t] = w2.outer[t];
+}
+
+// Phase ph stages operand rows [ph sw_rows, (ph + 1) sw_rows); a lane
+// stops where the tables say its column crosses the phase's last row.
+template <int BP>
+__global__ void __launch_bounds__(kThreadsDx, 1) k_sweep(const SpmmArgs a) {
+    static_assert(BP <= 4, "one lane holds all BP columns of an entry");
+    constexpr int NT = kThreadsDx;
+    extern __shared__ float4 smem4[];
+    float* xs = reinterpret_cast<float*>(smem4);
+    SweepLane<BP> w;
+    w.init(a.sw_lane[a.sw_blk[2 * blockIdx.x].w + threadIdx.x]);
+    const int n_rows = (int)a.n_src;
+    const int v0 = a.sw_blk[2 * blockIdx.x].w + threadIdx.x;
+    for (int ph = 0; ph < a.sw_phases; ++ph) {
+        const int r0 = ph * a.sw_rows, r1 = min(n_rows, r0 + a.sw_rows);
+        if (ph > 0) __syncthreads();   // the previous phase's rows are read no more
+        stage_transposed<BP>(xs, a.X + r0, a.n_src, a.b, r1 - r0, threadIdx.x, NT);
+        __syncthreads();
+        // this lane's resume quad at row r1 (twice it, plus one when that
+        // quad also holds entries below r1)
+        const bool cut = ph + 1 < a.sw_phases;
+        const int sp = cut ? __ldg(a.sw_split + (int64_t)((ph + 1) * a.sw_stride - 1) * a.sw_nlane + v0) : -2;
+        w.run(a, xs, r0, r1, cut ? (uint32_t)(sp >> 1) + (uint32_t)(sp & 1) : 0xffffffffu);
+        if (cut) w.u = (uint32_t)(sp >> 1);
+    }
+    const int4 b = a.sw_blk[2 * blockIdx.x], b2 = a.sw_blk[2 * blockIdx.x + 1];
+    const int T = b.z;   // virtual lanes, a multiple of NT
+    float* gred = a.sw_gpart + (int64_t)b2.y * BP;
+    for (int v = threadIdx.x + NT; v < T; v += NT)
+        sweep_extra<BP>(a, a.sw_lane[b.w + v], gred + (int64_t)(v - NT) * BP);
+    __syncthreads();   // the operand is read no more: its space takes the partials
+    float* red = xs;
+#pragma unroll
+    for (int t = 0; t < BP; ++t) red[threadIdx.x * BP + t] = w.outer[t];
+    __syncthreads();
+    const int lo = b.x, ncols = b.y - b.x;
+    for (int i = threadIdx.x; i < ncols; i += NT) {
+        const int c = lo + i;
+        if (c == b2.z || c == b2.w) continue;
+        const int2 cr = a.sw_col[b2.x + i];
+        float sum[BP];
+        sweep_sum<BP>(red, gred, cr.x, cr.y, sum);
+#pragma unroll
+        for (int t = 0; t < BP; ++t)
+            if (t < a.b) a.Y[(int64_t)t * a.n_seg + c] = sum[t];
+    }
+    // the columns cut by the block's boundaries: warp 0 the head, warp 1 the tail
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = warp == 0 ? b2.z : (warp == 1 ? b2.w : -1);
+    if (c >= 0) {
+        const int2 cr = a.sw_col[b2.x + (c - lo)];
+        float sum[BP];
+        sweep_sum<BP>(red, gred, cr.x, cr.y, sum);
+        const BlockDesc bd = a.bdesc[blockIdx.x];
+        if (warp == 0) {
+            if (__ldg(a.seg_ptr + c + 1) <= bd.k1)
+                cross_block<BP>(a, c, 0, sum, bd.head_first, blockIdx.x, bd.n_head, lane, 0);
+            else
+                cross_block<BP>(a, c, 0, sum, bd.head_first, bd.tail_last, bd.n_head + bd.n_tail - 1, lane, 0);
+        } else {
+            cross_block<BP>(a, c, 1, sum, blockIdx.x, bd.tail_last, bd.n_tail, lane, 0);
+        }
+    }
+}
+
 // Transposed copy of the operand for the global-memory path.
 template <int BP>
 __global__ void k_transpose(const float* __restrict__ X, int64_t n, int b, float* __restrict__ xt) {
@@ -399,6 +658,39 @@ static int launch_bp(Layer* L, SpmmArgs a, cudaStream_t s) {
     constexpr int NT = SpmmShape<GATHER>::kNT;
     const size_t slots = spmm_slot_bytes<BP, GATHER>();
     const size_t smem = operand_floats(a.n_src, BP) * sizeof(float) + slots;
+    if constexpr (GATHER && BP <= 4) {
+        // the column sweep, when the layer has its tables: the tables cut
+        // the rows into P equal phases (P a power of two); a 4-column tile
+        // takes them all, 2 and 1 columns take P / 2 and P / 4 (at least one)
+        SweepView v;
+        if (a.idx16 && !a.bias && sweep_view(L, &v)) {
+            // Phases pay for a barrier and a restart of every lane's stream;
+            // with fewer than 32 entries per lane (8 quads) one phase is
+            // faster when the whole operand fits (10000^2, 99%, b = 4: 18.5
+            // against 20.4 us).
+            const bool few = a.nnz < (int64_t)32 * a.n_blocks * kThreadsDx;
+            const bool fits = operand_floats(a.n_src, BP) * sizeof(float) <= (size_t)L->max_smem;
+            const int phases = (few && fits) ? 1 : std::max(1, v.phases * BP / 4);
+            const int stride = v.phases / phases;
+            const int64_t rows = phases == 1 ? a.n_src : std::min<int64_t>(a.n_src, (int64_t)v.rows * stride);
+            const size_t smem_sw = std::max(operand_floats(rows, BP), (size_t)kThreadsDx * BP) * sizeof(float);
+            if (smem_sw <= (size_t)L->max_smem) {
+                a.sw_blk = v.blk;
+                a.sw_col = v.col;
+                a.sw_lane = v.lane;
+                a.sw_split = v.split;
+                a.sw_nlane = v.n_lane;
+                a.sw_gpart = L->xt;
+                a.sw_rows = (int)rows;
+                a.sw_phases = phases;
+                a.sw_stride = stride;
+                auto fn = k_sweep<BP>;
+                if (set_smem(fn, smem_sw) != SNK_OK) return SNK_ERR_CUDA;
+                fn<<<a.n_blocks, kThreadsDx, smem_sw, s>>>(a);
+                return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
+            }
+        }
+    }
     if (smem <= (size_t)L->max_smem && a.idx16) {
         auto fn = k_spmm<BP, GATHER, true>;
         if (set_smem(fn, smem) != SNK_OK) return SNK_ERR_CUDA;

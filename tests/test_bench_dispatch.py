@@ -73,3 +73,12 @@ def test_source_digest_ignores_comments():
     b = "// lead\nint f() {\n    return 1;\n}\nint g;  /* trailing */"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only("int f() { return 2; }") != bench._code_only("int f() { return 1; }")
+
+
+def test_dx_kernel_tag_follows_the_dispatch():
+    """dX runs the column sweep for tiles of up to 4 columns on layers with
+    16-bit row copies, else the chunk walk."""
+    assert bench.dx_kernel(10_000, 10_000, 4) == "k_sweep_dx"
+    assert bench.dx_kernel(10_000, 10_000, 1) == "k_sweep_dx"
+    assert bench.dx_kernel(10_000, 10_000, 5) == "k_spmm_dx"
+    assert bench.dx_kernel(70_000, 40, 1) == "k_spmm_dx"
