@@ -384,7 +384,9 @@ __global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmAr
 
 // ---------------------------------------------------------------------------
 // Column sweep of the transposed product (batch tile BP <= 4, operand in
-// shared memory).  Every column of the block has its own lanes (snk_sweep.cu
+// shared memory).  (An 8-column version measured no faster than the chunk
+// walk at 10000^2, 90%, and slower at 95% and 99%: two 128-bit operand loads
+// per entry and twice the row phases.)  Every column of the block has its own lanes (snk_sweep.cu
 // builds the tables); lane j of a column with n lanes takes the column's
 // aligned quads j, j + n, j + 2n, ... and masks the entries outside the
 // column's range in this block.  Rows rise along a column, so all lanes move
@@ -423,12 +425,19 @@ __device__ __forceinline__ uint2 sw_ld2(const uint2* p) {
 }
 
 // The walk of one virtual lane, resumable across row phases: between phases
-// it keeps only its next quad and its partial sums.
+// it keeps only its next quad and its partial sums.  (Priming a phase before
+// its operand rows are staged, to overlap the first loads with the staging,
+// measured no faster: the pipeline registers then live across the staging.)
 template <int BP>
 struct SweepLane {
+    static constexpr int NS = SNK_SWEEP_NS;   // quads in flight
     uint32_t u;          // next quad
     uint32_t st, s, e;   // quad stride; the column's entry range in the block
+    uint32_t qe;         // quad bound of the current phase
     float outer[BP];     // partial sums
+    int pp[NS][4];       // canonical slots of quads in flight
+    uint32_t rr[NS][2];  // their rows, two 16-bit rows per word
+    float ww[NS][4];     // their gathered values
 
     __device__ __forceinline__ void init(const int4 ln) {
         u = (uint32_t)ln.x;
@@ -438,17 +447,47 @@ struct SweepLane {
 #pragma unroll
         for (int t = 0; t < BP; ++t) outer[t] = 0.f;
     }
+    __device__ __forceinline__ int row_of(int sl, int j) const {
+        const uint32_t w2 = rr[sl][j >> 1];
+        return (int)((j & 1) ? (w2 >> 16) : (w2 & 0xffffu));
+    }
+    __device__ __forceinline__ void issue(const SpmmArgs& a, int sl, uint32_t q) {
+        const int4 p4 = sw_ld4(reinterpret_cast<const int4*>(a.perm) + q);
+        const uint2 r4 = sw_ld2(reinterpret_cast<const uint2*>(a.idx16) + q);
+        pp[sl][0] = p4.x;
+        pp[sl][1] = p4.y;
+        pp[sl][2] = p4.z;
+        pp[sl][3] = p4.w;
+        rr[sl][0] = r4.x;
+        rr[sl][1] = r4.y;
+    }
+    __device__ __forceinline__ void gather(const SpmmArgs& a, int sl, uint32_t q) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t k = 4 * q + j;
+            ww[sl][j] = (k >= s && k < e) ? __ldg(a.val + pp[sl][j]) : 0.f;
+        }
+    }
 
-    // Entries with rows in [r0, r1); xs holds those operand rows.  Quads
-    // stream NS - 1 ahead; their values are gathered one ahead.  Two
-    // accumulators (even and odd positions of the quad) fold into the
-    // partial sums every 8 quads and at the end of the phase, so no running
-    // sum takes more than 16 terms.
-    // Quads from u up to (not including) qend, entries with rows in [r0, r1).
+    // Start the phase that ends before quad qend: index loads of its first
+    // NS - 1 quads, the values of the first.
+    __device__ __forceinline__ void prime(const SpmmArgs& a, uint32_t qend) {
+        qe = min((e + 3) >> 2, qend);
+        if (u >= qe) return;
+#pragma unroll
+        for (int k = 0; k < NS - 1; ++k)
+            if (u + k * st < qe) issue(a, k, u + k * st);
+        gather(a, 0, u);
+    }
+
+    // The primed phase: quads from u up to qe, entries with rows in
+    // [r0, r1) (xs holds those operand rows, or with GX the operand is read
+    // from X).  Quads stream NS - 1 ahead; their values are gathered one
+    // ahead.  Two accumulators (even and odd positions of the quad) fold into
+    // the partial sums every 8 quads and at the end of the phase, so no
+    // running sum takes more than 16 terms.
     template <bool GX = false>
-    __device__ __forceinline__ void run(const SpmmArgs& a, const float* xs, int r0, int r1, uint32_t qend) {
-        constexpr int NS = SNK_SWEEP_NS;
-        const uint32_t qe = min((e + 3) >> 2, qend);
+    __device__ __forceinline__ void run(const SpmmArgs& a, const float* xs, int r0, int r1) {
         float acc[2][BP];
 #pragma unroll
         for (int t = 0; t < BP; ++t) acc[0][t] = acc[1][t] = 0.f;
@@ -458,30 +497,6 @@ struct SweepLane {
             for (int t = 0; t < BP; ++t) {
                 outer[t] += acc[0][t] + acc[1][t];
                 acc[0][t] = acc[1][t] = 0.f;
-            }
-        };
-        int pp[NS][4];
-        uint32_t rr[NS][2];   // rows, two 16-bit rows per word
-        float ww[NS][4];
-        auto row_of = [&](int sl, int j) -> int {
-            const uint32_t w2 = rr[sl][j >> 1];
-            return (int)((j & 1) ? (w2 >> 16) : (w2 & 0xffffu));
-        };
-        auto issue = [&](int sl, uint32_t q) {
-            const int4 p4 = sw_ld4(reinterpret_cast<const int4*>(a.perm) + q);
-            const uint2 r4 = sw_ld2(reinterpret_cast<const uint2*>(a.idx16) + q);
-            pp[sl][0] = p4.x;
-            pp[sl][1] = p4.y;
-            pp[sl][2] = p4.z;
-            pp[sl][3] = p4.w;
-            rr[sl][0] = r4.x;
-            rr[sl][1] = r4.y;
-        };
-        auto gather = [&](int sl, uint32_t q) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t k = 4 * q + j;
-                ww[sl][j] = (k >= s && k < e) ? __ldg(a.val + pp[sl][j]) : 0.f;
             }
         };
         // the quad's entries with rows in [r0, r1)
@@ -513,17 +528,13 @@ struct SweepLane {
             u = qe;
             return;
         }
-#pragma unroll
-        for (int k = 0; k < NS - 1; ++k)
-            if (u + k * st < qe) issue(k, u + k * st);
-        gather(0, u);
         for (uint32_t qb = u; qb < qe; qb += NS * st) {
 #pragma unroll
             for (int i = 0; i < NS; ++i) {
                 const uint32_t q = qb + i * st;
                 if (q < qe) {
-                    if (q + (NS - 1) * st < qe) issue((i + NS - 1) % NS, q + (NS - 1) * st);
-                    if (q + st < qe) gather((i + 1) % NS, q + st);
+                    if (q + (NS - 1) * st < qe) issue(a, (i + NS - 1) % NS, q + (NS - 1) * st);
+                    if (q + st < qe) gather(a, (i + 1) % NS, q + st);
                     consume(i, q);
                 }
             }
@@ -562,7 +573,8 @@ template <int BP>
 __device__ __forceinline__ void sweep_extra(const SpmmArgs& a, const int4 ln, float* g) {
     SweepLane<BP> w2;
     w2.init(ln);
-    w2.template run<true>(a, nullptr, 0, (int)a.n_src, 0xffffffffu);
+    w2.prime(a, 0xffffffffu);
+    w2.template run<true>(a, nullptr, 0, (int)a.n_src);
 #pragma unroll
     for (int t = 0; t < BP; ++t) g[t] = w2.outer[t];
 }
@@ -581,14 +593,15 @@ __global__ void __launch_bounds__(kThreadsDx, 1) k_sweep(const SpmmArgs a) {
     const int v0 = a.sw_blk[2 * blockIdx.x].w + threadIdx.x;
     for (int ph = 0; ph < a.sw_phases; ++ph) {
         const int r0 = ph * a.sw_rows, r1 = min(n_rows, r0 + a.sw_rows);
-        if (ph > 0) __syncthreads();   // the previous phase's rows are read no more
-        stage_transposed<BP>(xs, a.X + r0, a.n_src, a.b, r1 - r0, threadIdx.x, NT);
-        __syncthreads();
         // this lane's resume quad at row r1 (twice it, plus one when that
         // quad also holds entries below r1)
         const bool cut = ph + 1 < a.sw_phases;
         const int sp = cut ? __ldg(a.sw_split + (int64_t)((ph + 1) * a.sw_stride - 1) * a.sw_nlane + v0) : -2;
-        w.run(a, xs, r0, r1, cut ? (uint32_t)(sp >> 1) + (uint32_t)(sp & 1) : 0xffffffffu);
+        if (ph > 0) __syncthreads();   // the previous phase's rows are read no more
+        stage_transposed<BP>(xs, a.X + r0, a.n_src, a.b, r1 - r0, threadIdx.x, NT);
+        __syncthreads();
+        w.prime(a, cut ? (uint32_t)(sp >> 1) + (uint32_t)(sp & 1) : 0xffffffffu);
+        w.run(a, xs, r0, r1);
         if (cut) w.u = (uint32_t)(sp >> 1);
     }
     const int4 b = a.sw_blk[2 * blockIdx.x], b2 = a.sw_blk[2 * blockIdx.x + 1];
@@ -619,14 +632,20 @@ __global__ void __launch_bounds__(kThreadsDx, 1) k_sweep(const SpmmArgs a) {
         const int2 cr = a.sw_col[b2.x + (c - lo)];
         float sum[BP];
         sweep_sum<BP>(red, gred, cr.x, cr.y, sum);
+        // in the chunk walk's lane layout: lane sub < LPE holds its VEC columns
+        using TL = Tile<BP>;
+        const int sub = lane % TL::LPE;
+        float mine[TL::VEC];
+#pragma unroll
+        for (int j = 0; j < TL::VEC; ++j) mine[j] = sum[TL::beta(sub, j)];
         const BlockDesc bd = a.bdesc[blockIdx.x];
         if (warp == 0) {
             if (__ldg(a.seg_ptr + c + 1) <= bd.k1)
-                cross_block<BP>(a, c, 0, sum, bd.head_first, blockIdx.x, bd.n_head, lane, 0);
+                cross_block<BP>(a, c, 0, mine, bd.head_first, blockIdx.x, bd.n_head, lane, sub);
             else
-                cross_block<BP>(a, c, 0, sum, bd.head_first, bd.tail_last, bd.n_head + bd.n_tail - 1, lane, 0);
+                cross_block<BP>(a, c, 0, mine, bd.head_first, bd.tail_last, bd.n_head + bd.n_tail - 1, lane, sub);
         } else {
-            cross_block<BP>(a, c, 1, sum, blockIdx.x, bd.tail_last, bd.n_tail, lane, 0);
+            cross_block<BP>(a, c, 1, mine, blockIdx.x, bd.tail_last, bd.n_tail, lane, sub);
         }
     }
 }
