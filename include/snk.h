@@ -49,12 +49,17 @@
  *   - Limits: 1 <= out, in <= 2^31 - 1; 0 <= nnz <= min(out*in, 2^31 - 1);
  *     out*in < 2^63.
  *   - Numerics: fp32 products accumulated in fp32 with at least 32 partial
- *     sums per output reduced by a tree, so that each output y satisfies
- *     |y - exact| <= 1e-5 * A + 1e-6 with A the sum of |terms| (+|bias|).
+ *     sums per output reduced by a tree (dX at batch <= 4: each lane of an
+ *     output column keeps two running sums, folds them into its partial every
+ *     16 terms, and the column adds its lanes' partials 32 at a time), so that
+ *     each output y satisfies |y - exact| <= 1e-5 * A + 1e-6 with A the sum
+ *     of |terms| (+|bias|).  The order of every sum is fixed by the topology:
+ *     repeated calls give the same bits.
  *
  * Large batches ([SNACK] appendix Table 13 trains at batch 4096)
- *   - From batch 256 on, when at least 1% of W is stored, the three product
- *     calls run on the tensor cores instead of 64-row batch tiling.  W is
+ *   - From batch 128 when at least 5% of W is stored, and from batch 256 when
+ *     at least 1% is, the three product calls run on the tensor cores instead
+ *     of 64-row batch tiling.  W is
  *     densified tile by tile in shared memory (never in device memory) and
  *     multiplied with the dense operand.  The environment variable
  *     SNK_LARGE_BATCH=on|off forces the choice for every batch size.
