@@ -180,16 +180,17 @@ def kernel_source_digest(kernel_tag=None):
 
 
 def committed_traffic(kernel_tag, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current sources of that kernel; else None."""
+    """DRAM bytes per launch from the committed ncu summary of that kernel on
+    that workload (profiles/traffic.json: kernel -> workload -> entry), if it
+    was taken on the current sources of the kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    e = d.get(kernel_tag)
-    if not e or e.get("workload") != workload or e.get("source_digest") != kernel_source_digest(kernel_tag):
+    e = d.get(kernel_tag, {}).get(workload)
+    if not e or e.get("source_digest") != kernel_source_digest(kernel_tag):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -53,7 +53,7 @@ struct Sweep {
     int4* blk = nullptr;
     int2* col = nullptr;
     int4* lane = nullptr;
-    int4* tmp = nullptr;     // [n_blocks]: (columns, T, m, gpart lanes) before the scan
+    int4* tmp = nullptr;     // [2 n_blocks]: (columns, T, m, gpart lanes), (first col, end col, head, tail)
     int32_t* err = nullptr;  // [2]: capacity overrun; the total virtual lanes
     int* split = nullptr;    // [phases - 1][cap_lane] resume quads at the cuts
     int phases = 1, rows = 0;
@@ -72,9 +72,9 @@ __device__ __forceinline__ void in_block(const int32_t* col_ptr, int64_t j, int6
 }
 
 // Per block: its column range (from the chunk table), the number m of
-// columns with entries inside the block, and T.
+// columns with entries inside the block, T, and the head / tail columns.
 __global__ void k_sw_count(const int4* __restrict__ cdesc, const int32_t* __restrict__ bnd,
-                           const int32_t* __restrict__ col_ptr, int warps, int4* __restrict__ tmp) {
+                           const int32_t* __restrict__ col_ptr, int warps, int n_blocks, int4* __restrict__ tmp) {
     __shared__ int red[32];
     const int c = blockIdx.x;
     const int64_t lo = cdesc[(int64_t)c * warps].z, hi = cdesc[(int64_t)c * warps + warps - 1].w;
@@ -92,39 +92,61 @@ __global__ void k_sw_count(const int4* __restrict__ cdesc, const int32_t* __rest
         int tot = 0;
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
         const int T = (2 * tot <= kNT) ? kNT : kNT * (int)((2 * (int64_t)tot + kNT - 1) / kNT);
-        tmp[c] = make_int4((int)(hi - lo), T, tot, T - kNT);
-    }
-}
-
-// Prefix sums over the blocks (one thread; n_blocks is the SM count) and the
-// head / tail columns.
-__global__ void k_sw_scan(const int4* __restrict__ tmp, const int4* __restrict__ cdesc,
-                          const int32_t* __restrict__ bnd, const int32_t* __restrict__ col_ptr, int n_blocks,
-                          int warps, int64_t cap_col, int64_t cap_lane, int4* __restrict__ blk,
-                          int32_t* __restrict__ err) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    int64_t rec = 0, lane = 0, gp = 0;
-    for (int c = 0; c < n_blocks; ++c) {
-        const int4 t = tmp[c];
-        const int lo = cdesc[(int64_t)c * warps].z, hi = cdesc[(int64_t)c * warps + warps - 1].w;
-        const int64_t b0 = bnd[c], b1 = bnd[c + 1];
         int head = -1, tail = -1;
         if (b1 > b0 && hi > lo) {
-            if ((int64_t)col_ptr[lo] < b0) head = lo;
+            if ((int64_t)col_ptr[lo] < b0) head = (int)lo;
             // below the last block, hi is the first column starting at or
             // after b1, so column hi - 1 holds entry b1 - 1: the tail when it
             // continues past b1 (and is not the head itself)
-            const int j = hi - 1;
+            const int j = (int)hi - 1;
             if (c < n_blocks - 1 && (int64_t)col_ptr[j + 1] > b1 && j != head) tail = j;
         }
-        blk[2 * c] = make_int4(lo, hi, t.y, (int)lane);
-        blk[2 * c + 1] = make_int4((int)rec, (int)gp, head, tail);
+        tmp[2 * c] = make_int4((int)(hi - lo), T, tot, T - kNT);
+        tmp[2 * c + 1] = make_int4((int)lo, (int)hi, head, tail);
+    }
+}
+
+// Prefix sums over the blocks: one warp, each lane a contiguous run of
+// blocks (n_blocks is the SM count).
+__global__ void k_sw_scan(const int4* __restrict__ tmp, int n_blocks, int64_t cap_col, int64_t cap_lane,
+                          int4* __restrict__ blk, int32_t* __restrict__ err) {
+    const int ln = threadIdx.x;
+    const int per = (n_blocks + 31) / 32;
+    const int c0 = min(n_blocks, ln * per), c1 = min(n_blocks, c0 + per);
+    long long rec = 0, lane = 0, gp = 0;
+    for (int c = c0; c < c1; ++c) {
+        const int4 t = tmp[2 * c];
         rec += t.x;
         lane += t.y;
         gp += t.w;
     }
-    if (rec > cap_col || lane > cap_lane) err[0] = 1;
-    err[1] = (int32_t)min(lane, cap_lane);
+    // exclusive prefix of the lanes' totals
+    long long r2 = rec, l2 = lane, g2 = gp;
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long a = __shfl_up_sync(0xffffffffu, r2, o), b = __shfl_up_sync(0xffffffffu, l2, o),
+                        g = __shfl_up_sync(0xffffffffu, g2, o);
+        if (ln >= o) {
+            r2 += a;
+            l2 += b;
+            g2 += g;
+        }
+    }
+    const long long rec_all = __shfl_sync(0xffffffffu, r2, 31), lane_all = __shfl_sync(0xffffffffu, l2, 31);
+    rec = r2 - rec;
+    lane = l2 - lane;
+    gp = g2 - gp;
+    for (int c = c0; c < c1; ++c) {
+        const int4 t = tmp[2 * c], u = tmp[2 * c + 1];
+        blk[2 * c] = make_int4(u.x, u.y, t.y, (int)lane);
+        blk[2 * c + 1] = make_int4((int)rec, (int)gp, u.z, u.w);
+        rec += t.x;
+        lane += t.y;
+        gp += t.w;
+    }
+    if (ln == 0) {
+        if (rec_all > cap_col || lane_all > cap_lane) err[0] = 1;
+        err[1] = (int32_t)min(lane_all, (long long)cap_lane);
+    }
 }
 
 // Lanes per column and the lane records.  Column records first (a block-wide
@@ -135,7 +157,7 @@ __global__ void k_sw_assign(const int4* __restrict__ tmp, const int4* __restrict
     __shared__ int red[33];
     if (*err) return;
     const int c = blockIdx.x;
-    const int4 t = tmp[c];
+    const int4 t = tmp[2 * c];
     const int4 b = blk[2 * c], b2 = blk[2 * c + 1];
     const int64_t b0 = bnd[c], b1 = bnd[c + 1];
     const int64_t L = b1 - b0;
@@ -265,7 +287,7 @@ int build_sweep(Layer* L, cudaStream_t s) {
         while (S->phases < 8 && (int64_t)S->phases * budget_rows < L->out_f) S->phases *= 2;
         S->rows = (int)((ceil_div(L->out_f, S->phases) + 3) & ~(int64_t)3);
         if (!sw_alloc(&S->blk, 2 * (int64_t)L->n_blocks) || !sw_alloc(&S->col, S->cap_col) ||
-            !sw_alloc(&S->lane, S->cap_lane) || !sw_alloc(&S->tmp, L->n_blocks) || !sw_alloc(&S->err, 2) ||
+            !sw_alloc(&S->lane, S->cap_lane) || !sw_alloc(&S->tmp, 2 * (int64_t)L->n_blocks) || !sw_alloc(&S->err, 2) ||
             !sw_alloc(&S->split, (int64_t)(S->phases - 1) * S->cap_lane)) {
             sw_free_arrays(S);
             return SNK_OK;
@@ -276,9 +298,8 @@ int build_sweep(Layer* L, cudaStream_t s) {
     if (!S->enabled) return SNK_OK;
     S->valid = false;
     cudaMemsetAsync(S->err, 0, 2 * sizeof(int32_t), s);
-    k_sw_count<<<L->n_blocks, 256, 0, s>>>(L->cdesc_c, L->bnd_c, L->col_ptr, W, S->tmp);
-    k_sw_scan<<<1, 32, 0, s>>>(S->tmp, L->cdesc_c, L->bnd_c, L->col_ptr, L->n_blocks, W, S->cap_col, S->cap_lane,
-                               S->blk, S->err);
+    k_sw_count<<<L->n_blocks, 256, 0, s>>>(L->cdesc_c, L->bnd_c, L->col_ptr, W, L->n_blocks, S->tmp);
+    k_sw_scan<<<1, 32, 0, s>>>(S->tmp, L->n_blocks, S->cap_col, S->cap_lane, S->blk, S->err);
     k_sw_assign<<<L->n_blocks, 256, 0, s>>>(S->tmp, S->blk, L->bnd_c, L->col_ptr, S->err, S->col, S->lane);
     if (S->phases > 1)
         k_sw_split<<<(unsigned)std::min<int64_t>(ceil_div(S->cap_lane, 256), (int64_t)L->num_sms * 8), 256, 0, s>>>(
