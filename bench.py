@@ -344,13 +344,26 @@ def tc_launches(op, out_f, in_f, b):
         chunk = max(64, (TC_CHUNK * k_stride) // (out_f + in_f) // 64 * 64)
         return 6 * ((b + chunk - 1) // chunk) + 1
     n_seg = in_f if op == "dx" else out_f
+    n_win = ((out_f if op == "dx" else in_f) + 63) // 64
     n_nt = (n_seg + TC_N - 1) // TC_N
     n = 3
     for c0 in range(0, b, TC_CHUNK):
         n_mt = (min(TC_CHUNK, b - c0) + 127) // 128
-        split = TC_SMS // (n_mt * n_nt)
-        n += 4 if split >= 2 else 3      # split pass, product, (partial sum), exact rows
+        n += 4 if tc_shares_tiles(n_mt * n_nt, n_win) else 3   # split pass, product, (partial sum), exact rows
     return n
+
+
+def tc_shares_tiles(tiles, n_win, sms=TC_SMS):
+    """Whether the tensor forward / dX shares output tiles between CTAs (and
+    so adds the partial-sum kernel): all tiles when they fill at most half a
+    wave, the last partial wave's when they fill more than one, whenever at
+    least 2 ways fit (at most 8, at most one per window)."""
+    def ways(n):
+        return min(8, n_win, sms // max(n, 1))
+    if 2 * tiles <= sms:
+        return ways(tiles) >= 2
+    rem = tiles % sms
+    return tiles > sms and rem > 0 and ways(rem) >= 2
 
 
 def launches_per_op(n_src, b, max_smem):

@@ -292,9 +292,20 @@ struct TcArgs {
     const float* bias;        // [n_seg] or null
     float* Y;                 // [b, n_seg]
     int32_t* status;
-    int split;                // CTAs sharing one output tile, each over a range of windows
-    float* part;              // [split][b][n_seg] their partial sums (split > 1)
+    int full;                 // tiles computed whole by one CTA each (the first `full` in raster order)
+    int split;                // CTAs sharing each remaining tile, each over a range of windows
+    float* part;              // [(tile - full) * split + slice][kTcM][kTcN] their partial sums
 };
+
+// Output tile `id` in raster order: groups of kTcGroupM dense-row tiles
+// sweep all segment tiles.
+__device__ __forceinline__ void tc_tile_of(int id, int n_mt, int n_nt, int& mt, int& nt) {
+    const int gsz = kTcGroupM * n_nt;
+    const int first_m = (id / gsz) * kTcGroupM;
+    const int gm = min(n_mt - first_m, kTcGroupM);
+    mt = first_m + (id % gsz) % gm;
+    nt = (id % gsz) / gm;
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_tc_spmm(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_l,
@@ -314,20 +325,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ int rec_info[kRecSlots][6];
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    // raster: groups of kTcGroupM dense-row tiles sweep all segment tiles;
-    // with a split, slice sk of the grid takes windows [w0, w1) of every tile
-    const int tiles = a.n_mt * a.n_nt;
-    const int sk = blockIdx.x / tiles;
-    const int id = blockIdx.x % tiles;
-    const int gsz = kTcGroupM * a.n_nt;
-    const int first_m = (id / gsz) * kTcGroupM;
-    const int gm = min(a.n_mt - first_m, kTcGroupM);
-    const int mt = first_m + (id % gsz) % gm;
-    const int nt = (id % gsz) / gm;
+    // CTAs below `full` take one whole tile each; the others share the
+    // remaining tiles `split` ways, slice sk taking windows [w0, w1)
+    const bool whole = (int)blockIdx.x < a.full;
+    const int jt = whole ? 0 : (int)blockIdx.x - a.full;   // slot of a shared tile's slice
+    const int id = whole ? (int)blockIdx.x : a.full + jt / a.split;
+    const int sk = whole ? 0 : jt % a.split;
+    const int spl = whole ? 1 : a.split;
+    int mt, nt;
+    tc_tile_of(id, a.n_mt, a.n_nt, mt, nt);
     const int64_t r0 = (int64_t)mt * kTcM;    // first dense row
     const int64_t s0 = (int64_t)nt * kTcN;    // first segment
-    const int w0 = (int)((int64_t)a.n_win * sk / a.split);
-    const int n_win = (int)((int64_t)a.n_win * (sk + 1) / a.split) - w0;   // windows of this CTA
+    const int w0 = (int)((int64_t)a.n_win * sk / spl);
+    const int n_win = (int)((int64_t)a.n_win * (sk + 1) / spl) - w0;   // windows of this CTA
     const int32_t* tp = a.tile_ptr + (int64_t)nt * a.n_win + w0;
 
     if (t == 0) {
@@ -546,10 +556,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int64_t rr = r0 + row;
         if (rr < a.b) {
             // undo the two power-of-two scalings (each factor a normal float);
-            // a split CTA leaves its partial sum for k_tc_split_sum
+            // a slice of a shared tile leaves its partial sum, in tile
+            // coordinates, for k_tc_split_sum
             const float ir = ok ? ldexpf(1.f, -a.row_exp[rr]) : __int_as_float(0x7fc00000);
-            float* yrow = a.split > 1 ? a.part + ((int64_t)sk * a.b + rr) * a.n_seg : a.Y + rr * a.n_seg;
-            const float* bias = a.split > 1 ? nullptr : a.bias;
+            float* yrow = whole ? a.Y + rr * a.n_seg + s0 : a.part + ((int64_t)jt * kTcM + row) * kTcN;
+            const float* bias = whole ? a.bias : nullptr;
             const int c0 = kColsPerThread * half;
 #pragma unroll
             for (int j = 0; j < kColsPerThread; ++j) {
@@ -557,7 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (sg < a.n_seg) {
                     float y = (acc[j] * ir) * __frcp_rn(pw_seg[c0 + j]);
                     if (bias) y += bias[sg];
-                    yrow[sg] = y;
+                    yrow[c0 + j] = y;
                 }
             }
         }
@@ -573,14 +584,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-// Y = bias + the split CTAs' partial sums, added in split order.
-__global__ void k_tc_split_sum(const float* __restrict__ part, int split, int64_t rows, int64_t n_seg,
-                               const float* __restrict__ bias, float* __restrict__ Y) {
-    const int64_t n = rows * n_seg;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+// Y = bias + the slices' partial sums of every shared tile (tiles full ..
+// tiles - 1 in raster order), added in slice order.  One block per shared
+// tile.
+__global__ void k_tc_split_sum(const float* __restrict__ part, int full, int split, int n_mt, int n_nt,
+                               int64_t rows, int64_t n_seg, const float* __restrict__ bias, float* __restrict__ Y) {
+    const int tl = blockIdx.x;   // shared tile, counted from `full`
+    int mt, nt;
+    tc_tile_of(full + tl, n_mt, n_nt, mt, nt);
+    const int64_t r0 = (int64_t)mt * kTcM, s0 = (int64_t)nt * kTcN;
+    for (int i = threadIdx.x; i < kTcM * kTcN; i += blockDim.x) {
+        const int row = i / kTcN, col = i % kTcN;
+        const int64_t rr = r0 + row, sg = s0 + col;
+        if (rr >= rows || sg >= n_seg) continue;
         float y = 0.f;
-        for (int k = 0; k < split; ++k) y += part[(int64_t)k * n + i];
-        Y[i] = bias ? y + bias[i % n_seg] : y;
+        for (int k = 0; k < split; ++k) y += part[((int64_t)(tl * split + k) * kTcM + row) * kTcN + col];
+        Y[rr * n_seg + sg] = bias ? y + bias[sg] : y;
     }
 }
 
@@ -1315,14 +1334,33 @@ bool encode_map(CUtensorMap* map, __half* base, int64_t len, int64_t rows, int64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// CTAs per output tile: when the output tiles fill at most half a wave,
-// each is shared by `split` CTAs over consecutive ranges of windows, as many
-// as still fit one wave (at most kTcMaxSplit).  A split that needs a second
-// wave was measured slower (10000^2, 90%, batch 256: 297 against 257 us).
+// How the output tiles map to CTAs (one CTA per SM).  When the tiles fill
+// at most half a wave, every tile is shared by `split` CTAs over consecutive
+// ranges of windows, as many as still fit one wave (at most kTcMaxSplit).
+// When they fill more than one wave, the tiles of the last, partial wave are
+// shared the same way, as many as fit beside each other, so that wave ends
+// sooner; the others are computed whole.  Anything else runs one CTA per
+// tile: a split that needs a second wave of its own was measured slower
+// (10000^2, 90%, batch 256: 297 against 257 us).
 constexpr int kTcMaxSplit = 8;
-int tc_split(int tiles, int n_win, int num_sms) {
-    const int sp = std::min(std::min(kTcMaxSplit, n_win), num_sms / std::max(tiles, 1));
-    return sp >= 2 ? sp : 1;
+struct TcGrid {
+    int full, split;
+};
+TcGrid tc_grid(int tiles, int n_win, int num_sms) {
+    auto ways = [&](int n) {
+        const int sp = std::min(std::min(kTcMaxSplit, n_win), num_sms / std::max(n, 1));
+        return sp >= 2 ? sp : 1;
+    };
+    if (2 * tiles <= num_sms) {
+        const int sp = ways(tiles);
+        return sp > 1 ? TcGrid{0, sp} : TcGrid{tiles, 1};
+    }
+    const int rem = tiles % num_sms;
+    if (tiles > num_sms && rem > 0) {
+        const int sp = ways(rem);
+        if (sp > 1) return TcGrid{tiles - rem, sp};
+    }
+    return TcGrid{tiles, 1};
 }
 
 // The large-batch workspace, allocated on first use.
@@ -1341,14 +1379,8 @@ int ensure_tc(Layer* L) {
         free_tc(L);
         return SNK_ERR_OOM;
     }
-    // split partials: a split only happens below one wave of tiles, i.e. for
-    // fewer than num_sms / (segment tiles) dense-row tiles
-    for (int side = 0; side < 2; ++side) {
-        const int64_t n_seg = side ? L->in_f : L->out_f;
-        const int64_t n_nt = ceil_div(n_seg, kTcN);
-        const int64_t m_tiles = std::max<int64_t>(1, (L->num_sms - 1) / n_nt);
-        T->part_len = std::max(T->part_len, (int64_t)kTcMaxSplit * kTcM * m_tiles * n_seg);
-    }
+    // slices' partial sums: at most one wave of shared-tile slices
+    T->part_len = (int64_t)L->num_sms * kTcM * kTcN;
     if (!tc_alloc(&T->part, T->part_len)) {
         free_tc(L);
         return SNK_ERR_OOM;
@@ -1415,13 +1447,20 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
         a.bias = bias;
         a.Y = Y + c0 * n_seg;
         a.status = L->status;
-        a.split = tc_split(a.n_mt * a.n_nt, a.n_win, L->num_sms);
+        const int tiles = a.n_mt * a.n_nt;
+        const TcGrid g = tc_grid(tiles, a.n_win, L->num_sms);
+        a.full = g.full;
+        a.split = g.split;
         a.part = T->part;
-        if (a.split > 1 && (int64_t)a.split * bc * n_seg > T->part_len) a.split = 1;
-        k_tc_spmm<<<a.split * a.n_mt * a.n_nt, kTcThreads, kTcSmem, s>>>(mh, ml, a);
-        if (a.split > 1)
-            k_tc_split_sum<<<grid_for((int64_t)bc * n_seg, TH, L->num_sms), TH, 0, s>>>(T->part, a.split, bc, n_seg,
-                                                                                       bias, Y + c0 * n_seg);
+        const int shared = tiles - g.full;   // tiles whose slices leave partial sums
+        if ((int64_t)shared * g.split * kTcM * kTcN > T->part_len) {
+            a.full = tiles;
+            a.split = 1;
+        }
+        k_tc_spmm<<<a.full + (tiles - a.full) * a.split, kTcThreads, kTcSmem, s>>>(mh, ml, a);
+        if (a.full < tiles)
+            k_tc_split_sum<<<tiles - a.full, 256, 0, s>>>(T->part, a.full, a.split, a.n_mt, a.n_nt, bc, n_seg, bias,
+                                                          Y + c0 * n_seg);
         // dense rows of this chunk that the split cannot carry: every output
         // of theirs again, per stored entry
         int st = launch_exact_rows(side, n_seg, Dc, k_len, bias, Y + c0 * n_seg, T->frows,

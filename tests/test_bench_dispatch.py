@@ -48,22 +48,36 @@ def test_rule(monkeypatch):
     assert not bench.tc_path(n, n, 10_000_000, 4096)
 
 
-@pytest.mark.parametrize("b", [256, 4096, 4097, 10_000])
-def test_launch_counts(b):
+# (batch, chunks, chunks whose output tiles are shared) at 10000^2 (53
+# segment tiles, 157 windows) on 152 SMs:
+#   256:   106 tiles, between half a wave and one wave: not shared
+#   4096:  1696 tiles = 11 waves + 24: the 24 shared 6 ways
+#   4097:  1749 tiles = 11 waves + 77: only one way fits, not shared
+#   10000: chunks of 8192 and 1808 rows: 3392 = 22 waves + 48 (3 ways) and
+#          795 = 5 waves + 35 (4 ways)
+@pytest.mark.parametrize("b,chunks,shared", [(256, 1, 0), (4096, 1, 1), (4097, 1, 0), (10_000, 2, 2)])
+def test_launch_counts(b, chunks, shared):
     # forward / dX: segment scales and tile-order values once, then a split,
-    # a product and an exact-row kernel per chunk of kTcChunk rows, and one
-    # exact-segment kernel
-    chunks = -(-b // bench.TC_CHUNK)
-    # one output-tile row (b <= 128) below half a wave of 53 segment tiles:
-    # a split over windows adds the partial-sum kernel
-    split = 1 if b > 128 else 2
-    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 3 + 3 * chunks + (chunks if split > 1 else 0)
+    # a product and an exact-row kernel per chunk of kTcChunk rows (plus the
+    # partial-sum kernel where tiles are shared), and one exact-segment kernel
+    assert chunks == -(-b // bench.TC_CHUNK)
+    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 3 + 3 * chunks + shared
     # dW: two column passes, a flag decision, two transposes and a product
     # kernel per chunk, then one exact-entry kernel; the chunk is what the
     # shared fp16 workspace holds for both operands
     k_stride = 10_000
     chunk = (bench.TC_CHUNK * k_stride) // 20_000 // 64 * 64
     assert bench.tc_launches("dw", 10_000, 10_000, b) == 6 * (-(-b // chunk)) + 1
+
+
+def test_tensor_tile_sharing():
+    """At most half a wave of tiles: all shared; more than a wave: the last
+    partial wave's; in between, or when fewer than 2 ways fit: none."""
+    assert bench.tc_shares_tiles(53, 157)          # b = 128 at 10000^2: 2 ways
+    assert not bench.tc_shares_tiles(106, 157)     # b = 256: one partial wave
+    assert bench.tc_shares_tiles(212, 157)         # b = 512: 60 left over, 2 ways
+    assert not bench.tc_shares_tiles(152, 157)     # exactly one wave
+    assert not bench.tc_shares_tiles(53, 1)        # one window: nothing to split
 
 
 def test_source_digest_ignores_comments():

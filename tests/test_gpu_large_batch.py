@@ -67,6 +67,8 @@ def _check(torch, lay, X, dY, bias, rows=None, weight=True):
     (64, 64, 0, 200),         # fully dense W
     (450, 390, 90, 4500),     # weight gradient over two batch chunks (4416 + 84 rows)
     (1000, 700, 99, 300),     # sparse windows: stages cleared entry by entry, not by bulk copy
+    (2000, 1500, 90, 2560),   # more output tiles than SMs (152): the last partial wave's
+                              # tiles shared 2 ways (forward, 220 tiles) and 8 ways (dX, 160)
 ])
 def test_forced_small_shapes(torch, monkeypatch, out_f, in_f, sp, b):
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
