@@ -310,8 +310,9 @@ def run_reference(args, workload, rank, world):
 # and more at density 1% and above, 128 and more at 5% and above) and the
 # launches that path makes per call: per-call passes plus the product kernels
 # of each batch chunk.
-TC_MIN_BATCH, TC_DENSITY_DIV, TC_CHUNK = 256, 100, 8192
+TC_MIN_BATCH, TC_DENSITY_DIV, TC_CHUNK = 256, 50, 8192
 TC_MIN_BATCH_DENSE, TC_DENSITY_DIV_DENSE = 128, 20
+TC_MIN_BATCH_SPARSE, TC_DENSITY_DIV_SPARSE = 512, 100
 TC_SMS, TC_N = 152, 192
 
 
@@ -319,8 +320,9 @@ def tc_path(out_f, in_f, nnz, b):
     mode = os.environ.get("SNK_LARGE_BATCH")
     if nnz == 0 or mode == "off":
         return False
-    return mode == "on" or (b >= TC_MIN_BATCH and nnz * TC_DENSITY_DIV >= out_f * in_f) or \
-        (b >= TC_MIN_BATCH_DENSE and nnz * TC_DENSITY_DIV_DENSE >= out_f * in_f)
+    return mode == "on" or (b >= TC_MIN_BATCH_DENSE and nnz * TC_DENSITY_DIV_DENSE >= out_f * in_f) or \
+        (b >= TC_MIN_BATCH and nnz * TC_DENSITY_DIV >= out_f * in_f) or \
+        (b >= TC_MIN_BATCH_SPARSE and nnz * TC_DENSITY_DIV_SPARSE >= out_f * in_f)
 
 
 def dx_kernel(out_f, in_f, b, num_sms=152):

@@ -1244,12 +1244,15 @@ int build_view(Layer* L, int mode, cudaStream_t s) {
 
 // Which path: SNK_LARGE_BATCH=on|off forces it (tests); otherwise the
 // measured crossover with 64-row batch tiling (10000^2 and 5000^2 layers):
+// from kTcMinBatchDense rows at density 1 / kTcDensityDivDense and above,
 // from kTcMinBatch rows at density 1 / kTcDensityDiv and above, and from
-// kTcMinBatchDense rows at density 1 / kTcDensityDivDense and above.
-constexpr int64_t kTcMinBatch = 256;
-constexpr int64_t kTcDensityDiv = 100;
+// kTcMinBatchSparse rows at density 1 / kTcDensityDivSparse and above.
 constexpr int64_t kTcMinBatchDense = 128;
 constexpr int64_t kTcDensityDivDense = 20;
+constexpr int64_t kTcMinBatch = 256;
+constexpr int64_t kTcDensityDiv = 50;
+constexpr int64_t kTcMinBatchSparse = 512;
+constexpr int64_t kTcDensityDivSparse = 100;
 
 }  // namespace
 
@@ -1262,8 +1265,9 @@ bool tc_eligible(const Layer* L, int64_t b) {
     const char* f = getenv("SNK_LARGE_BATCH");
     if (f && strcmp(f, "off") == 0) return false;
     if (f && strcmp(f, "on") == 0) return true;
-    return (b >= kTcMinBatch && L->nnz * kTcDensityDiv >= L->out_f * L->in_f) ||
-           (b >= kTcMinBatchDense && L->nnz * kTcDensityDivDense >= L->out_f * L->in_f);
+    return (b >= kTcMinBatchDense && L->nnz * kTcDensityDivDense >= L->out_f * L->in_f) ||
+           (b >= kTcMinBatch && L->nnz * kTcDensityDiv >= L->out_f * L->in_f) ||
+           (b >= kTcMinBatchSparse && L->nnz * kTcDensityDivSparse >= L->out_f * L->in_f);
 }
 
 void free_tc(Layer* L) {

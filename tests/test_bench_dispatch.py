@@ -29,6 +29,8 @@ def test_constants_match_the_library():
     assert bench.TC_CHUNK == _const("kTcChunk")
     assert bench.TC_MIN_BATCH_DENSE == _const("kTcMinBatchDense")
     assert bench.TC_DENSITY_DIV_DENSE == _const("kTcDensityDivDense")
+    assert bench.TC_MIN_BATCH_SPARSE == _const("kTcMinBatchSparse")
+    assert bench.TC_DENSITY_DIV_SPARSE == _const("kTcDensityDivSparse")
 
 
 def test_rule(monkeypatch):
@@ -39,7 +41,11 @@ def test_rule(monkeypatch):
     assert bench.tc_path(n, n, 5_000_000, 128)           # exactly 5%
     assert not bench.tc_path(n, n, 4_999_999, 255)       # below 5%: from 256 rows
     assert bench.tc_path(n, n, 4_999_999, 256)
-    assert bench.tc_path(n, n, 1_000_000, 4096)          # exactly 1%
+    assert bench.tc_path(n, n, 2_000_000, 256)           # exactly 2%
+    assert not bench.tc_path(n, n, 1_999_999, 511)       # below 2%: from 512 rows
+    assert bench.tc_path(n, n, 1_999_999, 512)
+    assert bench.tc_path(n, n, 1_000_000, 512)           # exactly 1%
+    assert bench.tc_path(n, n, 1_000_000, 4096)
     assert not bench.tc_path(n, n, 999_999, 4096)        # below 1%
     assert not bench.tc_path(n, n, 0, 4096)
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
