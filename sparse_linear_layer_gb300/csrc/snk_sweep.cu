@@ -62,6 +62,7 @@ struct Sweep {
 namespace {
 
 constexpr int kNT = kThreadsDx;
+constexpr int64_t kSweepMaxCols = int64_t(1) << 24;   // 16M columns: 128 MB of column records
 
 // Entry range of column j inside block [b0, b1).
 __device__ __forceinline__ void in_block(const int32_t* col_ptr, int64_t j, int64_t b0, int64_t b1, int64_t& s,
@@ -265,8 +266,10 @@ void free_sweep(Layer* L) {
 // Build (or rebuild in place) the sweep tables after the column view and its
 // partition.  The first build allocates them at their upper bounds: column
 // records <= in + n_blocks (neighbouring blocks share at most the cut
-// column), virtual lanes <= NT n_blocks + 2 (in + n_blocks), global partials
-// <= 2 (in + n_blocks) lanes of 4 floats in the transposed-operand scratch.
+// column), virtual lanes <= NT n_blocks + 2 min(in + n_blocks, nnz +
+// n_blocks), global partials <= 2 (in + n_blocks) lanes of 4 floats in the
+// transposed-operand scratch.  Layers wider than kSweepMaxCols columns get
+// no tables.
 // Layers without 16-bit rows (out > 65536) or entries get no tables; so does
 // a layer whose scratch is too small.  A failure leaves the chunk walk in use.
 int build_sweep(Layer* L, cudaStream_t s) {
@@ -276,8 +279,13 @@ int build_sweep(Layer* L, cudaStream_t s) {
         L->sweep = new Sweep();
         Sweep* S = L->sweep;
         if (!L->rc16 || n == 0) return SNK_OK;
+        // a record per column (empty ones too): very wide layers keep the
+        // chunk walk rather than gigabytes of tables
+        if (L->in_f > kSweepMaxCols) return SNK_OK;
         S->cap_col = L->in_f + L->n_blocks;
-        S->cap_lane = (int64_t)kNT * L->n_blocks + 2 * S->cap_col;
+        // non-empty columns per block, summed, are at most the entries (plus
+        // the columns cut between blocks)
+        S->cap_lane = (int64_t)kNT * L->n_blocks + 2 * std::min(S->cap_col, n + L->n_blocks);
         if (8 * S->cap_col > std::max(L->out_f, L->in_f) * kMaxBatchTile) return SNK_OK;
         if (S->cap_lane >= INT32_MAX || n >= INT32_MAX) return SNK_OK;
         // phases: the least power of two (at most 8) that keeps a phase of a
