@@ -137,6 +137,8 @@ struct SweepView {
     int64_t n_lane;
     int phases;         // row phases of the tables (a power of two, at most 8)
     int rows;           // rows per phase (a multiple of 4)
+    const int32_t* perm;   // the column view's slots and 16-bit rows, reordered within quads
+    const uint16_t* r16;
 };
 int build_sweep(Layer* L, cudaStream_t s);
 void mark_sweep(Layer* L);

@@ -703,6 +703,8 @@ static int launch_bp(Layer* L, SpmmArgs a, cudaStream_t s) {
                 a.sw_rows = (int)rows;
                 a.sw_phases = phases;
                 a.sw_stride = stride;
+                a.perm = v.perm;
+                a.idx16 = v.r16;
                 auto fn = k_sweep<BP>;
                 if (set_smem(fn, smem_sw) != SNK_OK) return SNK_ERR_CUDA;
                 fn<<<a.n_blocks, kThreadsDx, smem_sw, s>>>(a);

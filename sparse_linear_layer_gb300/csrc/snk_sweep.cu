@@ -57,6 +57,8 @@ struct Sweep {
     int32_t* err = nullptr;  // [2]: capacity overrun; the total virtual lanes
     int* split = nullptr;    // [phases - 1][cap_lane] resume quads at the cuts
     int phases = 1, rows = 0;
+    int32_t* perm = nullptr;  // [nnz_pad] the column view's slots, reordered within quads
+    uint16_t* r16 = nullptr;  // [nnz_pad] its rows, reordered the same way
 };
 
 namespace {
@@ -230,6 +232,119 @@ __global__ void k_sw_split(const int4* __restrict__ lane, const int32_t* __restr
     }
 }
 
+// Order within quads.  In a 128-bit shared load of operand rows a warp is
+// served 8 lanes at a time; two lanes of such a quarter that read different
+// rows with the same row mod 8 (the same 4 banks, with 4-column rows) cost
+// an extra pass.  The quarter's 8 lanes load their quads' entries in the
+// same slot order, and the order of the 4 entries inside a quad is free (a
+// lane adds them into its own sums).  So for every quarter (8 consecutive
+// lanes of a block) and every step of its walk (the quads its lanes take
+// side by side, phase by phase, as a 4-column tile runs them), the entries
+// of each quad are put in the order that, lane after lane, adds the fewest
+// repeated row groups per slot (greedy over the 24 orders; modelled 2.60 ->
+// 1.96 passes per quarter with random rows).  Only quads wholly inside their
+// column's range in the block and not straddling a phase cut are reordered;
+// each such quad belongs to exactly one lane, so the writes do not overlap.
+// The copies the sweep reads (perm, 16-bit rows) are the library's own; the
+// column view returned to callers keeps its order.
+__device__ __forceinline__ int sw_cost_add(const unsigned char (&cnt)[4][8], const int (&g)[4], const int (&o)[4]) {
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c += cnt[j][g[o[j]]];   // entries already in that slot's group
+    return c;
+}
+
+__global__ void k_sw_order(const int4* __restrict__ lane, const int4* __restrict__ blk, const int* __restrict__ split,
+                           int phases, int64_t cap_lane, const int32_t* __restrict__ err,
+                           const int32_t* __restrict__ perm, const uint16_t* __restrict__ r16,
+                           int32_t* __restrict__ perm_o, uint16_t* __restrict__ r16_o) {
+    if (err[0]) return;
+    const int c = blockIdx.x;
+    const int quarter = threadIdx.x;   // blockDim = kNT / 8
+    const int4 b = blk[2 * c];
+    const int lane0 = b.w + quarter * 8;
+    // the 24 orders of a quad
+    int orders[24][4];
+    {
+        int n = 0;
+        for (int a0 = 0; a0 < 4; ++a0)
+            for (int a1 = 0; a1 < 4; ++a1)
+                for (int a2 = 0; a2 < 4; ++a2) {
+                    const int a3 = 6 - a0 - a1 - a2;
+                    if (a0 == a1 || a0 == a2 || a1 == a2 || a3 < 0 || a3 > 3 || a3 == a0 || a3 == a1 || a3 == a2)
+                        continue;
+                    orders[n][0] = a0;
+                    orders[n][1] = a1;
+                    orders[n][2] = a2;
+                    orders[n][3] = a3;
+                    ++n;
+                }
+    }
+    int4 ln[8];
+    for (int l = 0; l < 8; ++l) ln[l] = lane[lane0 + l];
+    for (int p = 0; p < phases; ++p) {
+        uint32_t u[8], qend[8];
+        int skip[8];   // a quad of this lane that straddles a cut (left unordered)
+        for (int l = 0; l < 8; ++l) {
+            const uint32_t qe = ((uint32_t)ln[l].w + 3) >> 2;
+            u[l] = p == 0 ? (uint32_t)ln[l].x : (uint32_t)(split[(int64_t)(p - 1) * cap_lane + lane0 + l] >> 1);
+            if (p + 1 < phases) {
+                const int sp = split[(int64_t)p * cap_lane + lane0 + l];
+                qend[l] = min(qe, (uint32_t)(sp >> 1) + (uint32_t)(sp & 1));
+                skip[l] = (sp & 1) ? (sp >> 1) : -1;
+            } else {
+                qend[l] = qe;
+                skip[l] = -1;
+            }
+        }
+        for (int i = 0;; ++i) {
+            bool any = false;
+            unsigned char cnt[4][8];
+            for (int j = 0; j < 4; ++j)
+                for (int g = 0; g < 8; ++g) cnt[j][g] = 0;
+            // quads of this step: fixed ones first, then the free ones lane by lane
+            for (int pass = 0; pass < 2; ++pass) {
+                for (int l = 0; l < 8; ++l) {
+                    const uint32_t st = (uint32_t)ln[l].y, s0 = (uint32_t)ln[l].z, e0 = (uint32_t)ln[l].w;
+                    const uint32_t q = u[l] + (uint32_t)i * st;
+                    if (q >= qend[l]) continue;
+                    any = true;
+                    const bool first_of_phase = p > 0 && q == u[l] && i == 0;   // may straddle the previous cut
+                    const bool free_q = 4 * q >= s0 && 4 * q + 3 < e0 && (int)q != skip[l] && !first_of_phase;
+                    if ((pass == 0) == free_q) continue;
+                    int g[4];
+                    for (int j = 0; j < 4; ++j) g[j] = r16[4 * q + j] & 7;
+                    if (!free_q) {
+                        for (int j = 0; j < 4; ++j) cnt[j][g[j]] += 1;
+                        continue;
+                    }
+                    int best = 0, best_cost = 1 << 30;
+                    for (int o = 0; o < 24; ++o) {
+                        const int cst = sw_cost_add(cnt, g, orders[o]);
+                        if (cst < best_cost) {
+                            best_cost = cst;
+                            best = o;
+                        }
+                    }
+                    int pv[4];
+                    uint16_t rv[4];
+                    for (int j = 0; j < 4; ++j) {
+                        const int src = 4 * q + orders[best][j];
+                        pv[j] = perm[src];
+                        rv[j] = r16[src];
+                        cnt[j][g[orders[best][j]]] += 1;
+                    }
+                    for (int j = 0; j < 4; ++j) {
+                        perm_o[4 * q + j] = pv[j];
+                        r16_o[4 * q + j] = rv[j];
+                    }
+                }
+            }
+            if (!any) break;
+        }
+    }
+}
+
 template <typename T>
 bool sw_alloc(T** p, int64_t count) {
     if (cudaMalloc((void**)p, (size_t)std::max<int64_t>(count, 1) * sizeof(T)) != cudaSuccess) {
@@ -241,10 +356,12 @@ bool sw_alloc(T** p, int64_t count) {
 }
 
 void sw_free_arrays(Sweep* S) {
-    void* ptrs[] = {S->blk, S->col, S->lane, S->tmp, S->err, S->split};
+    void* ptrs[] = {S->blk, S->col, S->lane, S->tmp, S->err, S->split, S->perm, S->r16};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     S->split = nullptr;
+    S->perm = nullptr;
+    S->r16 = nullptr;
     S->blk = nullptr;
     S->col = nullptr;
     S->lane = nullptr;
@@ -296,7 +413,8 @@ int build_sweep(Layer* L, cudaStream_t s) {
         S->rows = (int)((ceil_div(L->out_f, S->phases) + 3) & ~(int64_t)3);
         if (!sw_alloc(&S->blk, 2 * (int64_t)L->n_blocks) || !sw_alloc(&S->col, S->cap_col) ||
             !sw_alloc(&S->lane, S->cap_lane) || !sw_alloc(&S->tmp, 2 * (int64_t)L->n_blocks) || !sw_alloc(&S->err, 2) ||
-            !sw_alloc(&S->split, (int64_t)(S->phases - 1) * S->cap_lane)) {
+            !sw_alloc(&S->split, (int64_t)(S->phases - 1) * S->cap_lane) || !sw_alloc(&S->perm, L->nnz_pad) ||
+            !sw_alloc(&S->r16, L->nnz_pad)) {
             sw_free_arrays(S);
             return SNK_OK;
         }
@@ -312,6 +430,11 @@ int build_sweep(Layer* L, cudaStream_t s) {
     if (S->phases > 1)
         k_sw_split<<<(unsigned)std::min<int64_t>(ceil_div(S->cap_lane, 256), (int64_t)L->num_sms * 8), 256, 0, s>>>(
             S->lane, S->err, L->rows_c, S->phases, S->rows, S->cap_lane, S->split);
+    // the sweep's own streams: the column view, then its quads reordered
+    cudaMemcpyAsync(S->perm, L->perm, L->nnz_pad * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    cudaMemcpyAsync(S->r16, L->rc16, L->nnz_pad * sizeof(uint16_t), cudaMemcpyDeviceToDevice, s);
+    k_sw_order<<<L->n_blocks, kNT / 8, 0, s>>>(S->lane, S->blk, S->split, S->phases, S->cap_lane, S->err, L->perm,
+                                              L->rc16, S->perm, S->r16);
     int32_t err = 0;
     if (cudaGetLastError() != cudaSuccess ||
         cudaMemcpyAsync(&err, S->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -334,6 +457,8 @@ bool sweep_view(const Layer* L, SweepView* v) {
     v->lane = S->lane;
     v->split = S->split;
     v->n_lane = S->cap_lane;
+    v->perm = S->perm;
+    v->r16 = S->r16;
     v->phases = S->phases;
     v->rows = S->rows;
     return true;
