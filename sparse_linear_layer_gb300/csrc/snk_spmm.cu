@@ -386,8 +386,10 @@ __global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmAr
 // Column sweep of the transposed product (batch tile BP <= 4, operand in
 // shared memory).  (An 8-column version measured no faster than the chunk
 // walk at 10000^2, 90%, and slower at 95% and 99%: two 128-bit operand loads
-// per entry and twice the row phases.)  Every column of the block has its own lanes (snk_sweep.cu
-// builds the tables); lane j of a column with n lanes takes the column's
+// per entry and twice the row phases.)  Every column of the block has its
+// own lanes (snk_sweep.cu builds the tables, and orders the entries within
+// quads so that the rows 8 lanes load together spread over the banks); lane j
+// of a column with n lanes takes the column's
 // aligned quads j, j + n, j + 2n, ... and masks the entries outside the
 // column's range in this block.  Rows rise along a column, so all lanes move
 // down the rows together, and the values they gather for nearby rows share
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmAr
 // 160 KB of an SM's 256 KB at out = 10000).  The tables cut the rows into P
 // equal phases (P a power of two, about SNK_SWEEP_PHASE_KB of shared memory
 // each at a 4-column tile) and hold, for every lane and cut, the quad where
-// the lane crosses it; a launch with a narrower tile merges phases.  A phase
+// the lane crosses it; a 1-column tile merges phases in pairs.  A phase
 // takes the entries whose rows it holds, up to that quad (inclusive when the
 // quad straddles the cut), and the next phase resumes there, so a lane's
 // loop bound is known before it starts.
@@ -679,8 +681,10 @@ static int launch_bp(Layer* L, SpmmArgs a, cudaStream_t s) {
     const size_t smem = operand_floats(a.n_src, BP) * sizeof(float) + slots;
     if constexpr (GATHER && BP <= 4) {
         // the column sweep, when the layer has its tables: the tables cut
-        // the rows into P equal phases (P a power of two); a 4-column tile
-        // takes them all, 2 and 1 columns take P / 2 and P / 4 (at least one)
+        // the rows into P equal phases (P a power of two, ~96 KB of a
+        // 4-column operand each); 4- and 2-column tiles take them all (the
+        // 2-column phases then leave L1 more room: 35.0 against 36.4 us at
+        // 10000^2, 90%), a 1-column tile takes P / 2 (at least one)
         SweepView v;
         if (a.idx16 && !a.bias && sweep_view(L, &v)) {
             // Phases pay for a barrier and a restart of every lane's stream;
@@ -689,7 +693,7 @@ static int launch_bp(Layer* L, SpmmArgs a, cudaStream_t s) {
             // against 20.4 us).
             const bool few = a.nnz < (int64_t)32 * a.n_blocks * kThreadsDx;
             const bool fits = operand_floats(a.n_src, BP) * sizeof(float) <= (size_t)L->max_smem;
-            const int phases = (few && fits) ? 1 : std::max(1, v.phases * BP / 4);
+            const int phases = (few && fits) ? 1 : (BP >= 2 ? v.phases : std::max(1, v.phases / 2));
             const int stride = v.phases / phases;
             const int64_t rows = phases == 1 ? a.n_src : std::min<int64_t>(a.n_src, (int64_t)v.rows * stride);
             const size_t smem_sw = std::max(operand_floats(rows, BP), (size_t)kThreadsDx * BP) * sizeof(float);
