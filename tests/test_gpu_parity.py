@@ -187,6 +187,18 @@ def test_operand_larger_than_shared_memory(torch):
         check_all_products(torch, lay, b)
 
 
+@pytest.mark.parametrize("in_f", [16_384, 28_000, 56_000])
+def test_sixteen_bit_columns_of_wide_layers(torch, in_f):
+    """The 16-bit column copy with its top bits in use (columns up to 55,999,
+    above 32,767 from 32,768 on): b = 1 stages every width here in shared
+    memory and takes the 16-bit path; b = 2 does so up to 28,000 columns and
+    reads 56,000 from global memory."""
+    lay = synth.make_layer(600, in_f, 98, 0.05, 61, 62)
+    assert lay.cols.max() == in_f - 1
+    for b in (1, 2):
+        check_all_products(torch, lay, b)
+
+
 def test_no_entries(torch):
     lay = synth.Layer(6, 9, np.zeros(0, np.float32), np.zeros(0, np.int32), np.zeros(0, np.int32))
     check_all_products(torch, lay, 3)
