@@ -58,6 +58,9 @@ def parse():
     p.add_argument("--inp", type=int, default=10000)
     p.add_argument("--sparsity", type=float, default=90)
     p.add_argument("--batch", type=int, default=4)
+    p.add_argument("--zipf", type=float, default=None, metavar="S",
+                   help="power-law (Zipf, exponent S) row degrees instead of a uniform support "
+                        "(the GPT-2-shaped MLP layers use S = 1.2)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-restructure", action="store_true")
@@ -270,7 +273,7 @@ def run_reference(args, workload, rank, world):
     import oracle
     from sparse_linear_layer_gb300 import synth
     oracle.build()
-    lay0 = synth.make_layer(args.out, args.inp, args.sparsity, 0.01, 21, 22)
+    lay0 = synth.make_layer(args.out, args.inp, args.sparsity, 0.01, 21, 22, zipf_s=args.zipf)
     can = oracle.canonicalize(args.out, args.inp, lay0.values, lay0.rows, lay0.cols)
     can["out"], can["in"] = args.out, args.inp
     b = args.batch
@@ -486,9 +489,9 @@ def summarize(per_op_ms, alg, formula, peak):
     return out
 
 
-def make_device_layer(torch, binding, synth, dev, out_f, in_f, sparsity, b):
+def make_device_layer(torch, binding, synth, dev, out_f, in_f, sparsity, b, zipf_s=None):
     import numpy as np
-    lay = synth.make_layer(out_f, in_f, sparsity, 0.01, 21, 22)
+    lay = synth.make_layer(out_f, in_f, sparsity, 0.01, 21, 22, zipf_s=zipf_s)
     X_h = synth.normal((b, in_f), 1.0, 23)
     dY_h = synth.normal((b, out_f), 1.0, 24)
     bias_h = synth.normal(out_f, 0.1, 25)
@@ -806,7 +809,7 @@ def run_ours(args, workload, rank, world, local):
 
     out_f, in_f, b = args.out, args.inp, args.batch
     lay, g, X_h, dY_h, X, dY, bias = make_device_layer(torch, binding, synth, dev, out_f, in_f,
-                                                       args.sparsity, b)
+                                                       args.sparsity, b, args.zipf)
     nnz = lay.nnz
     Y = torch.empty((b, out_f), device=dev)
     dX = torch.empty((b, in_f), device=dev)
@@ -1018,9 +1021,12 @@ def main():
         nnz = synth.nnz_for(args.out, args.inp, args.sparsity)
     except Exception:
         pass
+    zipf = "" if args.zipf is None else f"_zipf{args.zipf:g}"
+    support = ("uniform random sparsity" if args.zipf is None
+               else f"sparsity with Zipf (s = {args.zipf:g}) row degrees")
     workload = {
-        "workload": f"layer{args.out}x{args.inp}_s{args.sparsity:g}_b{args.batch}",
-        "description": f"W {args.out}x{args.inp}, {args.sparsity:g}% uniform random sparsity, fp32, "
+        "workload": f"layer{args.out}x{args.inp}_s{args.sparsity:g}{zipf}_b{args.batch}",
+        "description": f"W {args.out}x{args.inp}, {args.sparsity:g}% {support}, fp32, "
                        f"batch {args.batch}; step = forward (bias) + backward_input + "
                        f"backward_weight (db)",
         "out": args.out, "in": args.inp, "sparsity_pct": args.sparsity, "nnz": nnz,
