@@ -25,6 +25,7 @@ static void free_layer(Layer* L) {
     free_pcsr(L);
     free_tc(L);
     free_sweep(L);
+    free_bands(L);
     void* ptrs[] = {L->row_ptr, L->col_ptr, L->rows_c, L->perm, L->c16, L->rc16, L->bnd_r, L->bnd_c, L->cdesc_r, L->cdesc_c,
                     L->bdesc_r, L->bdesc_c,
                     L->part, L->cnt, L->xt, L->status, L->sort_keys, L->sort_vals,

@@ -164,6 +164,63 @@ __device__ __forceinline__ void padded4(const int32_t* __restrict__ p, uint32_t 
     w[3] = t.w;
 }
 
+// ---- a band of the transposed operand into shared memory, by the TMA engine
+// (one contiguous run: cp.async.bulk, issued by one thread, completed on an
+// mbarrier that every thread then waits on, within a bounded number of
+// cycles).
+constexpr long long kStageWaitCycles = 4000000000LL;   // about two seconds at the boost clock
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void stage_bar_init(uint64_t* bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// bytes: a multiple of 16, both addresses 16-byte aligned; copied in runs of
+// at most 64 KB, all counted on the same barrier phase.
+__device__ __forceinline__ void stage_bulk(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    for (uint32_t off = 0; off < bytes; off += 65536u) {
+        const uint32_t n = min(65536u, bytes - off);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_addr(static_cast<char*>(dst) + off)),
+                     "l"(static_cast<const char*>(src) + off), "r"(n), "r"(smem_addr(bar))
+                     : "memory");
+    }
+}
+// Wait for phase 0 of the barrier; false once `limit` cycles have passed.
+__device__ __forceinline__ bool stage_wait(uint64_t* bar, long long limit) {
+    long long t0 = 0;
+    for (int spin = 0;; ++spin) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(smem_addr(bar))
+            : "memory");
+        if (ok) return true;
+        if (spin == 0)
+            t0 = clock64();
+        else if (clock64() - t0 > limit)
+            return false;
+    }
+}
+// Rows [r0, r0 + rows) of a transposed operand xt[n][BP] into dst.  A wait
+// that runs out records kStatLimit in *status and waits once more (for the
+// copy still landing) before the block goes on; its results are then not
+// to be trusted, and the caller learns it from the status word.
+template <int BP>
+__device__ __forceinline__ void stage_band(float* dst, const float* xt, int r0, int rows, uint64_t* bar,
+                                           int32_t* status) {
+    if (threadIdx.x == 0) stage_bar_init(bar);
+    __syncthreads();
+    if (rows <= 0) return;
+    if (threadIdx.x == 0) stage_bulk(dst, xt + (int64_t)r0 * BP, (uint32_t)rows * BP * 4u, bar);
+    if (!stage_wait(bar, kStageWaitCycles)) {
+        if (status) atomicOr(status, kStatLimit);
+        stage_wait(bar, kStageWaitCycles);
+    }
+}
+
 // Stage the operand transposed: dst[i*BP + beta] = src[beta*ld + i] for
 // beta < b, 0 for b <= beta < BP, for i < n.  When the rows of src are
 // 16-byte aligned, groups of 4 columns are read with 128-bit loads (one per

@@ -38,6 +38,9 @@ constexpr int kWarp = 32;
 #ifndef SNK_SWEEP_NS
 #define SNK_SWEEP_NS 3     // column sweep: quads in flight per lane
 #endif
+#ifndef SNK_BANDS
+#define SNK_BANDS 1        // dW: row runs over column bands for wide operands at batch tiles >= 8
+#endif
 
 constexpr int kThreads = SNK_THREADS;
 constexpr int kWarpsPerBlock = kThreads / kWarp;
@@ -56,6 +59,7 @@ struct RestructureWs;
 struct PcsrState;
 struct TcState;
 struct Sweep;
+struct Bands;
 
 // Per block: its entry range [k0, k1), and for the segment that enters the
 // block from before (head) and the one that leaves it (tail) the first and
@@ -122,6 +126,7 @@ struct Layer {
     PcsrState* pcsr = nullptr;    // Padded-CSR view, built on request
     TcState* tc = nullptr;        // tile-ordered views of the large-batch path, built on first use
     Sweep* sweep = nullptr;       // lane tables of the column sweep (snk_sweep.cu)
+    Bands* bands = nullptr;       // dW's row-run tables over column bands (snk_band.cu), built on first use
 };
 
 void free_pcsr(Layer* L);
@@ -144,6 +149,20 @@ int build_sweep(Layer* L, cudaStream_t s);
 void mark_sweep(Layer* L);
 void free_sweep(Layer* L);
 bool sweep_view(const Layer* L, SweepView* v);
+
+// ---- row runs over column bands (snk_band.cu) ------------------------------
+// dW for a batch tile of bp >= 8 columns whose operand does not fit shared
+// memory: each block stages one band of the transposed operand and walks the
+// runs of its rows in that band.  *done says whether the layer took this path
+// (false: no bands for it; the caller goes on).
+int band_backward_weight(Layer* L, int bp, const float* X, const float* dY, int b, float* dW, bool accumulate,
+                         const float* dY_all, int64_t b_all, float* db, cudaStream_t s, bool* done);
+// The band count and width for a batch tile of bp columns; false when the
+// layer takes no bands (operand fits, runs too short, or too few entries).
+bool band_shape(const Layer* L, int bp, int* nb, int* width);
+int refresh_bands(Layer* L, cudaStream_t s);
+void mark_bands(Layer* L);
+void free_bands(Layer* L);
 
 // ---- large-batch path on the tensor cores (snk_tc.cu) ---------------------
 bool tc_eligible(const Layer* L, int64_t b);

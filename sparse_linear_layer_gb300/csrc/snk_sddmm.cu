@@ -214,6 +214,15 @@ template <int BP>
 static int launch_bp(Layer* L, SddmmArgs a, cudaStream_t s) {
     const size_t smem = (size_t)a.in_f * BP * sizeof(float);
     const int grid = a.n_blocks;
+    if constexpr (BP >= 8 && SNK_BANDS) {
+        // an operand too wide for shared memory: row runs over column bands
+        if (smem > (size_t)L->max_smem) {
+            bool done = false;
+            const int st = band_backward_weight(L, BP, a.X, a.dY, a.b, a.dW, a.accumulate, a.dY_all, a.b_all,
+                                                a.db, s, &done);
+            if (st != SNK_OK || done) return st;
+        }
+    }
     if (smem <= (size_t)L->max_smem && a.col16) {
         auto fn = k_sddmm<BP, true>;
         if (smem > 48 * 1024 &&

@@ -550,11 +550,13 @@ int build_views(Layer* L, cudaStream_t s) {
         return SNK_ERR_CUDA;
     if (refresh_tc_views(L, s) != SNK_OK) return SNK_ERR_CUDA;
     if (int st = build_sweep(L, s); st != SNK_OK) return st;
+    if (int st = refresh_bands(L, s); st != SNK_OK) return st;
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SNK_ERR_CUDA;
     L->topology_version += 1;
     mark_tc_views(L);
     mark_sweep(L);
+    mark_bands(L);
     return SNK_OK;
 }
 
