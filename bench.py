@@ -156,6 +156,7 @@ KERNEL_SOURCES = {
     "k_spmm_dx": ["snk_spmm.cu", "snk_device.cuh", "snk_internal.cuh"],
     "k_sweep_dx": ["snk_spmm.cu", "snk_sweep.cu", "snk_device.cuh", "snk_internal.cuh"],
     "k_sddmm": ["snk_sddmm.cu", "snk_device.cuh", "snk_internal.cuh"],
+    "k_band_dw": ["snk_band.cu", "snk_device.cuh", "snk_internal.cuh"],
     "k_tc_spmm": ["snk_tc.cu", "snk_internal.cuh"],
     "k_tc_sddmm": ["snk_tc.cu", "snk_internal.cuh"],
 }
