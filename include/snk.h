@@ -41,9 +41,14 @@
  *     captured into a CUDA graph (the inference-latency mode); a replay gives
  *     the same bits as a direct call.  A graph stays valid across
  *     snk_prune_regrow (nnz and the workspace addresses do not change) and
- *     becomes invalid at snk_destroy.  The one exception is the first call
- *     of each product on the large-batch path (below): it allocates that
- *     path's workspace and builds its view, so capture after one such call.
+ *     becomes invalid at snk_destroy.  The exceptions are the first call
+ *     of each product on the large-batch path (below), and the first
+ *     snk_backward_weight at each batch tile of 8, 16, 32 or 64 columns that
+ *     runs on column bands (an X too wide for shared memory, in <= 65536,
+ *     and runs of 40 entries or more on average): each allocates its
+ *     workspace and builds its table, so capture after one such call.  The
+ *     band tables, like the large-batch views, are rebuilt in place by
+ *     snk_prune_regrow.
  *   - Nothing crosses the ABI as an exception; every entry point returns a
  *     status code (snk_status_string gives its text).
  *   - Limits: 1 <= out, in <= 2^31 - 1; 0 <= nnz <= min(out*in, 2^31 - 1);
