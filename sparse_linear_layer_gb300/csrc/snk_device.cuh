@@ -221,13 +221,18 @@ __device__ __forceinline__ void stage_band(float* dst, const float* xt, int r0, 
     }
 }
 
+// Component i (0..3, a runtime value) of a float4, without local memory.
+__device__ __forceinline__ float f4_at(const float4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
 // Stage the operand transposed: dst[i*BP + beta] = src[beta*ld + i] for
 // beta < b, 0 for b <= beta < BP, for i < n.  When the rows of src are
 // 16-byte aligned, groups of 4 columns are read with 128-bit loads (one per
 // source row) and transposed in registers, so each thread issues 4x fewer
 // loads; the remaining columns (and unaligned sources) use 32-bit loads.
 // Several groups are loaded before any is stored, to keep loads in flight.
-template <int BP>
+template <int BP, bool ROT = true>
 __device__ __forceinline__ void stage_transposed(float* dst, const float* __restrict__ src,
                                                  int64_t ld, int b, int64_t n, int tid,
                                                  int nthreads) {
@@ -254,10 +259,21 @@ __device__ __forceinline__ void stage_transposed(float* dst, const float* __rest
                     const int64_t g = g0 + (int64_t)u * nthreads;
                     if (g < groups) {
                         float* d = dst + 4 * g * BP + r0;
-                        *reinterpret_cast<float4*>(d + 0 * BP) = make_float4(t[u][0].x, t[u][1].x, t[u][2].x, t[u][3].x);
-                        *reinterpret_cast<float4*>(d + 1 * BP) = make_float4(t[u][0].y, t[u][1].y, t[u][2].y, t[u][3].y);
-                        *reinterpret_cast<float4*>(d + 2 * BP) = make_float4(t[u][0].z, t[u][1].z, t[u][2].z, t[u][3].z);
-                        *reinterpret_cast<float4*>(d + 3 * BP) = make_float4(t[u][0].w, t[u][1].w, t[u][2].w, t[u][3].w);
+                        // The 4 rows of group g, in an order rotated per
+                        // thread (ROT): the lanes of a quarter-warp
+                        // (consecutive g) then store to different banks
+                        // (BP = 4: 8 distinct 16-byte slots of 128 bytes,
+                        // where the plain order puts 4 lanes on the same
+                        // banks).  The column sweep, which stages a phase
+                        // at a time, measured no gain and keeps the plain
+                        // order.
+                        const int rot = !ROT ? 0 : (BP == 4 ? (int)((g >> 1) & 3) : (int)(g & 3));
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int jj = (q + rot) & 3;
+                            *reinterpret_cast<float4*>(d + jj * BP) =
+                                make_float4(f4_at(t[u][0], jj), f4_at(t[u][1], jj), f4_at(t[u][2], jj), f4_at(t[u][3], jj));
+                        }
                     }
                 }
             }

@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kThreadsDx, 1) k_sweep(const SpmmArgs a) {
         const bool cut = ph + 1 < a.sw_phases;
         const int sp = cut ? __ldg(a.sw_split + (int64_t)((ph + 1) * a.sw_stride - 1) * a.sw_nlane + v0) : -2;
         if (ph > 0) __syncthreads();   // the previous phase's rows are read no more
-        stage_transposed<BP>(xs, a.X + r0, a.n_src, a.b, r1 - r0, threadIdx.x, NT);
+        stage_transposed<BP, false>(xs, a.X + r0, a.n_src, a.b, r1 - r0, threadIdx.x, NT);
         __syncthreads();
         w.prime(a, cut ? (uint32_t)(sp >> 1) + (uint32_t)(sp & 1) : 0xffffffffu);
         w.run(a, xs, r0, r1);
