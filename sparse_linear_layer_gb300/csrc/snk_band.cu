@@ -44,6 +44,7 @@ namespace snk {
 
 struct BandTable {
     bool alloc = false;   // arrays allocated (shapes fixed)
+    bool failed = false;  // allocation failed: this tile keeps the row-order kernel
     bool valid = false;   // built for `version`
     int bp = 0, nb = 0, width = 0, bpb = 0;   // batch tile, bands, columns per band, blocks per band
     int64_t version = -1;
@@ -147,14 +148,17 @@ const BandTable* band_table(Layer* L, int bp, cudaStream_t s, int* status) {
     if (!L->bands) L->bands = new Bands();
     BandTable* t = &L->bands->t[tile_slot(bp)];
     if (t->valid && t->version == L->topology_version) return t;
+    if (t->failed) return nullptr;
     if (!t->alloc) {
         t->bp = bp;
         t->nb = nb;
         t->width = width;
         t->bpb = L->n_blocks / nb;
         if (!b_alloc(&t->run, (int64_t)(nb + 1) * L->out_f) || !b_alloc(&t->cut, t->bpb + 1)) {
+            // the bands are an optimisation: without their table the call
+            // runs the row-order kernel, now and later
             free_table(t);
-            *status = SNK_ERR_OOM;
+            t->failed = true;
             return nullptr;
         }
         t->alloc = true;
