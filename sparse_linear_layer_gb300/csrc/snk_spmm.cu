@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(SpmmShape<GATHER>::kNT, 1) k_spmm(const SpmmAr
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
-    constexpr int D = GATHER ? SNK_PIPE_DX : (BP == 1 ? SNK_PIPE_FWD_NARROW : SNK_PIPE_FWD);
+    constexpr int D = GATHER ? (BP == 16 ? SNK_PIPE_DX16 : SNK_PIPE_DX) : (BP == 1 ? SNK_PIPE_FWD_NARROW : SNK_PIPE_FWD);
     constexpr int NS = D + 1;
     // blocks whose values are gathered ahead of the consumed one (the
     // permutation of a block arrives NS - G blocks before its gather)
