@@ -39,6 +39,10 @@ constexpr int kWarp = 32;
 #ifndef SNK_PIPE_DW_NARROW
 #define SNK_PIPE_DW_NARROW 6   // the same for tiles of 1 or 2 batch columns
 #endif
+#ifndef SNK_PIPE_DW_WIDE
+#define SNK_PIPE_DW_WIDE 2     // the same for tiles of 8+ columns read from the transposed
+                               // copy in global memory (99%, b = 64: 62.5 -> 57.2 us)
+#endif
 // (10000^2, b = 1: forward 19.4 -> 18.9 us at 90%; dW b = 1 / 2 at 90%
 // 22.5 / 23.4 -> 21.3 / 22.6 us, at 95% b = 2 16.4 -> 15.2; the forward at
 // b = 2 and the 99% layer do not gain.)

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sddmm(const SddmmArgs a) {
     using TL = Tile<BP>;
     constexpr int VEC = TL::VEC, LPE = TL::LPE, GPW = TL::GPW;
     constexpr uint32_t BLK = 4 * GPW;
-    constexpr int D = BP <= 2 ? SNK_PIPE_DW_NARROW : SNK_PIPE_DW;
+    constexpr int D = BP <= 2 ? SNK_PIPE_DW_NARROW : ((BP == 4 || SMEM) ? SNK_PIPE_DW : SNK_PIPE_DW_WIDE);
     constexpr int NS = D + 1;
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
