@@ -267,7 +267,9 @@ __device__ __forceinline__ void stage_transposed(float* dst, const float* __rest
                         // banks).  The column sweep, which stages a phase
                         // at a time, measured no gain and keeps the plain
                         // order.
-                        const int rot = !ROT ? 0 : (BP == 4 ? (int)((g >> 1) & 3) : (int)(g & 3));
+                        // (Wider rows keep the plain order: the rotation
+                        // buys little there and its selects cost registers.)
+                        const int rot = !(ROT && BP <= 8) ? 0 : (BP == 4 ? (int)((g >> 1) & 3) : (int)(g & 3));
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int jj = (q + rot) & 3;
