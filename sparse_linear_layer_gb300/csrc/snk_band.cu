@@ -27,8 +27,8 @@
 // (99%, b = 64: 59.8 -> 91.2).  So the bands are taken only when the runs
 // average at least kMinRun entries and a block's entries are at least twice
 // its band's columns.  (The forward on the same runs, its band results added
-// by a second kernel, measured no faster than the row-order kernel at any
-// batch: 90%, b = 8: 50.5 -> 55.7 us; b = 64: 155 -> 178.)
+// by a second kernel, was slower than the row-order kernel at b = 8, 16 and
+// 64 and within 2% at 32: 90%, b = 8: 50.5 -> 55.7 us; b = 64: 155 -> 178.)
 //
 // Table (per batch tile 8, 16, 32, 64; built on first use, rebuilt in place
 // with the topology so captured graphs stay valid):
