@@ -240,42 +240,50 @@ __device__ __forceinline__ void stage_transposed(float* dst, const float* __rest
     if ((((uintptr_t)src) & 15) == 0 && (ld & 3) == 0) n_vec = n & ~(int64_t)3;
     const int64_t groups = n_vec >> 2;
     if constexpr (BP >= 4) {
+        // Items (row group qb of 4 batch rows, column group g), all spread
+        // over the threads at once: with one pass per row group, a 64-row
+        // tile took 16 dependent rounds of loads with only the column groups'
+        // threads busy.
+        constexpr int QB = BP / 4;
         constexpr int U = 2;
-        for (int qb = 0; qb < BP / 4; ++qb) {
-            const int r0 = 4 * qb;
-            for (int64_t g0 = tid; g0 < groups; g0 += (int64_t)nthreads * U) {
-                float4 t[U][4];
+        const int64_t items = groups * QB;
+        for (int64_t i0 = tid; i0 < items; i0 += (int64_t)nthreads * U) {
+            float4 t[U][4];
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t g = g0 + (int64_t)u * nthreads;
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * nthreads;
+                const int qb = (QB == 1 || i >= items) ? 0 : (int)(i / groups);
+                const int64_t g = i - (int64_t)qb * groups;
+                const int r0 = 4 * qb;
 #pragma unroll
-                    for (int rr = 0; rr < 4; ++rr)
-                        t[u][rr] = (g < groups && r0 + rr < b)
-                                       ? __ldg(reinterpret_cast<const float4*>(src + (r0 + rr) * ld) + g)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                for (int rr = 0; rr < 4; ++rr)
+                    t[u][rr] = (i < items && r0 + rr < b)
+                                   ? __ldg(reinterpret_cast<const float4*>(src + (r0 + rr) * ld) + g)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t g = g0 + (int64_t)u * nthreads;
-                    if (g < groups) {
-                        float* d = dst + 4 * g * BP + r0;
-                        // The 4 rows of group g, in an order rotated per
-                        // thread (ROT): the lanes of a quarter-warp
-                        // (consecutive g) then store to different banks
-                        // (BP = 4: 8 distinct 16-byte slots of 128 bytes,
-                        // where the plain order puts 4 lanes on the same
-                        // banks).  The column sweep, which stages a phase
-                        // at a time, measured no gain and keeps the plain
-                        // order.
-                        // (Wider rows keep the plain order: the rotation
-                        // buys little there and its selects cost registers.)
-                        const int rot = !(ROT && BP <= 8) ? 0 : (BP == 4 ? (int)((g >> 1) & 3) : (int)(g & 3));
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * nthreads;
+                if (i < items) {
+                    const int qb = QB == 1 ? 0 : (int)(i / groups);
+                    const int64_t g = i - (int64_t)qb * groups;
+                    float* d = dst + 4 * g * BP + 4 * qb;
+                    // The 4 rows of group g, in an order rotated per
+                    // thread (ROT): the lanes of a quarter-warp
+                    // (consecutive g) then store to different banks
+                    // (BP = 4: 8 distinct 16-byte slots of 128 bytes,
+                    // where the plain order puts 4 lanes on the same
+                    // banks).  The column sweep, which stages a phase
+                    // at a time, measured no gain and keeps the plain
+                    // order.  (Wider rows keep the plain order: the
+                    // rotation buys little there and its selects cost
+                    // registers.)
+                    const int rot = !(ROT && BP <= 8) ? 0 : (BP == 4 ? (int)((g >> 1) & 3) : (int)(g & 3));
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int jj = (q + rot) & 3;
-                            *reinterpret_cast<float4*>(d + jj * BP) =
-                                make_float4(f4_at(t[u][0], jj), f4_at(t[u][1], jj), f4_at(t[u][2], jj), f4_at(t[u][3], jj));
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        const int jj = (q + rot) & 3;
+                        *reinterpret_cast<float4*>(d + jj * BP) =
+                            make_float4(f4_at(t[u][0], jj), f4_at(t[u][1], jj), f4_at(t[u][2], jj), f4_at(t[u][3], jj));
                     }
                 }
             }
