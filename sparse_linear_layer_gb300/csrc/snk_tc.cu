@@ -585,15 +585,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // Y = bias + the slices' partial sums of every shared tile (tiles full ..
-// tiles - 1 in raster order), added in slice order.  One block per shared
-// tile.
+// tiles - 1 in raster order), added in slice order.  Blocks (shared tile,
+// slice of its outputs): every output's loads are in flight at once (one
+// block per tile, looping over its 24,576 outputs, left each thread ~100
+// dependent rounds).
 __global__ void k_tc_split_sum(const float* __restrict__ part, int full, int split, int n_mt, int n_nt,
                                int64_t rows, int64_t n_seg, const float* __restrict__ bias, float* __restrict__ Y) {
     const int tl = blockIdx.x;   // shared tile, counted from `full`
     int mt, nt;
     tc_tile_of(full + tl, n_mt, n_nt, mt, nt);
     const int64_t r0 = (int64_t)mt * kTcM, s0 = (int64_t)nt * kTcN;
-    for (int i = threadIdx.x; i < kTcM * kTcN; i += blockDim.x) {
+    for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < kTcM * kTcN; i += gridDim.y * blockDim.x) {
         const int row = i / kTcN, col = i % kTcN;
         const int64_t rr = r0 + row, sg = s0 + col;
         if (rr >= rows || sg >= n_seg) continue;
@@ -1463,8 +1465,8 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
         }
         k_tc_spmm<<<a.full + (tiles - a.full) * a.split, kTcThreads, kTcSmem, s>>>(mh, ml, a);
         if (a.full < tiles)
-            k_tc_split_sum<<<tiles - a.full, 256, 0, s>>>(T->part, a.full, a.split, a.n_mt, a.n_nt, bc, n_seg, bias,
-                                                          Y + c0 * n_seg);
+            k_tc_split_sum<<<dim3((unsigned)(tiles - a.full), kTcM * kTcN / 256), 256, 0, s>>>(
+                T->part, a.full, a.split, a.n_mt, a.n_nt, bc, n_seg, bias, Y + c0 * n_seg);
         // dense rows of this chunk that the split cannot carry: every output
         // of theirs again, per stored entry
         int st = launch_exact_rows(side, n_seg, Dc, k_len, bias, Y + c0 * n_seg, T->frows,
