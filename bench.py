@@ -314,9 +314,10 @@ def run_reference(args, workload, rank, world):
 # and more at density 1% and above, 128 and more at 5% and above) and the
 # launches that path makes per call: per-call passes plus the product kernels
 # of each batch chunk.
-TC_MIN_BATCH, TC_DENSITY_DIV, TC_CHUNK = 256, 50, 8192
-TC_MIN_BATCH_DENSE, TC_DENSITY_DIV_DENSE = 128, 20
-TC_MIN_BATCH_SPARSE, TC_DENSITY_DIV_SPARSE = 512, 100
+TC_CHUNK = 8192
+# (first batch, density divisor) of the tensor path's tiers: from that many
+# rows at density 1 / divisor and above
+TC_TIERS = ((128, 20), (256, 34), (384, 50), (768, 100))
 TC_SMS, TC_N = 152, 192
 
 
@@ -324,9 +325,7 @@ def tc_path(out_f, in_f, nnz, b):
     mode = os.environ.get("SNK_LARGE_BATCH")
     if nnz == 0 or mode == "off":
         return False
-    return mode == "on" or (b >= TC_MIN_BATCH_DENSE and nnz * TC_DENSITY_DIV_DENSE >= out_f * in_f) or \
-        (b >= TC_MIN_BATCH and nnz * TC_DENSITY_DIV >= out_f * in_f) or \
-        (b >= TC_MIN_BATCH_SPARSE and nnz * TC_DENSITY_DIV_SPARSE >= out_f * in_f)
+    return mode == "on" or any(b >= tb and nnz * div >= out_f * in_f for tb, div in TC_TIERS)
 
 
 def dx_kernel(out_f, in_f, b, num_sms=152):

@@ -1245,16 +1245,15 @@ int build_view(Layer* L, int mode, cudaStream_t s) {
 }
 
 // Which path: SNK_LARGE_BATCH=on|off forces it (tests); otherwise the
-// measured crossover with 64-row batch tiling (10000^2 and 5000^2 layers):
-// from kTcMinBatchDense rows at density 1 / kTcDensityDivDense and above,
-// from kTcMinBatch rows at density 1 / kTcDensityDiv and above, and from
-// kTcMinBatchSparse rows at density 1 / kTcDensityDivSparse and above.
-constexpr int64_t kTcMinBatchDense = 128;
-constexpr int64_t kTcDensityDivDense = 20;
-constexpr int64_t kTcMinBatch = 256;
-constexpr int64_t kTcDensityDiv = 50;
-constexpr int64_t kTcMinBatchSparse = 512;
-constexpr int64_t kTcDensityDivSparse = 100;
+// measured crossover with 64-row batch tiling (10000^2 and 5000^2 layers,
+// forward + dX + dW): from kTcTierBatch[t] rows at density
+// 1 / kTcTierDiv[t] and above, for any tier t.
+//   10% (10000^2): tiled at 64, tensor from 96;  5%: tie at 128, tensor at 192;
+//   3%: tiled at 192, tensor at 256;  2%: tiled at 256, tensor at 384;
+//   1%: tiled to 640, tie at 768, tensor at 1024.
+constexpr int kTcTiers = 4;
+constexpr int64_t kTcTierBatch[kTcTiers] = {128, 256, 384, 768};
+constexpr int64_t kTcTierDiv[kTcTiers] = {20, 34, 50, 100};
 
 }  // namespace
 
@@ -1267,9 +1266,9 @@ bool tc_eligible(const Layer* L, int64_t b) {
     const char* f = getenv("SNK_LARGE_BATCH");
     if (f && strcmp(f, "off") == 0) return false;
     if (f && strcmp(f, "on") == 0) return true;
-    return (b >= kTcMinBatchDense && L->nnz * kTcDensityDivDense >= L->out_f * L->in_f) ||
-           (b >= kTcMinBatch && L->nnz * kTcDensityDiv >= L->out_f * L->in_f) ||
-           (b >= kTcMinBatchSparse && L->nnz * kTcDensityDivSparse >= L->out_f * L->in_f);
+    for (int t = 0; t < kTcTiers; ++t)
+        if (b >= kTcTierBatch[t] && L->nnz * kTcTierDiv[t] >= L->out_f * L->in_f) return true;
+    return false;
 }
 
 void free_tc(Layer* L) {

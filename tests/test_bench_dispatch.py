@@ -2,10 +2,10 @@
 
 bench.py counts the kernel launches of the timed region and picks the
 roofline (HBM for the batch-tiled kernels, tensor for the large-batch path)
-from the same rule the library applies in snk_tc.cu: batches of
-kTcMinBatch rows and more at density 1 / kTcDensityDiv and above, dense
-operands in chunks of kTcChunk rows.  These tests read the constants out of
-the CUDA source, so the two cannot drift apart silently."""
+from the same rule the library applies in snk_tc.cu: from kTcTierBatch[t]
+rows at density 1 / kTcTierDiv[t] and above, dense operands in chunks of
+kTcChunk rows.  These tests read the constants out of the CUDA source, so
+the two cannot drift apart silently."""
 import os
 import re
 
@@ -23,14 +23,16 @@ def _const(name):
     return int(m.group(1))
 
 
+def _array(name):
+    m = re.search(r"constexpr\s+\w+\s+" + name + r"\[\w+\]\s*=\s*\{([^}]*)\}", open(SRC).read())
+    assert m, name
+    return [int(x) for x in m.group(1).split(",")]
+
+
 def test_constants_match_the_library():
-    assert bench.TC_MIN_BATCH == _const("kTcMinBatch")
-    assert bench.TC_DENSITY_DIV == _const("kTcDensityDiv")
     assert bench.TC_CHUNK == _const("kTcChunk")
-    assert bench.TC_MIN_BATCH_DENSE == _const("kTcMinBatchDense")
-    assert bench.TC_DENSITY_DIV_DENSE == _const("kTcDensityDivDense")
-    assert bench.TC_MIN_BATCH_SPARSE == _const("kTcMinBatchSparse")
-    assert bench.TC_DENSITY_DIV_SPARSE == _const("kTcDensityDivSparse")
+    assert [t[0] for t in bench.TC_TIERS] == _array("kTcTierBatch")
+    assert [t[1] for t in bench.TC_TIERS] == _array("kTcTierDiv")
 
 
 def test_rule(monkeypatch):
@@ -39,12 +41,14 @@ def test_rule(monkeypatch):
     assert not bench.tc_path(n, n, 10_000_000, 127)
     assert bench.tc_path(n, n, 10_000_000, 128)          # 10%: from 128 rows
     assert bench.tc_path(n, n, 5_000_000, 128)           # exactly 5%
-    assert not bench.tc_path(n, n, 4_999_999, 255)       # below 5%: from 256 rows
-    assert bench.tc_path(n, n, 4_999_999, 256)
-    assert bench.tc_path(n, n, 2_000_000, 256)           # exactly 2%
-    assert not bench.tc_path(n, n, 1_999_999, 511)       # below 2%: from 512 rows
-    assert bench.tc_path(n, n, 1_999_999, 512)
-    assert bench.tc_path(n, n, 1_000_000, 512)           # exactly 1%
+    assert not bench.tc_path(n, n, 4_999_999, 255)       # below 5%: from 256 rows at 1/34
+    assert bench.tc_path(n, n, 3_000_000, 256)           # 3% (1/34 = 2.94%)
+    assert not bench.tc_path(n, n, 2_941_176, 256)       # just below 1/34
+    assert bench.tc_path(n, n, 2_941_177, 256)
+    assert not bench.tc_path(n, n, 2_000_000, 383)       # 2%: from 384 rows
+    assert bench.tc_path(n, n, 2_000_000, 384)
+    assert not bench.tc_path(n, n, 1_999_999, 767)       # below 2%: from 768 rows
+    assert bench.tc_path(n, n, 1_000_000, 768)           # exactly 1%
     assert bench.tc_path(n, n, 1_000_000, 4096)
     assert not bench.tc_path(n, n, 999_999, 4096)        # below 1%
     assert not bench.tc_path(n, n, 0, 4096)
