@@ -697,9 +697,10 @@ LARGE_BATCHES = [256, 1024, 4096]
 
 
 def measure_large_batch(torch, binding, g, lay, b, dev, flush, reps, tiled_reps):
-    """Device µs of forward, dX and dW at batch b on the tensor-core path (the
-    library's own dispatch) and on 64-row batch tiling (SNK_LARGE_BATCH=off),
-    L2 flushed before every call.  The tensor roofline counts what the path
+    """Device µs of forward, dX and dW at batch b on the tensor-core path
+    (SNK_LARGE_BATCH=on, so that a batch below the layer's tier is measured
+    on that path too) and on 64-row batch tiling (SNK_LARGE_BATCH=off), L2
+    flushed before every call.  The tensor roofline counts what the path
     executes: three fp16 products (hi*hi, hi*lo, lo*hi) of the densified
     tiles, 6 * b * out * in flops per call, against the measured bf16 dense
     peak (kind::f16 runs at the bf16 rate)."""
@@ -732,6 +733,7 @@ def measure_large_batch(torch, binding, g, lay, b, dev, flush, reps, tiled_reps)
 
     saved = os.environ.pop("SNK_LARGE_BATCH", None)
     try:
+        os.environ["SNK_LARGE_BATCH"] = "on"
         tc = {n: timed(f, reps) for n, f in ops.items()}
         tiled = {}
         if tiled_reps:
