@@ -246,7 +246,10 @@ __global__ void k_sw_split(const int4* __restrict__ lane, const int32_t* __restr
 // column's range in the block and not straddling a phase cut are reordered;
 // each such quad belongs to exactly one lane, so the writes do not overlap.
 // The copies the sweep reads (perm, 16-bit rows) are the library's own; the
-// column view returned to callers keeps its order.
+// column view returned to callers keeps its order.  Steps are independent of
+// one another (the counts start afresh at each), so the kSwOrderSteps threads
+// of a quarter take its steps in turn.
+constexpr int kSwOrderSteps = 8;
 __device__ __forceinline__ int sw_cost_add(const unsigned char (&cnt)[4][8], const int (&g)[4], const int (&o)[4]) {
     int c = 0;
 #pragma unroll
@@ -260,7 +263,8 @@ __global__ void k_sw_order(const int4* __restrict__ lane, const int4* __restrict
                            int32_t* __restrict__ perm_o, uint16_t* __restrict__ r16_o) {
     if (err[0]) return;
     const int c = blockIdx.x;
-    const int quarter = threadIdx.x;   // blockDim = kNT / 8
+    const int quarter = threadIdx.x % (kNT / 8);   // blockDim = kNT / 8 * kSwOrderSteps
+    const int step0 = threadIdx.x / (kNT / 8);
     const int4 b = blk[2 * c];
     const int lane0 = b.w + quarter * 8;
     // the 24 orders of a quad
@@ -297,7 +301,7 @@ __global__ void k_sw_order(const int4* __restrict__ lane, const int4* __restrict
                 skip[l] = -1;
             }
         }
-        for (int i = 0;; ++i) {
+        for (int i = step0;; i += kSwOrderSteps) {
             bool any = false;
             unsigned char cnt[4][8];
             for (int j = 0; j < 4; ++j)
@@ -433,8 +437,8 @@ int build_sweep(Layer* L, cudaStream_t s) {
     // the sweep's own streams: the column view, then its quads reordered
     cudaMemcpyAsync(S->perm, L->perm, L->nnz_pad * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
     cudaMemcpyAsync(S->r16, L->rc16, L->nnz_pad * sizeof(uint16_t), cudaMemcpyDeviceToDevice, s);
-    k_sw_order<<<L->n_blocks, kNT / 8, 0, s>>>(S->lane, S->blk, S->split, S->phases, S->cap_lane, S->err, L->perm,
-                                              L->rc16, S->perm, S->r16);
+    k_sw_order<<<L->n_blocks, kNT / 8 * kSwOrderSteps, 0, s>>>(S->lane, S->blk, S->split, S->phases, S->cap_lane,
+                                                               S->err, L->perm, L->rc16, S->perm, S->r16);
     int32_t err = 0;
     if (cudaGetLastError() != cudaSuccess ||
         cudaMemcpyAsync(&err, S->err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
