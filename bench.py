@@ -317,7 +317,7 @@ def run_reference(args, workload, rank, world):
 TC_CHUNK = 8192
 # (first batch, density divisor) of the tensor path's tiers: from that many
 # rows at density 1 / divisor and above
-TC_TIERS = ((128, 20), (256, 34), (384, 50), (768, 100))
+TC_TIERS = ((96, 20), (192, 34), (256, 50), (512, 100))
 TC_SMS, TC_N = 152, 192
 
 

@@ -62,9 +62,9 @@
  *     repeated calls give the same bits.
  *
  * Large batches ([SNACK] appendix Table 13 trains at batch 4096)
- *   - From batch 128 when at least 5% of W is stored, from batch 256 when at
- *     least 1/34 (2.9%) is, from batch 384 when at least 2% is, and from
- *     batch 768 when at least 1% is, the three product calls run on the
+ *   - From batch 96 when at least 5% of W is stored, from batch 192 when at
+ *     least 1/34 (2.9%) is, from batch 256 when at least 2% is, and from
+ *     batch 512 when at least 1% is, the three product calls run on the
  *     tensor cores instead of 64-row batch tiling.  W is
  *     densified tile by tile in shared memory (never in device memory) and
  *     multiplied with the dense operand.  The environment variable

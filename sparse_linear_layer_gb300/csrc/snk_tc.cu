@@ -51,7 +51,8 @@ namespace snk {
 struct TcView {
     int32_t* perm_t = nullptr;    // [nnz] canonical slot of the j-th entry in tile order
     uint16_t* off = nullptr;      // [nnz + pad] byte offset of the entry in its swizzled fp16 tile
-    int32_t* tile_ptr = nullptr;  // [n_tiles + 1] first entry of each (segment tile, window)
+    int32_t* tile_ptr = nullptr;  // [n_tiles + 1] first entry of each (segment tile, window);
+                                  // weight gradient: [n_tiles * kWGroups + 1], of each (block, group)
     int64_t n_tiles = 0;
     int n_win = 0;                // windows along the reduction dimension
     int n_nt = 0;                 // segment tiles
@@ -148,7 +149,6 @@ static_assert(kTcSmem <= 227 * 1024 - 4096, "pipeline stages exceed shared memor
 static_assert(kTcN % 64 == 0 && kTcN <= 256, "two builder halves of whole 32-column loads");
 static_assert(kRecCap % 8 == 0, "staged ranges are whole 16-byte units");
 constexpr int kTcPad = 16;         // entries readable past nnz in the tile-order arrays
-constexpr int kWStride = kTcN + 1; // row stride (floats) of the weight-gradient sums tile: no bank conflicts
 // An fp16 piece of a sparse tile holds kTcN * kTcK / 64 = 192 words per bank,
 // so fewer than kRankSpan entries of one window share a bank.
 constexpr uint32_t kRankSpan = 512;
@@ -716,30 +716,46 @@ __global__ void k_tc_split(const float* __restrict__ D, int64_t len, int64_t ks,
 
 // ------------------------------------------------------------ weight gradient
 // dW_k = sum_b dY[b, r_k] X[b, c_k] on the tensor cores: the dense product
-// dY^T X over one batch chunk for a 128-row x 192-column block of W, kept
-// only at the block's entries.  A = dY^T (rows of W, batch contiguous) and
+// dY^T X over one batch chunk for 128-row x 192-column blocks of W, kept
+// only at each block's entries.  A = dY^T (rows of W, batch contiguous) and
 // B = X^T (columns of W), both scaled per row and split into fp16 hi / lo by
 // k_tc_tsplit, arrive by TMA; the accumulators take turns and are drained
-// into registers as in k_tc_spmm; the block's sums then go through shared
-// memory to the entries listed by the weight-gradient view.
+// into registers as in k_tc_spmm.
+//
+// The CTAs are persistent, one per SM: CTA c takes the blocks c, c + grid,
+// c + 2 grid, ... in raster order, and counts its windows, accumulator turns
+// and barrier phases across them, so the loads and MMAs of its next block
+// run while the builders drain and write out the last one.  The write-out
+// needs no block-wide step: builder warp (quarter q, half h) owns the block's
+// rows 32q..32q+31 (its TMEM lanes) and columns 96h..96h+95, and writes its
+// sums one 32 x 32 chunk at a time into its own shared-memory scratch, from
+// which its lanes send the chunk's entries to their canonical slots.  The
+// weight-gradient view lists every block's entries grouped by (quarter,
+// chunk) for this.
 struct TcwArgs {
-    int n_win;                // batch windows in this chunk
-    int n_ot, n_it;           // row blocks (of kTcM) and column blocks (of kTcN) of W
+    int n_win;                 // batch windows in this chunk
+    int n_ot, n_it;            // row blocks (of kTcM) and column blocks (of kTcN) of W
     int64_t out_f, in_f;
-    const int32_t* e_row;     // [out] scale exponents of dY^T rows
-    const int32_t* e_col;     // [in] scale exponents of X^T rows
-    const int32_t* perm;      // weight-gradient view: canonical slot per entry
-    const uint16_t* off;      // offset in the block's fp32 tile
-    const int32_t* tile_ptr;  // [n_ot * n_it + 1]
+    const int32_t* e_row;      // [out] scale exponents of dY^T rows
+    const int32_t* e_col;      // [in] scale exponents of X^T rows
+    const int32_t* perm;       // weight-gradient view: canonical slot per entry
+    const uint16_t* off;       // row within the quarter * 32 + column within the chunk
+    const int32_t* group_ptr;  // [n_ot * n_it * kWGroups + 1] first entry of each (block, group)
     float* dW;
-    int accumulate;           // add to dW (later batch chunks) instead of writing it
+    int accumulate;            // add to dW (later batch chunks) instead of writing it
     int32_t* status;
 };
 
 constexpr int kWThreads = kTcBuilders + 64;       // 8 drain warps, a TMA warp, an MMA warp
 constexpr int kWStage = kStageA + kStageB;        // one batch window of A and B
-constexpr int kWSmem = 2 * kWStage + 1024;
-static_assert(kTcM * kWStride * 4 <= 2 * kWStage, "the sums tile reuses the pipeline stages");
+constexpr int kWChunks = kTcN / 32;               // 32-column chunks per block
+constexpr int kWGroups = 32;                      // group slots per block: quarter * kWChunks + chunk
+constexpr int kWScratch = 32 * 33;                // floats per builder warp: one chunk, rows padded
+constexpr int kWUnroll = 4;                       // entries per lane whose loads are in flight together
+constexpr int kWSmem = 2 * kWStage + (kTcBuilders / 32) * kWScratch * 4 + 1024;
+static_assert((kTcM / 32) * kWChunks <= kWGroups, "quarters and chunks fit the group slots");
+static_assert(kColsPerThread == 3 * 32, "each builder warp owns three chunks");
+static_assert(kWSmem <= 227 * 1024 - 4096, "stages and scratch exceed shared memory");
 
 __global__ void __launch_bounds__(kWThreads, 1)
     k_tc_sddmm(const __grid_constant__ CUtensorMap map_ah, const __grid_constant__ CUtensorMap map_al,
@@ -750,17 +766,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __shared__ uint64_t full[2], empty[2], accf[2], acce[2], fin;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float ipw_row[kTcM], ipw_col[kTcN];
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int id = blockIdx.x;
-    const int gsz = kTcGroupM * a.n_it;
-    const int first_m = (id / gsz) * kTcGroupM;
-    const int gm = min(a.n_ot - first_m, kTcGroupM);
-    const int ot = first_m + (id % gsz) % gm;
-    const int it = (id % gsz) / gm;
-    const int64_t o0 = (int64_t)ot * kTcM, i0 = (int64_t)it * kTcN;
     const int n_win = a.n_win;
+    const int n_per = (n_win + kTcPeriod - 1) / kTcPeriod;
+    const int tiles = a.n_ot * a.n_it;
+    const int grid = (int)gridDim.x, first = (int)blockIdx.x;
+    const int mine = (tiles - first + grid - 1) / grid;   // blocks of this CTA (grid <= tiles)
 
     if (t == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -780,58 +792,64 @@ __global__ void __launch_bounds__(kWThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (t < kTcM) ipw_row[t] = ldexpf(1.f, o0 + t < a.out_f ? -a.e_row[o0 + t] : 0);
-    if (t < kTcN) ipw_col[t] = ldexpf(1.f, i0 + t < a.in_f ? -a.e_col[i0 + t] : 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
     bool ok = true;
-    const int n_per = (n_win + kTcPeriod - 1) / kTcPeriod;
 
     if (warp == kTmaWarp) {
         if (lane == 0) {
-            int w = 0;
-            for (; w < n_win; ++w) {
-                const int s = w & 1;
-                if (w >= 2 && !mbar_wait(&empty[s], ((w >> 1) - 1) & 1)) {
-                    ok = false;
-                    break;
+            int gw = 0;   // windows issued by this CTA, over all its blocks
+            for (int i = 0; i < mine && ok; ++i) {
+                int ot, it;
+                tc_tile_of(first + i * grid, a.n_ot, a.n_it, ot, it);
+                const int y0 = ot * kTcM, x0 = it * kTcN;
+                for (int w = 0; w < n_win; ++w, ++gw) {
+                    const int s = gw & 1;
+                    if (gw >= 2 && !mbar_wait(&empty[s], ((gw >> 1) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* st = sm + s * kWStage;
+                    mbar_expect_tx(&full[s], kWStage);
+                    tma_load_2d(st, &map_ah, w * kTcK, y0, &full[s]);
+                    tma_load_2d(st + kPieceA, &map_al, w * kTcK, y0, &full[s]);
+                    tma_load_2d(st + kStageA, &map_bh, w * kTcK, x0, &full[s]);
+                    tma_load_2d(st + kStageA + kPieceB, &map_bl, w * kTcK, x0, &full[s]);
                 }
-                unsigned char* st = sm + s * kWStage;
-                mbar_expect_tx(&full[s], kWStage);
-                tma_load_2d(st, &map_ah, w * kTcK, (int)o0, &full[s]);
-                tma_load_2d(st + kPieceA, &map_al, w * kTcK, (int)o0, &full[s]);
-                tma_load_2d(st + kStageA, &map_bh, w * kTcK, (int)i0, &full[s]);
-                tma_load_2d(st + kStageA + kPieceB, &map_bl, w * kTcK, (int)i0, &full[s]);
             }
-            if (!ok) drain_ring(full, 2, w);
+            if (!ok) drain_ring(full, 2, gw);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            for (int w = 0; w < n_win; ++w) {
-                const int s = w & 1;
-                const int q = w / kTcPeriod, ab = q & 1;
-                const bool first = (w % kTcPeriod) == 0;
-                if (!mbar_wait(&full[s], (w >> 1) & 1) ||
-                    (first && q >= 2 && !mbar_wait(&acce[ab], ((q >> 1) - 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ah = smem_u32(sm + s * kWStage), al = ah + kPieceA;
-                const uint32_t bh = ah + kStageA, bl = bh + kPieceB;
-                const uint32_t d = tmem + ab * kAccStride;
+            const int total = mine * n_win;
+            int gw = 0;
+            for (int i = 0; i < mine && ok; ++i) {
+                for (int w = 0; w < n_win; ++w, ++gw) {
+                    const int s = gw & 1;
+                    const int q = i * n_per + w / kTcPeriod, ab = q & 1;   // accumulator turn
+                    const bool turn0 = (w % kTcPeriod) == 0;
+                    if (!mbar_wait(&full[s], (gw >> 1) & 1) ||
+                        (turn0 && q >= 2 && !mbar_wait(&acce[ab], ((q >> 1) - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ah = smem_u32(sm + s * kWStage), al = ah + kPieceA;
+                    const uint32_t bh = ah + kStageA, bl = bh + kPieceB;
+                    const uint32_t d = tmem + ab * kAccStride;
 #pragma unroll
-                for (int kk = 0; kk < kTcK / 16; ++kk) {
-                    const uint32_t o = 32 * kk;
-                    mma_f16(d, desc_sw128(ah + o), desc_sw128(bh + o), (first && kk == 0) ? 0u : 1u);
-                    mma_f16(d, desc_sw128(ah + o), desc_sw128(bl + o), 1u);
-                    mma_f16(d, desc_sw128(al + o), desc_sw128(bh + o), 1u);
+                    for (int kk = 0; kk < kTcK / 16; ++kk) {
+                        const uint32_t o = 32 * kk;
+                        mma_f16(d, desc_sw128(ah + o), desc_sw128(bh + o), (turn0 && kk == 0) ? 0u : 1u);
+                        mma_f16(d, desc_sw128(ah + o), desc_sw128(bl + o), 1u);
+                        mma_f16(d, desc_sw128(al + o), desc_sw128(bh + o), 1u);
+                    }
+                    if (gw + 2 < total) mma_commit(&empty[s]);
+                    if ((w % kTcPeriod) == kTcPeriod - 1 || w == n_win - 1) mma_commit(&accf[ab]);
                 }
-                if (w + 2 < n_win) mma_commit(&empty[s]);
-                if ((w % kTcPeriod) == kTcPeriod - 1 || w == n_win - 1) mma_commit(&accf[ab]);
             }
             mma_commit(&fin);
             if (!mbar_wait(&fin, 0, kTcDrainCycles)) ok = false;
@@ -839,55 +857,104 @@ __global__ void __launch_bounds__(kWThreads, 1)
         __syncwarp();
     } else {
         const int lq = warp & 3, half = warp >> 2;
-        float acc[kColsPerThread];
+        const int row = 32 * lq + lane;
+        float* scr = reinterpret_cast<float*>(sm + 2 * kWStage) + warp * kWScratch;
+        // false once one of this warp's waits has run out (the same in every
+        // lane): from then on its entries get NaN, so none is left stale
+        bool wok = true;
+        for (int i = 0; i < mine; ++i) {
+            int ot, it;
+            tc_tile_of(first + i * grid, a.n_ot, a.n_it, ot, it);
+            const int64_t o0 = (int64_t)ot * kTcM, i0 = (int64_t)it * kTcN;
+            // the block's scales and entry ranges, loaded before the wait
+            const float ir = ldexpf(1.f, o0 + row < a.out_f ? -a.e_row[o0 + row] : 0);
+            float ic[3];
 #pragma unroll
-        for (int j = 0; j < kColsPerThread; ++j) acc[j] = 0.f;
-        for (int q = 0; q < n_per && ok; ++q) {
-            const int ab = q & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&accf[ab], (q >> 1) & 1))) {
-                ok = false;
-                break;
+            for (int cc = 0; cc < 3; ++cc) {
+                const int64_t col = i0 + 32 * (3 * half + cc) + lane;
+                ic[cc] = ldexpf(1.f, col < a.in_f ? -a.e_col[col] : 0);
             }
-            tc_fence_after();
-            const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + ab * kAccStride + kColsPerThread * half;
+            const int32_t* gp =
+                a.group_ptr + ((int64_t)ot * a.n_it + it) * kWGroups + lq * kWChunks + 3 * half;
+            int jr[4];
 #pragma unroll
-            for (int c = 0; c < kColsPerThread / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(ta + 32 * c, r);
+            for (int k = 0; k < 4; ++k) jr[k] = gp[k];
+            // kWUnroll entries per lane at a time, their loads issued together;
+            // the first batch of each chunk is loaded one step early (the first
+            // chunk's before the drain)
+            auto load = [&](int jb, int j1, int (&o)[kWUnroll], int (&pm)[kWUnroll]) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[32 * c + i] += __uint_as_float(r[i]);
+                for (int u = 0; u < kWUnroll; ++u) {
+                    const int j = jb + 32 * u + lane;
+                    o[u] = j < j1 ? (int)__ldg(a.off + j) : 0;
+                    pm[u] = j < j1 ? __ldg(a.perm + j) : 0;
+                }
+            };
+            auto send = [&](int jb, int j1, float cscale, const int (&o)[kWUnroll], const int (&pm)[kWUnroll]) {
+#pragma unroll
+                for (int u = 0; u < kWUnroll; ++u) {
+                    const float cs = __shfl_sync(0xffffffffu, cscale, o[u] & 31);
+                    if (jb + 32 * u + lane < j1) {
+                        float* dst = a.dW + pm[u];
+                        if (!wok) {
+                            *dst = __int_as_float(0x7fc00000);
+                        } else {
+                            const float v = scr[o[u] + (o[u] >> 5)] * cs;
+                            *dst = a.accumulate ? *dst + v : v;
+                        }
+                    }
+                }
+            };
+            int o_cur[kWUnroll], p_cur[kWUnroll];
+            load(jr[0], jr[1], o_cur, p_cur);
+            float acc[kColsPerThread];
+#pragma unroll
+            for (int j = 0; j < kColsPerThread; ++j) acc[j] = 0.f;
+            for (int ql = 0; ql < n_per && wok; ++ql) {
+                const int q = i * n_per + ql, ab = q & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&accf[ab], (q >> 1) & 1))) {
+                    wok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ta =
+                    tmem + ((uint32_t)(32 * lq) << 16) + ab * kAccStride + kColsPerThread * half;
+#pragma unroll
+                for (int c = 0; c < kColsPerThread / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(ta + 32 * c, r);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[32 * c + k] += __uint_as_float(r[k]);
+                }
+                tc_fence_before();
+                mbar_arrive(&acce[ab]);
             }
-            tc_fence_before();
-            mbar_arrive(&acce[ab]);
+#pragma unroll
+            for (int cc = 0; cc < 3; ++cc) {
+                if (wok) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) scr[lane * 33 + k] = acc[32 * cc + k] * ir;
+                }
+                __syncwarp();
+                int o_nxt[kWUnroll], p_nxt[kWUnroll];
+                if (cc < 2) load(jr[cc + 1], jr[cc + 2], o_nxt, p_nxt);
+                const int j1 = jr[cc + 1];
+                send(jr[cc], j1, ic[cc], o_cur, p_cur);
+                for (int jb = jr[cc] + 32 * kWUnroll; jb < j1; jb += 32 * kWUnroll) {
+                    load(jb, j1, o_cur, p_cur);
+                    send(jb, j1, ic[cc], o_cur, p_cur);
+                }
+                __syncwarp();
+                if (cc < 2) {
+#pragma unroll
+                    for (int u = 0; u < kWUnroll; ++u) {
+                        o_cur[u] = o_nxt[u];
+                        p_cur[u] = p_nxt[u];
+                    }
+                }
+            }
         }
-        // every MMA has completed (all turns drained): the stages hold the
-        // sums tile.  After an early stop the block's entries get NaN instead,
-        // so no stale gradient is left behind.
-        const bool stopped = builders_any(!ok);
-        float* tile = reinterpret_cast<float*>(sm);
-        if (!stopped) {
-            const int row = 32 * lq + lane;
-            const float ir = ipw_row[row];
-#pragma unroll
-            for (int j = 0; j < kColsPerThread; ++j) {
-                const int col = kColsPerThread * half + j;
-                tile[row * kWStride + col] = (acc[j] * ir) * ipw_col[col];
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kTcBuilders) : "memory");
-        } else {
-            ok = false;
-        }
-        const int32_t* tp = a.tile_ptr + (int64_t)ot * a.n_it + it;
-        const int j1 = tp[1];
-        for (int j = tp[0] + t; j < j1; j += kTcBuilders) {
-            float* dst = a.dW + a.perm[j];
-            if (stopped) {
-                *dst = __int_as_float(0x7fc00000);
-            } else {
-                const float v = tile[a.off[j]];
-                *dst = a.accumulate ? *dst + v : v;
-            }
-        }
+        ok = wok;
     }
     if (!ok) atomicExch(&abort_flag, 1);
     tc_fence_before();
@@ -1091,17 +1158,20 @@ __global__ void k_tc_values(const float* __restrict__ v, const int32_t* __restri
 // ------------------------------------------------------------ view build
 // Tile shapes of the three views: mode 0 tiles W's rows (kTcN segments x
 // kTcK reduction indices, offsets in the swizzled fp16 tile), mode 1 its
-// columns the same way, mode 2 blocks of kTcM rows x kTcN columns (offsets
-// in the fp32 accumulator tile, row stride kWStride).
+// columns the same way, mode 2 blocks of kTcM rows x kTcN columns, each
+// cut into (32-row quarter, 32-column chunk) groups (key: block * kWGroups +
+// group; offset: row * 32 + column within the group).
 struct TileOf {
     int mode, n_inner;   // tiles along the second coordinate
     __device__ __forceinline__ uint32_t key(int32_t r, int32_t c) const {
-        if (mode == 2) return (uint32_t)(r / kTcM) * (uint32_t)n_inner + (uint32_t)(c / kTcN);
+        if (mode == 2)
+            return ((uint32_t)(r / kTcM) * (uint32_t)n_inner + (uint32_t)(c / kTcN)) * kWGroups +
+                   (uint32_t)((r % kTcM) / 32 * kWChunks + (c % kTcN) / 32);
         const int32_t sg = mode ? c : r, kk = mode ? r : c;
         return (uint32_t)(sg / kTcN) * (uint32_t)n_inner + (uint32_t)(kk / kTcK);
     }
     __device__ __forceinline__ uint16_t off(int32_t r, int32_t c) const {
-        if (mode == 2) return (uint16_t)((r % kTcM) * kWStride + c % kTcN);
+        if (mode == 2) return (uint16_t)((r & 31) * 32 + (c % kTcN) % 32);
         const int32_t sg = mode ? c : r, kk = mode ? r : c;
         return (uint16_t)sw128(sg % kTcN, kk % kTcK);
     }
@@ -1186,24 +1256,34 @@ void tc_shape(const Layer* L, bool columns, int64_t* n_seg, int64_t* k_len) {
 int build_view(Layer* L, int mode, cudaStream_t s) {
     TcView& V = L->tc->view[mode];
     const int64_t n = L->nnz;
+    if (mode == 2) {
+        V.n_win = (int)ceil_div(L->in_f, kTcN);    // column blocks
+        V.n_nt = (int)ceil_div(L->out_f, kTcM);    // row blocks
+    } else {
+        int64_t n_seg, k_len;
+        tc_shape(L, mode == 1, &n_seg, &k_len);
+        V.n_win = (int)ceil_div(k_len, kTcK);
+        V.n_nt = (int)ceil_div(n_seg, kTcN);
+    }
+    V.n_tiles = (int64_t)V.n_win * V.n_nt;
+    // sort keys: tiles, or (block, group) pairs for the weight gradient
+    const int64_t n_keys = mode == 2 ? V.n_tiles * kWGroups : V.n_tiles;
     if (!V.perm_t) {
-        if (mode == 2) {
-            V.n_win = (int)ceil_div(L->in_f, kTcN);    // column blocks
-            V.n_nt = (int)ceil_div(L->out_f, kTcM);    // row blocks
-        } else {
-            int64_t n_seg, k_len;
-            tc_shape(L, mode == 1, &n_seg, &k_len);
-            V.n_win = (int)ceil_div(k_len, kTcK);
-            V.n_nt = (int)ceil_div(n_seg, kTcN);
-        }
-        V.n_tiles = (int64_t)V.n_win * V.n_nt;
-        if (!tc_alloc(&V.perm_t, n) || !tc_alloc(&V.off, n + kTcPad) || !tc_alloc(&V.tile_ptr, V.n_tiles + 1))
+        if (!tc_alloc(&V.perm_t, n) || !tc_alloc(&V.off, n + kTcPad) || !tc_alloc(&V.tile_ptr, n_keys + 1)) {
+            // all or nothing: a later call starts over
+            void* ptrs[] = {V.perm_t, V.off, V.tile_ptr};
+            for (void* p : ptrs)
+                if (p) cudaFree(p);
+            V.perm_t = nullptr;
+            V.off = nullptr;
+            V.tile_ptr = nullptr;
             return SNK_ERR_OOM;
+        }
     }
     const TileOf tile{mode, V.n_win};
     const int T = 256;
     const int G = grid_for(n, T, L->num_sms);
-    const int tile_bits = bits_of((uint64_t)V.n_tiles);
+    const int tile_bits = bits_of((uint64_t)n_keys);
     // the sparse-tile views also spread each window's entries over the banks
     // when the (tile, rank, bank) key fits 32 bits
     const bool by_bank = mode != 2 && tile_bits + 14 <= 32;
@@ -1239,7 +1319,7 @@ int build_view(Layer* L, int mode, cudaStream_t s) {
         }
         shift = 14;
     }
-    k_tc_finish<<<grid_for(n + 1, T, L->num_sms), T, 0, s>>>(kk, vv, n, V.n_tiles, shift, L->r, L->c, tile,
+    k_tc_finish<<<grid_for(n + 1, T, L->num_sms), T, 0, s>>>(kk, vv, n, n_keys, shift, L->r, L->c, tile,
                                                              V.perm_t, V.off, V.tile_ptr);
     return cudaGetLastError() == cudaSuccess ? SNK_OK : SNK_ERR_CUDA;
 }
@@ -1248,11 +1328,12 @@ int build_view(Layer* L, int mode, cudaStream_t s) {
 // measured crossover with 64-row batch tiling (10000^2 and 5000^2 layers,
 // forward + dX + dW): from kTcTierBatch[t] rows at density
 // 1 / kTcTierDiv[t] and above, for any tier t.
-//   10% (10000^2): tiled at 64, tensor from 96;  5%: tie at 128, tensor at 192;
-//   3%: tiled at 192, tensor at 256;  2%: tiled at 256, tensor at 384;
-//   1%: tiled to 640, tie at 768, tensor at 1024.
+//   10% (10000^2 and 5000^2): tiled at 64, tensor from 96;  5%: tiled at 64,
+//   tensor from 96 (3% ahead there);  3%: tiled at 128, tensor at 192;
+//   2%: tiled at 192, tensor at 256;  1%: tiled to 384, tie at 512,
+//   tensor at 640.
 constexpr int kTcTiers = 4;
-constexpr int64_t kTcTierBatch[kTcTiers] = {128, 256, 384, 768};
+constexpr int64_t kTcTierBatch[kTcTiers] = {96, 192, 256, 512};
 constexpr int64_t kTcTierDiv[kTcTiers] = {20, 34, 50, 100};
 
 }  // namespace
@@ -1263,6 +1344,8 @@ bool tc_eligible(const Layer* L, int64_t b) {
                             ceil_div(L->in_f, kTcN) * ceil_div(L->out_f, kTcK) +
                             ceil_div(L->out_f, kTcM) * ceil_div(L->in_f, kTcN);
     if (n_tiles > INT32_MAX / 2) return false;
+    // the weight-gradient view's (block, group) keys
+    if (ceil_div(L->out_f, kTcM) * ceil_div(L->in_f, kTcN) * kWGroups > INT32_MAX) return false;
     const char* f = getenv("SNK_LARGE_BATCH");
     if (f && strcmp(f, "off") == 0) return false;
     if (f && strcmp(f, "on") == 0) return true;
@@ -1539,11 +1622,13 @@ int run_tc_sddmm(Layer* L, const float* X, const float* dY, int64_t b, float* dW
         a.e_col = T->col_exp;
         a.perm = V.perm_t;
         a.off = V.off;
-        a.tile_ptr = V.tile_ptr;
+        a.group_ptr = V.tile_ptr;
         a.dW = dW;
         a.accumulate = acc;
         a.status = L->status;
-        k_tc_sddmm<<<a.n_ot * a.n_it, kWThreads, kWSmem, s>>>(mah, mal, mbh, mbl, a);
+        // persistent: one CTA per SM, each taking every grid-th block
+        const int grid = (int)std::min<int64_t>((int64_t)a.n_ot * a.n_it, L->num_sms);
+        k_tc_sddmm<<<grid, kWThreads, kWSmem, s>>>(mah, mal, mbh, mbl, a);
     }
     if (cudaGetLastError() != cudaSuccess) return SNK_ERR_CUDA;
     // rows and columns of W flagged by any chunk: their entries again, over the whole batch

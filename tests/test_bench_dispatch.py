@@ -38,17 +38,17 @@ def test_constants_match_the_library():
 def test_rule(monkeypatch):
     monkeypatch.delenv("SNK_LARGE_BATCH", raising=False)
     n = 10_000
-    assert not bench.tc_path(n, n, 10_000_000, 127)
-    assert bench.tc_path(n, n, 10_000_000, 128)          # 10%: from 128 rows
-    assert bench.tc_path(n, n, 5_000_000, 128)           # exactly 5%
-    assert not bench.tc_path(n, n, 4_999_999, 255)       # below 5%: from 256 rows at 1/34
-    assert bench.tc_path(n, n, 3_000_000, 256)           # 3% (1/34 = 2.94%)
-    assert not bench.tc_path(n, n, 2_941_176, 256)       # just below 1/34
-    assert bench.tc_path(n, n, 2_941_177, 256)
-    assert not bench.tc_path(n, n, 2_000_000, 383)       # 2%: from 384 rows
-    assert bench.tc_path(n, n, 2_000_000, 384)
-    assert not bench.tc_path(n, n, 1_999_999, 767)       # below 2%: from 768 rows
-    assert bench.tc_path(n, n, 1_000_000, 768)           # exactly 1%
+    assert not bench.tc_path(n, n, 10_000_000, 95)
+    assert bench.tc_path(n, n, 10_000_000, 96)           # 10%: from 96 rows
+    assert bench.tc_path(n, n, 5_000_000, 96)            # exactly 5%
+    assert not bench.tc_path(n, n, 4_999_999, 191)       # below 5%: from 192 rows at 1/34
+    assert bench.tc_path(n, n, 3_000_000, 192)           # 3% (1/34 = 2.94%)
+    assert not bench.tc_path(n, n, 2_941_176, 192)       # just below 1/34
+    assert bench.tc_path(n, n, 2_941_177, 192)
+    assert not bench.tc_path(n, n, 2_000_000, 255)       # 2%: from 256 rows
+    assert bench.tc_path(n, n, 2_000_000, 256)
+    assert not bench.tc_path(n, n, 1_999_999, 511)       # below 2%: from 512 rows
+    assert bench.tc_path(n, n, 1_000_000, 512)           # exactly 1%
     assert bench.tc_path(n, n, 1_000_000, 4096)
     assert not bench.tc_path(n, n, 999_999, 4096)        # below 1%
     assert not bench.tc_path(n, n, 0, 4096)

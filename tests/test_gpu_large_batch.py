@@ -107,6 +107,31 @@ def test_default_dispatch_weight_gradient(torch, monkeypatch):
     g.close()
 
 
+@pytest.mark.parametrize("b", [1300, 4300])
+def test_weight_gradient_blocks_per_cta(torch, monkeypatch, b):
+    """dW and db at 3000 x 2900, 90%: 24 x 16 = 384 blocks of W, two or
+    three per CTA of the persistent kernel.  b = 1300 gives 21 batch windows
+    (the last one ragged), so three accumulator turns per block and an odd
+    number of turns per CTA; b = 4300 runs two batch chunks (4160 + 140
+    rows), the second adding to the first.  A repeat call gives the same
+    bits."""
+    monkeypatch.delenv("SNK_LARGE_BATCH", raising=False)
+    lay = synth.make_layer(3000, 2900, 90, 0.02, 151, 152)
+    X = synth.normal((b, 2900), 1.0, 153)
+    dY = synth.normal((b, 3000), 1.0, 154)
+    g = make_gpu_layer(torch, lay)
+    can = oracle.canonicalize(lay.out_f, lay.in_f, lay.values, lay.rows, lay.cols)
+    Xd, dYd = dev(X, torch), dev(dY, torch)
+    dW, db = g.backward_weight(Xd, dYd, with_bias=True)
+    dW2, _ = g.backward_weight(Xd, dYd, with_bias=True)
+    torch.cuda.synchronize()
+    assert torch.equal(dW, dW2), "repeat call differs"
+    dWr, Aw, dbr, Ab = oracle.backward_weight(3000, 2900, can["rows"], can["cols"], X, dY)
+    assert_within(host(dW), dWr, Aw, "backward_weight")
+    assert_within(host(db), dbr, Ab, "bias grad")
+    g.close()
+
+
 @pytest.mark.parametrize("out_f,in_f", [(300, 10_000), (10_000, 300)])
 def test_all_positive_long_reduction(torch, monkeypatch, out_f, in_f):
     """Sign-coherent sums over 10000 terms: every rounding error of a
