@@ -341,9 +341,10 @@ def dx_kernel(out_f, in_f, b, num_sms=152):
 def tc_launches(op, out_f, in_f, b):
     """Kernels per call on the tensor-core path: per batch chunk the column
     passes, the flag decision, the transposes and the product, plus the exact
-    recomputation of flagged entries (dW); the segment and value passes, per
-    chunk the split, the product and the exact recomputation of flagged rows,
-    plus that of flagged segments (forward, dX)."""
+    recomputation of flagged entries (dW); the segment scale pass, the value
+    pass and the candidate list, per chunk the split, the product and the
+    exact recomputation of flagged rows, plus that of flagged segments
+    (forward, dX)."""
     if op == "dw":
         k_stride = (max(out_f, in_f) + 7) // 8 * 8
         chunk = max(64, (TC_CHUNK * k_stride) // (out_f + in_f) // 64 * 64)
@@ -351,7 +352,7 @@ def tc_launches(op, out_f, in_f, b):
     n_seg = in_f if op == "dx" else out_f
     n_win = ((out_f if op == "dx" else in_f) + 63) // 64
     n_nt = (n_seg + TC_N - 1) // TC_N
-    n = 3
+    n = 4
     for c0 in range(0, b, TC_CHUNK):
         n_mt = (min(TC_CHUNK, b - c0) + 127) // 128
         n += 4 if tc_shares_tiles(n_mt * n_nt, n_win) else 3   # split pass, product, (partial sum), exact rows

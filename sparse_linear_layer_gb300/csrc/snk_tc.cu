@@ -1088,14 +1088,13 @@ __global__ void k_tc_tsplit(const float* __restrict__ D, int64_t rows, int64_t n
 
 // ------------------------------------------------------------ per-call passes
 // Per segment of W (a row, or a column through perm): the scale exponent of
-// its largest finite magnitude and its code (tc_needs_exact: an inf or NaN,
-// and the count of nonzero values below 2^-3 after scaling); segments with a
-// nonzero code become candidates for the exact recomputation.  Also the
-// largest sum of finite magnitudes over the segments and the largest
+// its largest finite magnitude, and bit 0 of its code (tc_needs_exact: it
+// holds an inf or NaN); k_tc_values adds the count of its tiny values.  Also
+// the largest sum of finite magnitudes over the segments and the largest
 // magnitude, which the dense rows' own check uses.
 __global__ void k_tc_seg_exp(const int32_t* __restrict__ ptr, const float* __restrict__ v,
                              const int32_t* __restrict__ perm, int64_t n_seg, int32_t* __restrict__ e,
-                             int32_t* __restrict__ code, int32_t* __restrict__ cand, uint32_t* __restrict__ fix) {
+                             int32_t* __restrict__ code, uint32_t* __restrict__ fix) {
     const int lane = threadIdx.x & 31;
     for (int64_t sg = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; sg < n_seg;
          sg += ((int64_t)gridDim.x * blockDim.x) >> 5) {
@@ -1117,40 +1116,43 @@ __global__ void k_tc_seg_exp(const int32_t* __restrict__ ptr, const float* __res
             sum += __shfl_xor_sync(0xffffffffu, sum, o);
         }
         nf = __any_sync(0xffffffffu, nf);
-        const int ex = tc_exponent(m);
-        const float tiny = ldexpf(0.125f, -ex);
-        int n_tiny = 0;
-        for (int k = k0 + lane; k < k1; k += 32) {
-            const float x = fabsf(perm ? v[perm[k]] : v[k]);
-            n_tiny += (x > 0.f && x < tiny) ? 1 : 0;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) n_tiny += __shfl_xor_sync(0xffffffffu, n_tiny, o);
         if (lane == 0) {
-            const int cd = (nf ? 1 : 0) | (n_tiny << 1);
-            e[sg] = ex;
-            code[sg] = cd;
-            if (cd) cand[atomicAdd(fix + kFixCand, 1u)] = (int32_t)sg;
+            e[sg] = tc_exponent(m);
+            code[sg] = nf ? 1 : 0;
             atomicMax(fix + kFixSegL1, __float_as_uint(sum));
             atomicMax(fix + kFixSegMax, __float_as_uint(m));
         }
     }
 }
 
+// Segments with a nonzero code (an inf or NaN, or tiny values) become
+// candidates for the exact recomputation.
+__global__ void k_tc_seg_cand(const int32_t* __restrict__ code, int64_t n_seg, int32_t* __restrict__ cand,
+                              uint32_t* __restrict__ fix) {
+    for (int64_t sg = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; sg < n_seg;
+         sg += (int64_t)gridDim.x * blockDim.x)
+        if (code[sg]) cand[atomicAdd(fix + kFixCand, 1u)] = (int32_t)sg;
+}
+
 // The values in tile order, scaled by their segment's power of two and
 // split into fp16 hi | lo << 16 (seg_of: rows for W's rows, cols for its
-// columns).
+// columns).  Each nonzero value below 2^-3 after scaling adds 2 to its
+// segment's code (the tiny count of tc_needs_exact).
 __global__ void k_tc_values(const float* __restrict__ v, const int32_t* __restrict__ perm_t,
                             const int32_t* __restrict__ seg_of, const int32_t* __restrict__ seg_exp, int64_t n,
-                            uint32_t* __restrict__ hl) {
+                            uint32_t* __restrict__ hl, int32_t* __restrict__ code) {
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
         const int32_t k = perm_t[j];
         const float x = v[k];
+        const int32_t sg = seg_of[k];
+        const int ex = seg_exp[sg];   // in [-120, 120]: 2^ex and 2^(-3-ex) are normal floats
+        const float ax = fabsf(x);
+        if (ax > 0.f && ax < __int_as_float((124 - ex) << 23)) atomicAdd(code + sg, 2);
         __half h, l;
         // an inf or NaN flags its segment for the exact recomputation; the
         // tile holds a zero in its place
-        split16(isfinite(x) ? x * ldexpf(1.f, seg_exp[seg_of[k]]) : 0.f, h, l);
+        split16(isfinite(x) ? x * __int_as_float((127 + ex) << 23) : 0.f, h, l);
         hl[j] = (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(l) << 16);
     }
 }
@@ -1494,10 +1496,11 @@ int run_tc(Layer* L, bool columns, const float* D, int64_t b, const float* bias,
     const int TH = 256;
     if (cudaMemsetAsync(T->fix, 0, kFixWords * sizeof(uint32_t), s) != cudaSuccess) return SNK_ERR_CUDA;
     k_tc_seg_exp<<<grid_for(n_seg * 32, TH, L->num_sms), TH, 0, s>>>(
-        columns ? L->col_ptr : L->row_ptr, L->v, columns ? L->perm : nullptr, n_seg, T->seg_exp,
-        T->seg_code, T->cand, T->fix);
+        columns ? L->col_ptr : L->row_ptr, L->v, columns ? L->perm : nullptr, n_seg, T->seg_exp, T->seg_code,
+        T->fix);
     k_tc_values<<<grid_for(L->nnz, TH, L->num_sms), TH, 0, s>>>(L->v, V.perm_t, columns ? L->c : L->r,
-                                                                T->seg_exp, L->nnz, T->hl);
+                                                                T->seg_exp, L->nnz, T->hl, T->seg_code);
+    k_tc_seg_cand<<<grid_for(n_seg, TH, L->num_sms), TH, 0, s>>>(T->seg_code, n_seg, T->cand, T->fix);
     if (cudaFuncSetAttribute(k_tc_spmm, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
         return SNK_ERR_CUDA;
     const bool vec = (k_len % 4) == 0 && ((uintptr_t)D & 15) == 0;

@@ -67,11 +67,13 @@ def test_rule(monkeypatch):
 #          795 = 5 waves + 35 (4 ways)
 @pytest.mark.parametrize("b,chunks,shared", [(256, 1, 0), (4096, 1, 1), (4097, 1, 0), (10_000, 2, 2)])
 def test_launch_counts(b, chunks, shared):
-    # forward / dX: segment scales and tile-order values once, then a split,
-    # a product and an exact-row kernel per chunk of kTcChunk rows (plus the
-    # partial-sum kernel where tiles are shared), and one exact-segment kernel
+    # forward / dX: segment scales, tile-order values (with the count of
+    # tiny values) and the candidate list once, then a split, a product
+    # and an exact-row kernel per chunk of kTcChunk rows (plus the partial-sum
+    # kernel where tiles are shared), and one exact-segment kernel
     assert chunks == -(-b // bench.TC_CHUNK)
-    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 3 + 3 * chunks + shared
+    assert bench.tc_launches("fwd", 10_000, 10_000, b) == 4 + 3 * chunks + shared
+    assert bench.tc_launches("dx", 10_000, 10_000, b) == 4 + 3 * chunks + shared
     # dW: two column passes, a flag decision, two transposes and a product
     # kernel per chunk, then one exact-entry kernel; the chunk is what the
     # shared fp16 workspace holds for both operands
