@@ -69,6 +69,8 @@ def _check(torch, lay, X, dY, bias, rows=None, weight=True):
     (1000, 700, 99, 300),     # sparse windows: stages cleared entry by entry, not by bulk copy
     (2000, 1500, 90, 2560),   # more output tiles than SMs (152): the last partial wave's
                               # tiles shared 2 ways (forward, 220 tiles) and 8 ways (dX, 160)
+    (1000, 700, 90, 8192),    # forward: 384 tiles, two full waves and 80 tiles one per CTA
+    (192, 4000, 90, 128),     # forward: one tile of 63 windows shared 8 ways
 ])
 def test_forced_small_shapes(torch, monkeypatch, out_f, in_f, sp, b):
     monkeypatch.setenv("SNK_LARGE_BATCH", "on")
