@@ -320,7 +320,9 @@ const char* snk_status_string(int status);
  * the large-batch path (above) bound every wait of their pipeline (about two
  * seconds).  A wait that runs out stops that kernel: it waits for the copies
  * and tensor-core operations it has already issued, writes NaN to every
- * output it owns (Y or dX entries, or the dW entries of its block), and
+ * output it owns (Y or dX entries, or the dW entries of its blocks of W:
+ * a weight-gradient warp whose wait ran out writes NaN to its share of the
+ * CTA's current block and of every later one), and
  * records the event in the handle's device status word.  The product calls
  * are asynchronous and cannot return that record themselves; this call
  * synchronises `stream`, reads the word and clears it.  No page has a
