@@ -109,6 +109,18 @@ def test_default_dispatch_weight_gradient(torch, monkeypatch):
     g.close()
 
 
+@pytest.mark.parametrize("b", [95, 96])
+def test_first_tier_boundary(torch, monkeypatch, b):
+    """2000 x 1500 at 90% (10% stored): 95 rows run batch-tiled, 96 on the
+    tensor cores (the first tier); both meet the contract."""
+    monkeypatch.delenv("SNK_LARGE_BATCH", raising=False)
+    lay = synth.make_layer(2000, 1500, 90, 0.05, 161, 162)
+    X = synth.normal((b, 1500), 1.0, 163)
+    dY = synth.normal((b, 2000), 1.0, 164)
+    bias = synth.normal(2000, 0.1, 165)
+    _check(torch, lay, X, dY, bias)
+
+
 @pytest.mark.parametrize("b", [1300, 4300])
 def test_weight_gradient_blocks_per_cta(torch, monkeypatch, b):
     """dW and db at 3000 x 2900, 90%: 24 x 16 = 384 blocks of W, two or
