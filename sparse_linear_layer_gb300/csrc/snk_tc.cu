@@ -1095,7 +1095,11 @@ __global__ void k_tc_tsplit(const float* __restrict__ D, int64_t rows, int64_t n
 __global__ void k_tc_seg_exp(const int32_t* __restrict__ ptr, const float* __restrict__ v,
                              const int32_t* __restrict__ perm, int64_t n_seg, int32_t* __restrict__ e,
                              int32_t* __restrict__ code, uint32_t* __restrict__ fix) {
-    const int lane = threadIdx.x & 31;
+    __shared__ float red[2][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    // the block's largest segment sum and magnitude, sent once per block: one
+    // atomic per segment on the same two words serialised in the L2
+    float m_run = 0.f, s_run = 0.f;
     for (int64_t sg = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; sg < n_seg;
          sg += ((int64_t)gridDim.x * blockDim.x) >> 5) {
         const int k0 = ptr[sg], k1 = ptr[sg + 1];
@@ -1119,9 +1123,22 @@ __global__ void k_tc_seg_exp(const int32_t* __restrict__ ptr, const float* __res
         if (lane == 0) {
             e[sg] = tc_exponent(m);
             code[sg] = nf ? 1 : 0;
-            atomicMax(fix + kFixSegL1, __float_as_uint(sum));
-            atomicMax(fix + kFixSegMax, __float_as_uint(m));
         }
+        m_run = fmaxf(m_run, m);
+        s_run = fmaxf(s_run, sum);
+    }
+    if (lane == 0) {
+        red[0][w] = s_run;
+        red[1][w] = m_run;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < (int)(blockDim.x >> 5); ++i) {
+            s_run = fmaxf(s_run, red[0][i]);
+            m_run = fmaxf(m_run, red[1][i]);
+        }
+        atomicMax(fix + kFixSegL1, __float_as_uint(s_run));
+        atomicMax(fix + kFixSegMax, __float_as_uint(m_run));
     }
 }
 
